@@ -1,0 +1,24 @@
+"""CPU oracle for the MXFP4 MoE expert FFN (test infrastructure).
+
+This package is the plain, slow, float64 CPU statement of what the hot path computes.
+It is test infrastructure: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference leg of ``bench.py`` may import or run it. The product path (the
+C-ABI library and its Python binding) never imports it, and it never imports them.
+"""
+from .mxfp4_oracle import (  # noqa: F401
+    act_quant_mxfp4,
+    bf16_bits_from_f64,
+    bf16_bits_to_f64,
+    e2m1_decode,
+    e4m3fn_decode,
+    e8m0_decode,
+    fp8_block_dequant_128x128,
+    mxfp4_dequant,
+    mxfp4_gemm_blockint,
+    mxfp4_gemm_bf16,
+    mxfp4_values,
+    moe_forward,
+    moe_route,
+    moe_flops_per_pair,
+    unpack_nibbles,
+)

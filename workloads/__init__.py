@@ -1,0 +1,15 @@
+"""Seeded synthetic inputs for the MXFP4 MoE expert FFN.
+
+This module is shared by the CUDA-path tests, ``bench.py`` and the oracle tests. It
+holds none of the method's arithmetic: it draws random bytes, normals and routing
+choices, and converts the float32 draws to the bfloat16 bit patterns that are the
+method's input dtype.
+"""
+from .generators import (  # noqa: F401
+    CONFIGS,
+    MoEInputs,
+    f32_to_bf16_bits,
+    make_config_inputs,
+    make_dequant_inputs,
+    make_moe_inputs,
+)
