@@ -1,0 +1,20 @@
+"""GB300 (sm_103a) MXFP4 mixture-of-experts expert FFN.
+
+The compute path is the C-ABI library ``libmxfp4moe.so`` (hand-written CUDA: tcgen05
+block-scaled grouped GEMM, routing, MX quantiser, combine, dequant kernels); this package
+only builds it (``build.build()``) and marshals torch tensors into its calls.
+"""
+from ._native import (  # noqa: F401
+    MXError,
+    act_quant_mxfp4,
+    device_status,
+    fp8_block_dequant_128x128,
+    lib,
+    library_path,
+    moe_mxfp4_forward,
+    moe_mxfp4_route,
+    moe_mxfp4_workspace_size,
+    mxfp4_dequant,
+    mxfp4_gemm_bf16,
+    status_string,
+)

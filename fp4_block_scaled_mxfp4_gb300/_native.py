@@ -1,0 +1,194 @@
+"""Thin ctypes binding of the C ABI in include/mxfp4moe.h (argument marshalling only).
+
+Every function takes torch CUDA tensors, checks dtype / shape / contiguity, passes raw
+device pointers and sizes to the library, and raises ``MXError`` on a non-zero status.
+All arithmetic runs in the library's CUDA kernels; there is no CPU or PyTorch fallback:
+if ``libmxfp4moe.so`` is missing or cannot be loaded every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4moe.so")
+_lib: Optional[ctypes.CDLL] = None
+
+_c_i64 = ctypes.c_int64
+_c_ptr = ctypes.c_void_p
+
+# name -> (restype, argtypes)
+_SIGNATURES = {
+    "mx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mx_version": (ctypes.c_int, []),
+    "mx_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "mxfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "fp8_block_dequant_128x128": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "act_quant_mxfp4": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "mxfp4_gemm_bf16": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_ptr]),
+    "moe_mxfp4_workspace_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
+    "moe_mxfp4_forward": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                         _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
+                                         _c_ptr]),
+    "moe_mxfp4_route": (ctypes.c_int, [_c_ptr, _c_i64, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                       ctypes.c_size_t, _c_ptr]),
+}
+
+MX_OK = 0
+
+
+class MXError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call} failed: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmxfp4moe.so (once). Raises if it is missing: there is no fallback path."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libmxfp4moe.so is not built ({_LIB_PATH}); run "
+                               "fp4_block_scaled_mxfp4_gb300.build.build() first")
+        handle = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mx_status_string(int(status)).decode()
+
+
+def _check(status: int, call: str) -> None:
+    if status != MX_OK:
+        raise MXError(status, call)
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+
+
+def _bf16_like(t):
+    import torch
+    return t.dtype in (torch.bfloat16, torch.uint16, torch.int16)
+
+
+def mxfp4_dequant(codes, sf, out, stream=None) -> None:
+    """out[r, c] = bf16(E2M1(codes) * 2^(sf - 127)); codes u8 [R, C/2], sf u8 [R, C/32], out [R, C]."""
+    import torch
+    R, half = codes.shape
+    C = 2 * half
+    _need(codes, torch.uint8, (R, half), "codes")
+    _need(sf, torch.uint8, (R, C // 32), "sf")
+    if not _bf16_like(out):
+        raise ValueError("out must be bfloat16 (or its 16-bit bit pattern)")
+    _need(out, out.dtype, (R, C), "out")
+    _check(lib().mxfp4_dequant(_ptr(codes), _ptr(sf), _ptr(out), R, C, _stream(stream)), "mxfp4_dequant")
+
+
+def fp8_block_dequant_128x128(q, sf, out, stream=None) -> None:
+    """out = bf16(e4m3(q) * 2^(sf[i/128, j/128] - 127)); q u8 [R, C], sf u8 [ceil(R/128), ceil(C/128)]."""
+    import torch
+    R, C = q.shape
+    _need(q, q.dtype, (R, C), "q")
+    if q.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError("q must be uint8 or float8_e4m3fn")
+    _need(sf, sf.dtype, ((R + 127) // 128, (C + 127) // 128), "sf")
+    _need(out, out.dtype, (R, C), "out")
+    _check(lib().fp8_block_dequant_128x128(_ptr(q), _ptr(sf), _ptr(out), R, C, _stream(stream)),
+           "fp8_block_dequant_128x128")
+
+
+def act_quant_mxfp4(x, codes, sf, stream=None) -> None:
+    """MX quantisation of BF16 x [M, K] into codes u8 [M, K/2] and E8M0 scales u8 [M, K/32]."""
+    import torch
+    M, K = x.shape
+    _need(x, x.dtype, (M, K), "x")
+    _need(codes, torch.uint8, (M, K // 2), "codes")
+    _need(sf, torch.uint8, (M, K // 32), "sf")
+    _check(lib().act_quant_mxfp4(_ptr(x), _ptr(codes), _ptr(sf), M, K, _stream(stream)), "act_quant_mxfp4")
+
+
+def mxfp4_gemm_bf16(a, sa, b, sb, d, stream=None) -> None:
+    """d = bf16(A . B^T) for MXFP4 A [M, K] (a u8 [M, K/2], sa [M, K/32]) and B [N, K]."""
+    import torch
+    M, half = a.shape
+    N = b.shape[0]
+    K = 2 * half
+    _need(a, torch.uint8, (M, half), "a")
+    _need(sa, torch.uint8, (M, K // 32), "sa")
+    _need(b, torch.uint8, (N, half), "b")
+    _need(sb, torch.uint8, (N, K // 32), "sb")
+    _need(d, d.dtype, (M, N), "d")
+    _check(lib().mxfp4_gemm_bf16(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(d), M, N, K, _stream(stream)),
+           "mxfp4_gemm_bf16")
+
+
+def moe_mxfp4_workspace_size(T: int, H: int, I: int, E: int, K: int, routed: bool = True) -> int:
+    return int(lib().moe_mxfp4_workspace_size(T, H, I, E, K, 1 if routed else 0))
+
+
+def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, stream=None) -> None:
+    """MoE expert FFN over MXFP4 weights; topk_ids/topk_w None selects the shared expert."""
+    import torch
+    T, H = x.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    K = topk_ids.shape[1] if topk_ids is not None else 1
+    _need(x, x.dtype, (T, H), "x")
+    if topk_ids is not None:
+        _need(topk_ids, torch.int32, (T, K), "topk_ids")
+        _need(topk_w, torch.float32, (T, K), "topk_w")
+    _need(w13, torch.uint8, (E, 2 * I, H // 2), "w13")
+    _need(s13, torch.uint8, (E, 2 * I, H // 32), "s13")
+    _need(w2, torch.uint8, (E, H, I // 2), "w2")
+    _need(s2, torch.uint8, (E, H, I // 32), "s2")
+    _need(out, out.dtype, (T, H), "out")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().moe_mxfp4_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2),
+                                   _ptr(s2), _ptr(out), T, H, I, E, K, _ptr(workspace), ws_bytes,
+                                   _stream(stream)), "moe_mxfp4_forward")
+
+
+def moe_mxfp4_route(topk_ids, E: int, counts, offsets, row_of, workspace, stream=None) -> None:
+    """Routing permutation only: counts [E], offsets [E+1], row_of [T, K] (int32)."""
+    import torch
+    T, K = topk_ids.shape
+    _need(topk_ids, torch.int32, (T, K), "topk_ids")
+    _need(counts, torch.int32, (E,), "counts")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(row_of, torch.int32, (T, K), "row_of")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().moe_mxfp4_route(_ptr(topk_ids), T, K, E, _ptr(counts), _ptr(offsets), _ptr(row_of),
+                                 _ptr(workspace), ws_bytes, _stream(stream)), "moe_mxfp4_route")
+
+
+def device_status(clear: bool = True) -> int:
+    """Synchronise and return the device status word as a status code (0 = MX_OK)."""
+    return int(lib().mx_device_status(1 if clear else 0))

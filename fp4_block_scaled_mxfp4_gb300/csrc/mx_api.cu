@@ -1,0 +1,376 @@
+// mx_api.cu -- the C ABI (include/mxfp4moe.h): argument validation, workspace layout,
+// TMA tensor-map encoding and the launch sequence of each call. No device memory is
+// allocated here; every launch goes to the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mxfp4moe.h"
+#include "mx_internal.h"
+
+namespace mx {
+
+// Device status word (one per device): bounded device-side waits OR an error code in.
+__device__ uint32_t g_mx_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int num_sms = 0;
+    uint32_t* status = nullptr;
+    bool ready = false;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MX_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_mx_status) != cudaSuccess) return MX_ERR_CUDA;
+        d.status = static_cast<uint32_t*>(p);
+        if (g_encode == nullptr) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return MX_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return MX_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D uint8 tensor [rows, inner_bytes] read in boxes of [box_rows, 128 bytes], 128-byte swizzle.
+int make_tmap(CUtensorMap* m, const void* base, int64_t inner_bytes, int64_t rows, uint32_t box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)inner_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)inner_bytes};
+    cuuint32_t box[2] = {128u, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace layout shared by moe_mxfp4_forward and moe_mxfp4_route.
+struct WsLayout {
+    int64_t R = 0, nchunks = 0, max_mtiles = 0;
+    size_t num_mtiles = 0, counts = 0, offsets = 0, chunk_counts = 0, chunk_base = 0, local_rank = 0,
+           row_of = 0, tile_expert = 0, tile_row0 = 0, tile_rows = 0, xq = 0, xs = 0, hq = 0, hs = 0, y = 0,
+           total = 0;
+};
+
+WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool routed) {
+    WsLayout L;
+    L.R = routed ? T * K : T;
+    L.nchunks = routed ? (L.R + kRouteChunk - 1) / kRouteChunk : 0;
+    L.max_mtiles = (L.R + kBM - 1) / kBM + (routed ? E : 0);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align256(off + bytes);
+        return at;
+    };
+    L.num_mtiles = take(16);
+    if (routed) {
+        L.counts = take(4 * (size_t)E);
+        L.offsets = take(4 * (size_t)(E + 1));
+        L.chunk_counts = take(4 * (size_t)(L.nchunks * E));
+        L.chunk_base = take(4 * (size_t)(L.nchunks * E));
+        L.local_rank = take(4 * (size_t)L.R);
+        L.row_of = take(4 * (size_t)L.R);
+        L.tile_expert = take(4 * (size_t)L.max_mtiles);
+        L.tile_row0 = take(4 * (size_t)L.max_mtiles);
+        L.tile_rows = take(4 * (size_t)L.max_mtiles);
+    }
+    L.xq = take((size_t)L.R * (size_t)(H / 2));
+    L.xs = take((size_t)L.R * (size_t)(H / 32));
+    L.hq = take((size_t)L.R * (size_t)(I / 2));
+    L.hs = take((size_t)L.R * (size_t)(I / 32));
+    if (routed) L.y = take((size_t)L.R * (size_t)H * 2);
+    L.total = off;
+    return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+RouteBufs route_bufs(void* ws, const WsLayout& L) {
+    RouteBufs rb;
+    rb.chunk_counts = at<int32_t>(ws, L.chunk_counts);
+    rb.chunk_base = at<int32_t>(ws, L.chunk_base);
+    rb.local_rank = at<int32_t>(ws, L.local_rank);
+    rb.counts = at<int32_t>(ws, L.counts);
+    rb.offsets = at<int32_t>(ws, L.offsets);
+    rb.row_of = at<int32_t>(ws, L.row_of);
+    rb.tile_expert = at<int32_t>(ws, L.tile_expert);
+    rb.tile_row0 = at<int32_t>(ws, L.tile_row0);
+    rb.tile_rows = at<int32_t>(ws, L.tile_rows);
+    rb.num_mtiles = at<int32_t>(ws, L.num_mtiles);
+    rb.nchunks = L.nchunks;
+    return rb;
+}
+
+int check_moe_dims(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool routed) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0) return MX_ERR_INVALID_ARG;
+    if (routed && K <= 0) return MX_ERR_INVALID_ARG;
+    if (H % 128 || I % 128) return MX_ERR_UNSUPPORTED;
+    if (E > kMaxExperts || (routed && K > kMaxTopK)) return MX_ERR_UNSUPPORTED;
+    if (!routed && E != 1) return MX_ERR_INVALID_ARG;
+    if (H >= (int64_t)1 << 24 || I >= (int64_t)1 << 24) return MX_ERR_UNSUPPORTED;
+    const int64_t R = routed ? T * K : T;
+    if (R >= ((int64_t)1 << 31) - (int64_t)kBM * (E + 1)) return MX_ERR_UNSUPPORTED;
+    if (E * 2 * I >= ((int64_t)1 << 31) || E * H >= ((int64_t)1 << 31)) return MX_ERR_UNSUPPORTED;
+    return MX_OK;
+}
+
+// Fill the GEMM arguments shared by L1 and L2.
+GemmArgs base_args(const uint8_t* sfa, const uint8_t* sfb, int64_t K, int64_t a_rows, int64_t b_rows,
+                   uint32_t* status) {
+    GemmArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.sfa = sfa;
+    g.sfb = sfb;
+    g.ld_sf = K / 32;
+    g.a_rows = a_rows;
+    g.b_rows = b_rows;
+    g.k_tiles = (int32_t)((K + kBK - 1) / kBK);
+    g.k_tail_half = (K % kBK) != 0 ? 1 : 0;
+    g.status = status;
+    return g;
+}
+
+int grid_for(int64_t work, int num_sms) {
+    int64_t g = work < num_sms ? work : num_sms;
+    return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" {
+
+const char* mx_status_string(int s) {
+    switch (s) {
+        case MX_OK: return "MX_OK";
+        case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG";
+        case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
+        case MX_ERR_MISALIGNED: return "MX_ERR_MISALIGNED";
+        case MX_ERR_WORKSPACE: return "MX_ERR_WORKSPACE";
+        case MX_ERR_CUDA: return "MX_ERR_CUDA";
+        case MX_ERR_DEVICE_TIMEOUT: return "MX_ERR_DEVICE_TIMEOUT";
+        default: return "MX_ERR_UNKNOWN";
+    }
+}
+
+int mx_version(void) { return 100; }
+
+int mx_device_status(int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return MX_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_mx_status, sizeof(v)) != cudaSuccess) return MX_ERR_CUDA;
+    if (clear) {
+        const uint32_t z = 0;
+        if (cudaMemcpyToSymbol(g_mx_status, &z, sizeof(z)) != cudaSuccess) return MX_ERR_CUDA;
+    }
+    return v ? MX_ERR_DEVICE_TIMEOUT : MX_OK;
+}
+
+int mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, void* out_bf16, int64_t rows, int64_t cols,
+                  mx_stream_t stream) {
+    if (rows < 0 || cols <= 0) return MX_ERR_INVALID_ARG;
+    if (cols % 32) return MX_ERR_UNSUPPORTED;
+    if (rows == 0) return MX_OK;
+    if (!codes || !sf || !out_bf16) return MX_ERR_INVALID_ARG;
+    if (!aligned16(codes) || !aligned16(out_bf16)) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_mxfp4_dequant(codes, sf, static_cast<uint16_t*>(out_bf16), rows, cols, d->num_sms,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_block_dequant_128x128(const uint8_t* q, const uint8_t* sf, void* out_bf16, int64_t rows, int64_t cols,
+                              mx_stream_t stream) {
+    if (rows < 0 || cols <= 0) return MX_ERR_INVALID_ARG;
+    if (cols % 16) return MX_ERR_UNSUPPORTED;
+    if (rows == 0) return MX_OK;
+    if (!q || !sf || !out_bf16) return MX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out_bf16)) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_fp8_dequant(q, sf, static_cast<uint16_t*>(out_bf16), rows, cols, d->num_sms,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int act_quant_mxfp4(const void* x_bf16, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K, mx_stream_t stream) {
+    if (M < 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (K % 32) return MX_ERR_UNSUPPORTED;
+    if (M == 0) return MX_OK;
+    if (!x_bf16 || !codes || !sf) return MX_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(codes)) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_act_quant(static_cast<const uint16_t*>(x_bf16), codes, sf, M, K, d->num_sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb, void* d_bf16,
+                    int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (K % 128 || N % 16) return MX_ERR_UNSUPPORTED;
+    if (M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 24)) return MX_ERR_UNSUPPORTED;
+    if (M == 0) return MX_OK;
+    if (!a || !sa || !b || !sb || !d_bf16) return MX_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(sa) || !aligned16(sb) || !aligned16(d_bf16))
+        return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    CUtensorMap ta, tb;
+    if (make_tmap(&ta, a, K / 2, M, 128) || make_tmap(&tb, b, K / 2, N, 256)) return MX_ERR_CUDA;
+    GemmArgs g = base_args(sa, sb, K, M, N, d->status);
+    g.num_mtiles_host = (int32_t)((M + kBM - 1) / kBM);
+    g.m_total = M;
+    g.n_tiles = (int32_t)((N + kBN - 1) / kBN);
+    g.b_rows_per_expert = N;
+    g.n_valid = N;
+    g.y = static_cast<uint16_t*>(d_bf16);
+    g.ld_y = N;
+    return cuda_status(launch_gemm_l2(ta, tb, g, grid_for((int64_t)g.num_mtiles_host * g.n_tiles, d->num_sms),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_mxfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed) {
+    if (check_moe_dims(T, H, I, E, K, routed != 0) != MX_OK) return 0;
+    return ws_layout(T, H, I, E, K, routed != 0).total;
+}
+
+int moe_mxfp4_route(const int32_t* topk_ids, int64_t T, int64_t K, int64_t E, int32_t* counts, int32_t* offsets,
+                    int32_t* row_of, void* workspace, size_t ws_bytes, mx_stream_t stream) {
+    if (T < 0 || K <= 0 || E <= 0) return MX_ERR_INVALID_ARG;
+    if (E > kMaxExperts || K > kMaxTopK) return MX_ERR_UNSUPPORTED;
+    if (T * K >= ((int64_t)1 << 31) - (int64_t)kBM * (E + 1)) return MX_ERR_UNSUPPORTED;
+    if (!counts || !offsets || !row_of) return MX_ERR_INVALID_ARG;
+    if (T > 0 && !topk_ids) return MX_ERR_INVALID_ARG;
+    // the routing part of the forward's workspace; H = I = 128 keeps the size check simple
+    const WsLayout L = ws_layout(T, 128, 128, E, K, true);
+    if (!workspace || ws_bytes < L.total) return MX_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    RouteBufs rb = route_bufs(workspace, L);
+    rb.counts = counts;
+    rb.offsets = offsets;
+    rb.row_of = row_of;
+    if (T == 0) {
+        if (cudaMemsetAsync(counts, 0, 4 * (size_t)E, s) != cudaSuccess) return MX_ERR_CUDA;
+        return cuda_status(cudaMemsetAsync(offsets, 0, 4 * (size_t)(E + 1), s));
+    }
+    if (cudaError_t e = launch_route(topk_ids, T, K, E, rb, s)) return MX_ERR_CUDA;
+    // row_of needs the gather pass; run it without writing activations (H = 0 columns)
+    return cuda_status(launch_quant_gather(nullptr, topk_ids, T, K, E, 0, rb, nullptr, nullptr, s));
+}
+
+int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                      const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T, int64_t H,
+                      int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream) {
+    const bool routed = topk_ids != nullptr;
+    if (routed != (topk_w != nullptr)) return MX_ERR_INVALID_ARG;
+    if (int e = check_moe_dims(T, H, I, E, K, routed)) return e;
+    if (T == 0) return MX_OK;
+    if (!x || !w13 || !s13 || !w2 || !s2 || !out) return MX_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w13) || !aligned16(s13) || !aligned16(w2) || !aligned16(s2) ||
+        !aligned16(out))
+        return MX_ERR_MISALIGNED;
+    const WsLayout L = ws_layout(T, H, I, E, K, routed);
+    if (!workspace || ws_bytes < L.total) return MX_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* xq = at<uint8_t>(workspace, L.xq);
+    uint8_t* xs = at<uint8_t>(workspace, L.xs);
+    uint8_t* hq = at<uint8_t>(workspace, L.hq);
+    uint8_t* hs = at<uint8_t>(workspace, L.hs);
+    const int64_t R = L.R;
+
+    GemmArgs g1 = base_args(xs, s13, H, R, E * 2 * I, d->status);
+    GemmArgs g2 = base_args(hs, s2, I, R, E * H, d->status);
+    RouteBufs rb{};
+    if (routed) {
+        rb = route_bufs(workspace, L);
+        if (launch_route(topk_ids, T, K, E, rb, s) != cudaSuccess) return MX_ERR_CUDA;
+        if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s) != cudaSuccess)
+            return MX_ERR_CUDA;
+        for (GemmArgs* g : {&g1, &g2}) {
+            g->tile_expert = rb.tile_expert;
+            g->tile_row0 = rb.tile_row0;
+            g->tile_rows = rb.tile_rows;
+            g->num_mtiles_dev = rb.num_mtiles;
+        }
+    } else {
+        if (launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s) != cudaSuccess)
+            return MX_ERR_CUDA;
+        for (GemmArgs* g : {&g1, &g2}) {
+            g->num_mtiles_host = (int32_t)((T + kBM - 1) / kBM);
+            g->m_total = T;
+        }
+    }
+    const int64_t max_mtiles = L.max_mtiles;
+
+    // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
+    CUtensorMap ta1, tb1, ta2, tb2;
+    if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap(&tb1, w13, H / 2, E * 2 * I, 128)) return MX_ERR_CUDA;
+    g1.n_tiles = (int32_t)(I / 128);
+    g1.b_rows_per_expert = 2 * I;
+    g1.n_half = I;
+    g1.n_valid = I;
+    g1.hq = hq;
+    g1.hs = hs;
+    g1.ld_hq = I / 2;
+    g1.ld_hs = I / 32;
+    if (launch_gemm_l1(ta1, tb1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), s) != cudaSuccess)
+        return MX_ERR_CUDA;
+
+    // L2: [R, I] x [H, I]^T per expert, BF16 out (to `out` directly without routing).
+    if (make_tmap(&ta2, hq, I / 2, R, 128) || make_tmap(&tb2, w2, I / 2, E * H, 256)) return MX_ERR_CUDA;
+    g2.n_tiles = (int32_t)((H + kBN - 1) / kBN);
+    g2.b_rows_per_expert = H;
+    g2.n_valid = H;
+    g2.y = routed ? at<uint16_t>(workspace, L.y) : static_cast<uint16_t*>(out);
+    g2.ld_y = H;
+    if (launch_gemm_l2(ta2, tb2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), s) != cudaSuccess)
+        return MX_ERR_CUDA;
+
+    if (routed) {
+        if (launch_combine(at<uint16_t>(workspace, L.y), rb.row_of, topk_w, static_cast<uint16_t*>(out), T, K, H,
+                           d->num_sms, s) != cudaSuccess)
+            return MX_ERR_CUDA;
+    }
+    return MX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,328 @@
+// mx_device.cuh -- device-side building blocks for the sm_103a kernels: BF16 and MXFP4
+// element helpers, the MX quantiser, mbarrier / TMA / cp.async / tcgen05 wrappers written
+// as inline PTX, and bounded waits that report through a device status word.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+// ------------------------------------------------------------------------------------
+// Device status word (one per device, owned by the API layer and passed to each kernel).
+// Bounded waits OR a code into it and give up.
+// ------------------------------------------------------------------------------------
+enum : uint32_t {
+    kErrWaitFull = 1u << 0,
+    kErrWaitEmpty = 1u << 1,
+    kErrWaitTmemFull = 1u << 2,
+    kErrWaitTmemEmpty = 1u << 3,
+    kErrWaitDrain = 1u << 4,
+};
+
+// Upper bound on one wait, in globaltimer nanoseconds. Every legitimate wait in these
+// kernels resolves in microseconds; two seconds only fires when a pipeline is broken.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {
+    if (status != nullptr) atomicOr(status, code);
+}
+
+// ------------------------------------------------------------------------------------
+// BF16 helpers (bit patterns as uint16)
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Round to BF16, nearest-even; NaN -> 0x7FC0 with its sign.
+__device__ __forceinline__ uint32_t f32_to_bf16(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return ((u >> 16) & 0x8000u) | 0x7FC0u;
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ float round_bf16(float f) { return bf16_to_f32(f32_to_bf16(f)); }
+
+// ------------------------------------------------------------------------------------
+// MX quantiser: shared exponent and E2M1 code (round to nearest even, saturating at 6)
+// ------------------------------------------------------------------------------------
+// Scale byte for a finite amax >= 0: floor(log2 amax) - 2 + 127, clamped at 0. For a normal
+// float amax this is its biased exponent minus 2; zero and subnormals give 0.
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+    int be = (int)(__float_as_uint(amax) >> 23);
+    return (uint32_t)max(be - 2, 0);
+}
+
+// 2^(127 - E) as a float for E in [0, 252] (always a normal float).
+__device__ __forceinline__ float mx_inv_scale(uint32_t E) { return __uint_as_float((254u - E) << 23); }
+
+// E2M1 code of a scaled value v (sign in bit 3). Thresholds are the midpoints of the
+// E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}; at a midpoint the even code wins.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+    float a = fabsf(v);
+    uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+                 (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+                 (uint32_t)(a > 5.0f);
+    return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// Quantise 8 consecutive BF16 values held by one thread; four consecutive lanes hold one
+// 32-element block (so every lane of the warp must call this). Returns the 8 packed codes
+// (element 0 in the lowest nibble) and writes the block's scale byte to `scale_byte`.
+__device__ __forceinline__ uint32_t mx_quant8_quad(const uint4 xv, uint32_t& scale_byte) {
+    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+    float f[8];
+    float amax = 0.0f;
+    uint32_t bad = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
+        bad |= ((lo & 0x7F80u) == 0x7F80u) | ((hi & 0x7F80u) == 0x7F80u);
+        f[2 * i] = bf16_to_f32(lo);
+        f[2 * i + 1] = bf16_to_f32(hi);
+        amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, 1);
+    bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, 2);
+    uint32_t packed = 0;
+    if (bad) {
+        scale_byte = 255u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) packed |= (((__float_as_uint(f[i]) >> 28) & 8u) | 7u) << (4 * i);
+    } else {
+        const uint32_t E = mx_scale_byte(amax);
+        const float inv = mx_inv_scale(E);
+        scale_byte = E;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) packed |= e2m1_code(f[i] * inv) << (4 * i);
+    }
+    return packed;
+}
+
+// Quantise one 32-element block held entirely by this thread (float values that are
+// already BF16 numbers). Writes 16 bytes of codes and returns the scale byte.
+__device__ __forceinline__ uint32_t mx_quant32(const float (&f)[32], uint4& codes) {
+    float amax = 0.0f;
+    uint32_t bad = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        bad |= (uint32_t)((__float_as_uint(f[i]) & 0x7F800000u) == 0x7F800000u);
+        amax = fmaxf(amax, fabsf(f[i]));
+    }
+    uint32_t w[4] = {0, 0, 0, 0};
+    uint32_t E;
+    if (bad) {
+        E = 255u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i >> 3] |= (((__float_as_uint(f[i]) >> 28) & 8u) | 7u) << (4 * (i & 7));
+    } else {
+        E = mx_scale_byte(amax);
+        const float inv = mx_inv_scale(E);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i >> 3] |= e2m1_code(f[i] * inv) << (4 * (i & 7));
+    }
+    codes = make_uint4(w[0], w[1], w[2], w[3]);
+    return E;
+}
+
+// E2M1 magnitude values by code (device constant table used by the dequant kernels).
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+    // magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 built from the bit fields
+    uint32_t e = (code >> 1) & 3u, m = code & 1u;
+    float mag = (e == 0) ? 0.5f * (float)m : __uint_as_float(((126u + e) << 23) | (m << 22));
+    return (code & 8u) ? -mag : mag;
+}
+
+// 2^(b - 127) for an E8M0 byte b < 255 (b = 0 gives the float32 subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t b) {
+    return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// ------------------------------------------------------------------------------------
+// Shared-memory addresses and mbarriers
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity. Returns false when the CTA-wide abort
+// flag is raised or the time limit passes (then it raises the flag and sets `code`).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            uint64_t t = globaltimer();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                set_status(status, code);
+                return false;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor) and cp.async
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------
+// tcgen05: tensor memory, block-scaled MMA, copies and loads
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand tile written by TMA with 128-byte
+// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                 // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024u >> 4) << 32;      // stride byte offset: one 8 x 128 B swizzle atom
+    d |= (uint64_t)1 << 46;                 // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+    return d;
+}
+
+// Descriptor of a 32-row x 16-byte scale-factor block (no swizzle, rows 16 bytes apart,
+// 8-row groups 128 bytes apart), the source of a 32x128b tcgen05.cp.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor of kind::mxf4 block-scaled MMA: E2M1 A and B (K-major), E8M0
+// scales, FP32 accumulation implied by the kind, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
+    return idesc | (b_id << 4) | (a_id << 29);
+}
+
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Copy a 32-row x 128-bit block from shared memory into tensor memory, replicated into
+// all four 32-lane quarters.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive 32-bit columns of this warp's 32 lanes.
+__device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+}  // namespace mx

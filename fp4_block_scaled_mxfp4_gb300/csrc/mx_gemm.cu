@@ -1,0 +1,396 @@
+// mx_gemm.cu -- grouped block-scaled MXFP4 GEMM on the sm_103a tensor cores (tcgen05,
+// kind::mxf4, E2M1 x E2M1 with E8M0 scales per 32 elements of K, FP32 accumulation in
+// tensor memory), with the two epilogues of the expert FFN:
+//   L1: D = A . W13^T over a tile of 128 gate + 128 up columns; the epilogue rounds g and u
+//       to BF16, forms h = bf16(silu(g) * u) and re-quantises h to MXFP4 (codes + E8M0).
+//   L2: D = A . W2^T over 256 output columns; the epilogue writes BF16.
+// The pipeline is the one the pages describe for their CuTeDSL experts kernel ("Current
+// Bug: vLLM produces empty/garbage output", "Phase 1: CuTeDSL Shared Expert Kernel":
+// L1 GEMM -> SiLU -> re-quant -> L2 GEMM; the shared expert is the one-group case), with
+// the weight format of "2026-05-08 DeepSeek V4 Pro NVFP4 Quantization", "FP4 (E2M1) expert
+// weight format confirmed".
+//
+// CTA layout (384 threads, one CTA per SM, persistent over the tile list):
+//   warp 0      TMA producer: A tile (128 rows x 128 B) and B tile (256 rows x 128 B) per
+//               K stage of 256 elements, 128-byte swizzle, into a 4-stage ring.
+//   warp 1      allocates 512 TMEM columns; lane 0 moves the stage's scale factors from
+//               shared to tensor memory (tcgen05.cp) and issues 4 MMAs of K = 64.
+//   warps 2, 3  scale-factor loaders for A and B: cp.async from the plain row-major
+//               [rows, K/32] scale tensors into the 32-lane x 16-byte blocks tcgen05.cp reads.
+//   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, each owning half of the
+//               columns; they drain the accumulator to registers, release it, then compute.
+// TMEM: columns [0, 256) accumulator; [256 + 24 s, 256 + 24 s + 24) the scale factors of
+// stage s (A: 2 K-words x 4 columns, B: 2 K-words x 8 columns).
+#include <cuda.h>
+
+#include "mx_device.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+
+namespace {
+
+constexpr int kABytes = kBM * kBK / 2;                 // 16 KB
+constexpr int kBBytes = kBN * kBK / 2;                 // 32 KB
+constexpr int kSfaBytes = 2 * 512;                     // 2 K-words x (32 lanes x 16 B)
+constexpr int kSfbBytes = 2 * 2 * 512;                 // 2 K-words x 2 row groups of 128
+constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 51 KB, 1024-aligned
+constexpr int kTmemCols = 512;
+constexpr int kSfTmemBase = 256;
+constexpr int kSfColsPerStage = 24;
+constexpr int kSfLag = kStages - 1;                    // scale stages in flight per loader
+constexpr uint32_t kIdesc = idesc_mxf4(kBM, kBN);
+static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+
+struct Ctl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tmem_full;
+    uint64_t tmem_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + sizeof(Ctl) + 1024;
+
+struct Tile {
+    int32_t expert;
+    int32_t rows;
+    int64_t row0;
+};
+
+__device__ __forceinline__ int num_mtiles(const GemmArgs& a) {
+    return a.num_mtiles_dev ? *a.num_mtiles_dev : a.num_mtiles_host;
+}
+
+__device__ __forceinline__ Tile get_tile(const GemmArgs& a, int mt) {
+    Tile t;
+    if (a.tile_expert != nullptr) {
+        t.expert = a.tile_expert[mt];
+        t.row0 = a.tile_row0[mt];
+        t.rows = a.tile_rows[mt];
+    } else {
+        t.expert = 0;
+        t.row0 = (int64_t)mt * kBM;
+        const int64_t left = a.m_total - t.row0;
+        t.rows = (int32_t)(left < kBM ? left : kBM);
+    }
+    return t;
+}
+
+// First row (in the stacked B tensor) of B tile rows [h*128, h*128 + 128).
+template <bool kL1>
+__device__ __forceinline__ int64_t b_row(const GemmArgs& a, int expert, int nt, int h) {
+    if (kL1) return (int64_t)expert * a.b_rows_per_expert + (h ? a.n_half : 0) + (int64_t)nt * 128;
+    return (int64_t)expert * a.b_rows_per_expert + (int64_t)nt * kBN + h * 128;
+}
+
+// Every lane polls; the warp proceeds only if all lanes saw the phase complete, so an
+// abort never splits a warp between two code paths.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status, uint32_t code) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, status, code)) != 0;
+}
+
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+
+template <bool kL1>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)kStages * kStageBytes);
+    volatile int* abort_flag = &ctl->abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 3);   // TMA producer + two scale loaders
+            mbar_init(smem_u32(&ctl->empty[s]), 1);  // MMA commit
+        }
+        mbar_init(smem_u32(&ctl->tmem_full), 1);
+        mbar_init(smem_u32(&ctl->tmem_empty), 8);    // one arrive per epilogue warp
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+
+    const int total = num_mtiles(args) * args.n_tiles;
+    const int k_tiles = args.k_tiles;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int w = blockIdx.x; w < total; w += gridDim.x) {
+                const Tile t = get_tile(args, w / args.n_tiles);
+                const int nt = w % args.n_tiles;
+                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                    if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status, kErrWaitEmpty))
+                        goto producer_done;
+                    const uint32_t st = sbase + s * kStageBytes;
+                    const uint32_t bar = smem_u32(&ctl->full[s]);
+                    mbar_arrive_expect_tx(bar, kABytes + kBBytes);
+                    tma_load_2d(st, &tmA, kt * (kBK / 2), (int32_t)t.row0, bar);
+                    if (kL1) {
+                        tma_load_2d(st + kABytes, &tmB, kt * (kBK / 2), (int32_t)b_row<true>(args, t.expert, nt, 0), bar);
+                        tma_load_2d(st + kABytes + kBBytes / 2, &tmB, kt * (kBK / 2),
+                                    (int32_t)b_row<true>(args, t.expert, nt, 1), bar);
+                    } else {
+                        tma_load_2d(st + kABytes, &tmB, kt * (kBK / 2), (int32_t)b_row<false>(args, t.expert, nt, 0), bar);
+                    }
+                }
+            }
+            // Tail: wait for the MMA commits that release the last stages, so no
+            // asynchronous arrive reaches this CTA's shared memory after it exits.
+            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i) {
+                if (!mbar_wait(smem_u32(&ctl->empty[i % kStages]), (i / kStages) & 1u, abort_flag, args.status,
+                               kErrWaitEmpty))
+                    break;
+            }
+        producer_done:
+            if (*abort_flag) __nanosleep(20000);   // let copies already in flight land
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        uint32_t it = 0, tc = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            if (!warp_wait(smem_u32(&ctl->tmem_empty), (tc & 1u) ^ 1u, abort_flag, args.status, kErrWaitTmemEmpty))
+                break;
+            tc_fence_after();
+            bool ok = true;
+            for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                if (!warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag, args.status, kErrWaitFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const bool half = args.k_tail_half && (kt == k_tiles - 1);
+                    const int nwords = half ? 1 : 2;
+                    const int nmma = half ? 2 : 4;
+                    const uint32_t st = sbase + s * kStageBytes;
+                    const uint32_t sfa_s = st + kABytes + kBBytes;
+                    const uint32_t sfb_s = sfa_s + kSfaBytes;
+                    const uint32_t sfa_t = tmem + kSfTmemBase + s * kSfColsPerStage;
+                    const uint32_t sfb_t = sfa_t + 8;
+                    for (int wd = 0; wd < nwords; ++wd) {
+                        tc_cp_32x128b_x4(sfa_t + 4 * wd, desc_sf(sfa_s + wd * 512));
+                        tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 1024));
+                        tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + wd * 1024 + 512));
+                    }
+                    const uint64_t adesc = desc_sw128(st);
+                    const uint64_t bdesc = desc_sw128(st + kABytes);
+                    for (int j = 0; j < nmma; ++j) {
+                        const uint32_t id = 2u * (j & 1);
+                        // advance 64 E2M1 elements (32 bytes) along K inside the swizzle atom
+                        tc_mma_mxf4(tmem, adesc + (uint64_t)(2 * j), bdesc + (uint64_t)(2 * j),
+                                    idesc_with_sf_ids(kIdesc, id, id), sfa_t + 4 * (j >> 1),
+                                    sfb_t + 8 * (j >> 1), (kt | j) != 0);
+                    }
+                    tc_commit(smem_u32(&ctl->empty[s]));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(smem_u32(&ctl->tmem_full));
+            __syncwarp();
+            ++tc;
+        }
+        if (*abort_flag) {
+            // make sure no MMA still writes tensor memory before it is released
+            if (lane == 0) tc_commit(smem_u32(&ctl->drain));
+            __syncwarp();
+            volatile int never = 0;
+            mbar_wait(smem_u32(&ctl->drain), 0, &never, args.status, kErrWaitDrain);
+        }
+    } else if (warp == 2 || warp == 3) {
+        // ---------------- scale-factor loaders (warp 2: A, warp 3: B) ----------------
+        const bool is_a = (warp == 2);
+        uint32_t it = 0;
+        bool aborted = false;
+        for (int w = blockIdx.x; w < total && !aborted; w += gridDim.x) {
+            const Tile t = get_tile(args, w / args.n_tiles);
+            const int nt = w % args.n_tiles;
+            for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                if (!warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status, kErrWaitEmpty)) {
+                    aborted = true;
+                    break;
+                }
+                const bool half = args.k_tail_half && (kt == k_tiles - 1);
+                const uint32_t st = sbase + s * kStageBytes;
+                const int64_t kcol = (int64_t)kt * 8;   // first 32-element block of this stage
+                if (is_a) {
+                    const uint32_t dst0 = st + kABytes + kBBytes + lane * 16;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int64_t grow = t.row0 + 32 * j + lane;
+                        const bool valid = grow < args.a_rows;
+                        const uint8_t* src = args.sfa + (valid ? grow * args.ld_sf + kcol : 0);
+#pragma unroll
+                        for (int wd = 0; wd < 2; ++wd) {
+                            const bool ok = valid && (wd == 0 || !half);
+                            cp_async_4(dst0 + wd * 512 + j * 4, ok ? src + 4 * wd : args.sfa, ok ? 4u : 0u);
+                        }
+                    }
+                } else {
+                    const uint32_t dst0 = st + kABytes + kBBytes + kSfaBytes + lane * 16;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t rbase = b_row<kL1>(args, t.expert, nt, h);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int64_t brow = rbase + 32 * j + lane;
+                            const bool valid = brow < args.b_rows;
+                            const uint8_t* src = args.sfb + (valid ? brow * args.ld_sf + kcol : 0);
+#pragma unroll
+                            for (int wd = 0; wd < 2; ++wd) {
+                                const bool ok = valid && (wd == 0 || !half);
+                                cp_async_4(dst0 + wd * 1024 + h * 512 + j * 4, ok ? src + 4 * wd : args.sfb,
+                                           ok ? 4u : 0u);
+                            }
+                        }
+                    }
+                }
+                cp_async_commit();
+                if (it >= (uint32_t)kSfLag) {
+                    cp_async_wait<kSfLag>();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->full[(it - kSfLag) % kStages]));
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (!aborted && !*abort_flag && lane == 0) {
+            const uint32_t first = it > (uint32_t)kSfLag ? it - kSfLag : 0;
+            for (uint32_t i = first; i < it; ++i) mbar_arrive(smem_u32(&ctl->full[i % kStages]));
+        }
+    } else {
+        // ---------------- epilogue warps 4..11 ----------------
+        const int q = warp & 3;              // TMEM lane quarter this warp may access
+        const int hf = (warp - 4) >> 2;      // which half of the columns
+        const int row_in_tile = 32 * q + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+        uint32_t tc = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x, ++tc) {
+            const Tile t = get_tile(args, w / args.n_tiles);
+            const int nt = w % args.n_tiles;
+            if (!warp_wait(smem_u32(&ctl->tmem_full), tc & 1u, abort_flag, args.status, kErrWaitTmemFull)) break;
+            tc_fence_after();
+            uint32_t v[4][32];
+            if (kL1) {
+                tc_ld_32x32b_x32(taddr + 64 * hf, v[0]);            // gate, block 0
+                tc_ld_32x32b_x32(taddr + 64 * hf + 32, v[1]);       // gate, block 1
+                tc_ld_32x32b_x32(taddr + 128 + 64 * hf, v[2]);      // up, block 0
+                tc_ld_32x32b_x32(taddr + 128 + 64 * hf + 32, v[3]); // up, block 1
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tc_ld_32x32b_x32(taddr + 128 * hf + 32 * i, v[i]);
+            }
+            tc_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tmem_empty));
+            if (row_in_tile >= t.rows) continue;
+            const int64_t grow = t.row0 + row_in_tile;
+            if (kL1) {
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float g = round_bf16(__uint_as_float(v[b][i]));
+                        const float u = round_bf16(__uint_as_float(v[2 + b][i]));
+                        h[i] = round_bf16(silu_f32(g) * u);
+                    }
+                    uint4 codes;
+                    const uint32_t E = mx_quant32(h, codes);
+                    const int64_t col = (int64_t)nt * 128 + 64 * hf + 32 * b;   // column of h
+                    *reinterpret_cast<uint4*>(args.hq + grow * args.ld_hq + col / 2) = codes;
+                    args.hs[grow * args.ld_hs + col / 32] = (uint8_t)E;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t col = (int64_t)nt * kBN + 128 * hf + 32 * i;
+                    uint32_t p[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        p[j] = f32_to_bf16(__uint_as_float(v[i][2 * j])) |
+                               (f32_to_bf16(__uint_as_float(v[i][2 * j + 1])) << 16);
+                    uint16_t* dst = args.y + grow * args.ld_y + col;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        if (col + 16 * c < args.n_valid) {
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
+                            d4[0] = make_uint4(p[8 * c + 0], p[8 * c + 1], p[8 * c + 2], p[8 * c + 3]);
+                            d4[1] = make_uint4(p[8 * c + 4], p[8 * c + 5], p[8 * c + 6], p[8 * c + 7]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool kL1>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid, cudaStream_t s) {
+    static int configured_mask = 0;   // one bit per device
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kSmemBytes);
+        if (err != cudaSuccess) return err;
+        __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
+    }
+    mxf4_gemm_kernel<kL1><<<grid, kGemmThreads, kSmemBytes, s>>>(ta, tb, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
+                           cudaStream_t s) {
+    return launch<true>(ta, tb, a, grid, s);
+}
+
+cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
+                           cudaStream_t s) {
+    return launch<false>(ta, tb, a, grid, s);
+}
+
+}  // namespace mx

@@ -1,0 +1,89 @@
+// mx_internal.h -- launcher interfaces between the C-ABI layer (mx_api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+// ---- GEMM tile geometry (tcgen05 kind::mxf4, one CTA per tile, M = 128, N = 256) ----
+constexpr int kBM = 128;           // rows of A per tile (TMEM lanes)
+constexpr int kBN = 256;           // columns of the accumulator (L1: 128 gate + 128 up)
+constexpr int kBK = 256;           // E2M1 elements of K per pipeline stage (128 bytes)
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 384;  // 4 control warps + 8 epilogue warps
+
+// Routing: pairs per counting block.
+constexpr int kRouteChunk = 2048;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 64;
+
+// Arguments of the expert GEMM kernels (plain data, copied into the kernel parameters).
+struct GemmArgs {
+    const uint8_t* sfa;          // A scales [a_rows, K/32]
+    const uint8_t* sfb;          // B scales [b_rows, K/32]
+    int64_t ld_sf;               // K/32: scale bytes per row (A and B share K)
+    int64_t a_rows;              // rows of A (bound for scale loads; TMA zero-fills beyond)
+    int64_t b_rows;              // rows of the stacked B tensor
+    int32_t k_tiles;             // ceil(K / 256)
+    int32_t k_tail_half;         // 1 when the last stage holds only 128 of K
+    // M tiles: from the routing tables (device) or uniform over m_total rows.
+    const int32_t* tile_expert;  // nullptr -> uniform tiling
+    const int32_t* tile_row0;
+    const int32_t* tile_rows;
+    const int32_t* num_mtiles_dev;
+    int32_t num_mtiles_host;
+    int64_t m_total;
+    int32_t n_tiles;             // tiles along N per M tile
+    int64_t b_rows_per_expert;   // L1: 2I, L2: N
+    int64_t n_half;              // L1: I (first up row); L2: 0
+    int64_t n_valid;             // L1: I; L2: N (columns that exist)
+    // outputs
+    uint8_t* hq;                 // L1: requantised activation codes [rows, I/2]
+    uint8_t* hs;                 // L1: its scales [rows, I/32]
+    int64_t ld_hq, ld_hs;
+    uint16_t* y;                 // L2: BF16 output [rows, ld_y]
+    int64_t ld_y;
+    uint32_t* status;            // device status word
+};
+
+size_t gemm_smem_bytes();
+cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
+                           cudaStream_t s);
+cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
+                           cudaStream_t s);
+
+// ---- element-wise kernels ----
+cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, uint16_t* out, int64_t rows,
+                                 int64_t cols, int num_sms, cudaStream_t s);
+cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* out, int64_t rows,
+                               int64_t cols, int num_sms, cudaStream_t s);
+cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
+                             int num_sms, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,
+                           int64_t T, int64_t K, int64_t H, int num_sms, cudaStream_t s);
+
+// ---- routing ----
+struct RouteBufs {
+    int32_t* chunk_counts;   // [nchunks, E]
+    int32_t* chunk_base;     // [nchunks, E]
+    int32_t* local_rank;     // [T*K]
+    int32_t* counts;         // [E]
+    int32_t* offsets;        // [E+1]
+    int32_t* row_of;         // [T*K]
+    int32_t* tile_expert;    // [max_mtiles]
+    int32_t* tile_row0;
+    int32_t* tile_rows;
+    int32_t* num_mtiles;     // [1]
+    int64_t nchunks;
+};
+cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, const RouteBufs& rb,
+                         cudaStream_t s);
+// Quantise each token row once and write it to the rows of all its routed pairs; also
+// writes row_of (needs launch_route first).
+cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,
+                                int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs,
+                                cudaStream_t s);
+
+}  // namespace mx

@@ -1,0 +1,162 @@
+// mx_route.cu -- routing permutation for the MoE ("Current Bug: vLLM produces empty/garbage
+// output", "Phase 1: CuTeDSL Shared Expert Kernel": the MoE pipeline is the shared-expert
+// pipeline plus routing, top-k and scatter).
+//
+// The routed (token, slot) pairs are grouped by expert in a stable order: expert, then
+// token, then slot. Three launches, no host synchronisation (graph-capturable):
+//   1. route_count: per chunk of 2048 pairs, per-expert counts and each pair's rank among
+//      the earlier pairs of its expert inside the chunk (warp match + a per-warp scan);
+//   2. route_scan (one CTA): per-expert prefix over chunks, expert offsets, and the list of
+//      128-row M tiles (expert, first row, valid rows) that the grouped GEMMs walk;
+//   3. quant_gather: row_of[t, k] = offsets[e] + chunk_base[chunk, e] + rank, and the MX
+//      quantisation of each token row written once per routed pair into the grouped rows.
+#include "mx_device.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+
+namespace {
+
+constexpr int kCountThreads = 256;
+constexpr int kCountWarps = kCountThreads / 32;
+
+__global__ void __launch_bounds__(kCountThreads) route_count_kernel(const int32_t* __restrict__ ids,
+                                                                    int64_t n_pairs, int E,
+                                                                    int32_t* __restrict__ chunk_counts,
+                                                                    int32_t* __restrict__ local_rank) {
+    __shared__ int32_t s_run[kMaxExperts];
+    __shared__ int32_t s_warp[kCountWarps][kMaxExperts];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += kCountThreads) s_run[e] = 0;
+    const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
+    for (int round = 0; round < kRouteChunk / kCountThreads; ++round) {
+        for (int i = tid; i < kCountWarps * E; i += kCountThreads) s_warp[i / E][i % E] = 0;
+        __syncthreads();
+        const int64_t p = base + (int64_t)round * kCountThreads + tid;
+        const int32_t e = (p < n_pairs) ? __ldg(ids + p) : -1;
+        const bool valid = (e >= 0) && (e < E);
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+        const uint32_t below = peers & ((1u << lane) - 1u);
+        const int rank_in_warp = __popc(below);
+        if (valid && rank_in_warp == 0) s_warp[warp][e] = __popc(peers);
+        __syncthreads();
+        for (int x = tid; x < E; x += kCountThreads) {
+            int32_t run = s_run[x];
+#pragma unroll
+            for (int w = 0; w < kCountWarps; ++w) {
+                const int32_t c = s_warp[w][x];
+                s_warp[w][x] = run;
+                run += c;
+            }
+            s_run[x] = run;
+        }
+        __syncthreads();
+        if (valid) local_rank[p] = s_warp[warp][e] + rank_in_warp;
+        __syncthreads();
+    }
+    for (int e = tid; e < E; e += kCountThreads) chunk_counts[(int64_t)blockIdx.x * E + e] = s_run[e];
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ chunk_counts,
+                                                          int64_t nchunks, int E, RouteBufs rb) {
+    __shared__ int32_t s_cnt[kMaxExperts];
+    __shared__ int32_t s_off[kMaxExperts + 1];
+    __shared__ int32_t s_toff[kMaxExperts + 1];
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) {
+        int32_t run = 0;
+        for (int64_t c = 0; c < nchunks; ++c) {
+            const int32_t v = chunk_counts[c * E + e];
+            rb.chunk_base[c * E + e] = run;
+            run += v;
+        }
+        s_cnt[e] = run;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int32_t off = 0, toff = 0;
+        for (int e = 0; e < E; ++e) {
+            s_off[e] = off;
+            s_toff[e] = toff;
+            off += s_cnt[e];
+            toff += (s_cnt[e] + kBM - 1) / kBM;
+        }
+        s_off[E] = off;
+        s_toff[E] = toff;
+        rb.offsets[E] = off;
+        *rb.num_mtiles = toff;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        rb.counts[e] = s_cnt[e];
+        rb.offsets[e] = s_off[e];
+        const int32_t nt = (s_cnt[e] + kBM - 1) / kBM;
+        for (int32_t m = 0; m < nt; ++m) {
+            const int32_t idx = s_toff[e] + m;
+            rb.tile_expert[idx] = e;
+            rb.tile_row0[idx] = s_off[e] + m * kBM;
+            rb.tile_rows[idx] = min(kBM, s_cnt[e] - m * kBM);
+        }
+    }
+}
+
+constexpr int kGatherThreads = 256;
+
+__global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
+    const uint4* __restrict__ x8, const int32_t* __restrict__ ids, int K, int E, int64_t groups_per_row,
+    RouteBufs rb, uint32_t* __restrict__ xq32, uint8_t* __restrict__ xs) {
+    __shared__ int32_t s_rows[kMaxTopK];
+    const int64_t t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid < K) {
+        const int64_t p = t * K + tid;
+        const int32_t e = __ldg(ids + p);
+        int32_t row = -1;
+        if (e >= 0 && e < E)
+            row = rb.offsets[e] + rb.chunk_base[(p / kRouteChunk) * E + e] + rb.local_rank[p];
+        s_rows[tid] = row;
+        rb.row_of[p] = row;
+    }
+    __syncthreads();
+    const uint4* xrow = x8 + t * groups_per_row;
+    for (int64_t g0 = (tid & ~31); g0 < groups_per_row; g0 += kGatherThreads) {
+        const int64_t g = g0 + lane;
+        const bool ok = g < groups_per_row;
+        const uint4 xv = ok ? __ldg(xrow + g) : make_uint4(0, 0, 0, 0);
+        uint32_t E8;
+        const uint32_t packed = mx_quant8_quad(xv, E8);
+        if (ok) {
+            for (int k = 0; k < K; ++k) {
+                const int32_t r = s_rows[k];
+                if (r < 0) continue;
+                xq32[(int64_t)r * groups_per_row + g] = packed;
+                if ((g & 3) == 0) xs[(int64_t)r * (groups_per_row >> 2) + (g >> 2)] = (uint8_t)E8;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, const RouteBufs& rb,
+                         cudaStream_t s) {
+    const int64_t n = T * K;
+    if (n == 0) return cudaSuccess;
+    route_count_kernel<<<(unsigned)rb.nchunks, kCountThreads, 0, s>>>(ids, n, (int)E, rb.chunk_counts,
+                                                                       rb.local_rank);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    route_scan_kernel<<<1, 1024, 0, s>>>(rb.chunk_counts, rb.nchunks, (int)E, rb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,
+                                int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    quant_gather_kernel<<<(unsigned)T, kGatherThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), ids, (int)K,
+                                                               (int)E, H / 8, rb,
+                                                               reinterpret_cast<uint32_t*>(xq), xs);
+    return cudaGetLastError();
+}
+
+}  // namespace mx

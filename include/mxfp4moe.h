@@ -1,0 +1,161 @@
+/*
+ * mxfp4moe.h -- C ABI of the GB300 (sm_103a) MXFP4 mixture-of-experts expert FFN library.
+ *
+ * The operations follow three pages of developer notes (cited by page title and section):
+ *   [FMT]  "2026-05-08 DeepSeek V4 Pro NVFP4 Quantization" -- "FP4 (E2M1) expert weight
+ *          format confirmed" (w1/w3 int8 [3072, 3584] + E8M0 [3072, 224] -> [3072, 7168];
+ *          w2 int8 [7168, 1536] + E8M0 [7168, 96] -> [7168, 3072]; code 0 = +0, code 8 = -0).
+ *   [DQ]   same page -- "Script update: dequant_fp8_to_bf16.py now handles ALL compressed
+ *          types", item 1 (FP8 E4M3 x E8M0 per 128x128 block -> BF16) and item 2 (two E2M1
+ *          values per byte, lower nibble first, LUT x E8M0 scale per row per 32 columns).
+ *   [PIPE] "Current Bug: vLLM produces empty/garbage output" -- "Phase 1: CuTeDSL Shared
+ *          Expert Kernel" (L1 GEMM -> SiLU -> re-quant -> L2 GEMM; MoE = that plus routing,
+ *          top-k and scatter; gate/up stacked; shared expert = one group, no routing;
+ *          cudagraph-safe with pre-allocated buffers).
+ *   [BF16] same page -- "Phase 3: Clean up" (BF16 only for the SiLU activation and the
+ *          final scatter).
+ *
+ * Conventions for every call below:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library allocates no
+ *     device memory, never synchronises the stream (except mx_device_status) and launches
+ *     its kernels asynchronously on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream). Calls are safe to capture in a CUDA graph.
+ *   - Layouts are row-major. MXFP4 tensors are a code tensor uint8 [rows, cols/2] (byte j
+ *     holds logical column 2j in its low nibble, 2j+1 in its high nibble) plus a scale
+ *     tensor uint8 [rows, cols/32] of E8M0 bytes (value 2^(b-127), b = 255 is NaN). The
+ *     checkpoint's int8 code dtype is read as raw bytes. BF16 tensors are uint16 bit
+ *     patterns. Weights are in the nn.Linear [out, in] layout (K contiguous).
+ *   - Base pointers must be 16-byte aligned (MX_ERR_MISALIGNED otherwise).
+ *   - Arguments are validated before anything is launched; on any error nothing is launched.
+ *     A CUDA launch error maps to MX_ERR_CUDA.
+ *   - Kernels never trap. Every device-side wait is bounded; a wait that runs out sets a
+ *     device status word and the kernel returns early. mx_device_status() reads (and
+ *     optionally clears) that word.
+ *   - NaN results are written as 0x7FC0 with the element's sign bit.
+ */
+#ifndef MXFP4MOE_H
+#define MXFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MX_OK = 0,
+    MX_ERR_INVALID_ARG = 1,     /* null pointer, negative or inconsistent size           */
+    MX_ERR_UNSUPPORTED = 2,     /* size outside what the kernels support (see each call) */
+    MX_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned                      */
+    MX_ERR_WORKSPACE = 4,       /* workspace missing or smaller than the size query      */
+    MX_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed                  */
+    MX_ERR_DEVICE_TIMEOUT = 6   /* a bounded device-side wait ran out (mx_device_status) */
+} mx_status;
+
+typedef void* mx_stream_t;      /* cudaStream_t */
+
+/* Human-readable name of a status code. Never returns NULL. */
+const char* mx_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int mx_version(void);
+
+/* Synchronises the current device, then returns MX_OK or MX_ERR_DEVICE_TIMEOUT from the
+ * device status word that bounded waits set; clears the word when `clear` is non-zero.
+ * Returns MX_ERR_CUDA if the synchronisation itself reports an error. */
+int mx_device_status(int clear);
+
+/*
+ * mxfp4_dequant -- MXFP4 -> BF16 ([DQ] item 2, [FMT]).
+ *   out[r, c] = bf16( E2M1(nibble(codes[r, c/2], c%2)) * 2^(sf[r, c/32] - 127) )
+ *   codes uint8 [rows, cols/2], sf uint8 [rows, cols/32], out uint16 [rows, cols].
+ *   cols must be a positive multiple of 32 (MX_ERR_UNSUPPORTED otherwise); rows >= 0
+ *   (rows == 0 launches nothing). The result is exact whenever it is finite. Stacked
+ *   expert tensors [E, R, C/2] are passed as rows = E * R.
+ */
+int mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, void* out_bf16,
+                  int64_t rows, int64_t cols, mx_stream_t stream);
+
+/*
+ * fp8_block_dequant_128x128 -- FP8 E4M3 x E8M0 128x128 block scale -> BF16 ([DQ] item 1).
+ *   out[i, j] = bf16( e4m3(q[i, j]) * 2^(sf[i/128, j/128] - 127) )
+ *   q uint8 [rows, cols] (E4M3 "fn" bytes), sf uint8 [ceil(rows/128), ceil(cols/128)],
+ *   out uint16 [rows, cols]. Partial edge blocks use the scale of the block they fall in.
+ *   cols must be a positive multiple of 16 (MX_ERR_UNSUPPORTED otherwise).
+ */
+int fp8_block_dequant_128x128(const uint8_t* q_e4m3, const uint8_t* sf, void* out_bf16,
+                              int64_t rows, int64_t cols, mx_stream_t stream);
+
+/*
+ * act_quant_mxfp4 -- BF16 -> MXFP4 activation quantisation (the "re-quant" of [PIPE],
+ * with the OCP MX rule, which the pages leave open):
+ *   per row and per 32-column block: E = clamp(floor(log2 amax) - 2 + 127, 0, 254)
+ *   (E = 0 when amax = 0); code = E2M1 round-to-nearest-even of x * 2^(127 - E),
+ *   saturating at +-6, sign kept (-0 -> code 8). A block holding NaN/Inf gets E = 255 and
+ *   codes sign|7. x uint16 [M, K], codes uint8 [M, K/2], sf uint8 [M, K/32].
+ *   K must be a positive multiple of 32.
+ */
+int act_quant_mxfp4(const void* x_bf16, uint8_t* codes, uint8_t* sf,
+                    int64_t M, int64_t K, mx_stream_t stream);
+
+/*
+ * mxfp4_gemm_bf16 -- D = bf16(A . B^T) with MXFP4 operands on the tcgen05 tensor cores:
+ * the one-group case of the expert GEMM ([PIPE]: "num_groups=1 is just a regular GEMM").
+ *   A codes uint8 [M, K/2] + sa [M, K/32]; B codes uint8 [N, K/2] + sb [N, K/32];
+ *   D uint16 [M, N]. Accumulation is float32, the result is rounded once to BF16.
+ *   K must be a positive multiple of 128, N a positive multiple of 16; M >= 0.
+ */
+int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                    void* d_bf16, int64_t M, int64_t N, int64_t K, mx_stream_t stream);
+
+/*
+ * moe_mxfp4_workspace_size -- bytes of device workspace moe_mxfp4_forward and
+ * moe_mxfp4_route need for these sizes (K is ignored when routed == 0). The workspace holds
+ * the routing tables, the quantised activations and the L2 output; 256-byte aligned.
+ */
+size_t moe_mxfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K,
+                                int routed);
+
+/*
+ * moe_mxfp4_forward -- the MoE expert FFN over MXFP4 weights ([PIPE], [BF16]):
+ *   xq = act_quant(x);
+ *   for each routed pair (t, k) with e = topk_ids[t, k] in [0, E):
+ *     g, u = xq[t] . w13[e][0:I]^T, xq[t] . w13[e][I:2I]^T   (gate rows first, then up)
+ *     h    = bf16( silu(bf16(g)) * bf16(u) ),  hq = act_quant(h)      (fused epilogue)
+ *     y    = bf16( hq . w2[e]^T )
+ *   out[t] = bf16( sum_k topk_w[t, k] * y(t, k) )   (float32, slot order k = 0..K-1)
+ *   An id outside [0, E) (e.g. -1) contributes nothing; a token with no valid id gets 0.
+ *   Shared-expert mode: topk_ids == NULL and topk_w == NULL, E must be 1, K is ignored,
+ *   out = y.
+ *   x uint16 [T, H]; topk_ids int32 [T, K]; topk_w float32 [T, K];
+ *   w13 uint8 [E, 2I, H/2], s13 uint8 [E, 2I, H/32]; w2 uint8 [E, H, I/2],
+ *   s2 uint8 [E, H, I/32]; out uint16 [T, H] (overwritten, not accumulated).
+ *   H and I must be positive multiples of 128 (MX_ERR_UNSUPPORTED otherwise); 1 <= E <= 1024,
+ *   1 <= K <= 64; T >= 0 (T == 0 launches nothing). workspace: device memory of at least
+ *   moe_mxfp4_workspace_size(T, H, I, E, K, topk_ids != NULL) bytes, 256-byte aligned, not
+ *   used by another call that runs at the same time.
+ */
+int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_w,
+                      const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
+                      const uint8_t* s2, void* out, int64_t T, int64_t H, int64_t I,
+                      int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                      mx_stream_t stream);
+
+/*
+ * moe_mxfp4_route -- the routing permutation step of moe_mxfp4_forward on its own
+ * ([PIPE]: "routing, topk, scatter"), for inspection and tests.
+ *   counts int32 [E]: valid pairs per expert; offsets int32 [E+1]: exclusive prefix sum;
+ *   row_of int32 [T, K]: the row of pair (t, k) in the expert-grouped order, which is
+ *   sorted by (expert, token, slot); -1 for a dropped pair. Same size rules and workspace
+ *   as moe_mxfp4_forward in routed mode.
+ */
+int moe_mxfp4_route(const int32_t* topk_ids, int64_t T, int64_t K, int64_t E,
+                    int32_t* counts, int32_t* offsets, int32_t* row_of,
+                    void* workspace, size_t ws_bytes, mx_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4MOE_H */

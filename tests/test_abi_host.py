@@ -1,0 +1,128 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library must build, load, and export every function include/mxfp4moe.h declares.
+Argument validation happens before any CUDA call, so the documented status codes for
+bad sizes, null pointers, misaligned pointers and short workspaces are checked here with
+fake (never dereferenced) addresses.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp4moe.h")
+
+MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_MISALIGNED, MX_ERR_WORKSPACE = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp4_block_scaled_mxfp4_gb300 import build
+    build.build()
+    from fp4_block_scaled_mxfp4_gb300 import _native
+    return _native.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("mxfp4_dequant", "fp8_block_dequant_128x128", "act_quant_mxfp4", "moe_mxfp4_forward",
+                 "moe_mxfp4_workspace_size", "mx_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.mx_status_string(0) == b"MX_OK"
+    assert lib.mx_status_string(4) == b"MX_ERR_WORKSPACE"
+    assert lib.mx_status_string(99) == b"MX_ERR_UNKNOWN"
+    assert lib.mx_version() >= 100
+
+
+FAKE = 1 << 20          # 16- and 256-byte aligned, never dereferenced
+ODD = FAKE + 8          # not 16-byte aligned
+
+
+def test_dequant_validation(lib):
+    assert lib.mxfp4_dequant(FAKE, FAKE, FAKE, 4, 48, None) == MX_ERR_UNSUPPORTED     # cols % 32
+    assert lib.mxfp4_dequant(FAKE, FAKE, FAKE, -1, 64, None) == MX_ERR_INVALID_ARG
+    assert lib.mxfp4_dequant(FAKE, FAKE, FAKE, 0, 64, None) == MX_OK                  # nothing to do
+    assert lib.mxfp4_dequant(None, FAKE, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
+    assert lib.mxfp4_dequant(ODD, FAKE, FAKE, 4, 64, None) == MX_ERR_MISALIGNED
+    assert lib.fp8_block_dequant_128x128(FAKE, FAKE, FAKE, 4, 40, None) == MX_ERR_UNSUPPORTED
+    assert lib.fp8_block_dequant_128x128(FAKE, FAKE, ODD, 4, 64, None) == MX_ERR_MISALIGNED
+    assert lib.act_quant_mxfp4(FAKE, FAKE, FAKE, 4, 40, None) == MX_ERR_UNSUPPORTED
+    assert lib.act_quant_mxfp4(FAKE, None, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
+
+
+def test_gemm_validation(lib):
+    assert lib.mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 192, None) == MX_ERR_UNSUPPORTED
+    assert lib.mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 250, 256, None) == MX_ERR_UNSUPPORTED
+    assert lib.mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 256, 256, None) == MX_OK
+    assert lib.mxfp4_gemm_bf16(FAKE, FAKE, None, FAKE, FAKE, 4, 256, 256, None) == MX_ERR_INVALID_ARG
+    assert lib.mxfp4_gemm_bf16(FAKE, ODD, FAKE, FAKE, FAKE, 4, 256, 256, None) == MX_ERR_MISALIGNED
+
+
+def _fwd(lib, ids=FAKE, w=FAKE, T=16, H=256, I=128, E=4, K=2, ws=FAKE, ws_bytes=None, x=FAKE):
+    if ws_bytes is None:
+        ws_bytes = lib.moe_mxfp4_workspace_size(T, H, I, E, K, 1 if ids else 0)
+    return lib.moe_mxfp4_forward(x, ids, w, FAKE, FAKE, FAKE, FAKE, FAKE, T, H, I, E, K, ws, ws_bytes, None)
+
+
+def test_forward_validation(lib):
+    assert _fwd(lib, H=200) == MX_ERR_UNSUPPORTED
+    assert _fwd(lib, I=96) == MX_ERR_UNSUPPORTED
+    assert _fwd(lib, E=0) == MX_ERR_INVALID_ARG
+    assert _fwd(lib, E=2000) == MX_ERR_UNSUPPORTED
+    assert _fwd(lib, K=0) == MX_ERR_INVALID_ARG
+    assert _fwd(lib, K=65) == MX_ERR_UNSUPPORTED
+    assert _fwd(lib, T=-1) == MX_ERR_INVALID_ARG
+    assert _fwd(lib, T=0) == MX_OK
+    assert _fwd(lib, w=None) == MX_ERR_INVALID_ARG                  # ids without weights
+    assert _fwd(lib, ids=None, w=None, E=2) == MX_ERR_INVALID_ARG  # shared mode needs E = 1
+    assert _fwd(lib, x=None) == MX_ERR_INVALID_ARG
+    assert _fwd(lib, x=ODD) == MX_ERR_MISALIGNED
+    need = lib.moe_mxfp4_workspace_size(16, 256, 128, 4, 2, 1)
+    assert need > 0
+    assert _fwd(lib, ws_bytes=need - 1) == MX_ERR_WORKSPACE
+    assert _fwd(lib, ws=None) == MX_ERR_WORKSPACE
+    assert _fwd(lib, ws=FAKE + 128) == MX_ERR_MISALIGNED
+    assert lib.moe_mxfp4_workspace_size(16, 200, 128, 4, 2, 1) == 0   # unsupported sizes -> 0
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    a = lib.moe_mxfp4_workspace_size(64, 7168, 3072, 48, 8, 1)
+    b = lib.moe_mxfp4_workspace_size(8192, 7168, 3072, 48, 8, 1)
+    s = lib.moe_mxfp4_workspace_size(256, 7168, 3072, 1, 1, 0)
+    assert 0 < a < b and s > 0
+    assert a % 256 == 0 and b % 256 == 0
+    # the routed workspace holds at least the quantised activations and the L2 output
+    assert b >= 8192 * 8 * (7168 // 2 + 7168 * 2)
+
+
+def test_route_validation(lib):
+    need = lib.moe_mxfp4_workspace_size(10, 128, 128, 4, 2, 1)
+    assert lib.moe_mxfp4_route(FAKE, 10, 2, 4, FAKE, FAKE, FAKE, FAKE, need - 1, None) == MX_ERR_WORKSPACE
+    assert lib.moe_mxfp4_route(FAKE, 10, 2, 0, FAKE, FAKE, FAKE, FAKE, need, None) == MX_ERR_INVALID_ARG
+    assert lib.moe_mxfp4_route(None, 10, 2, 4, FAKE, FAKE, FAKE, FAKE, need, None) == MX_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from fp4_block_scaled_mxfp4_gb300 import _native
+    monkeypatch.setattr(_native, "_lib", None)
+    monkeypatch.setattr(_native, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _native.lib()

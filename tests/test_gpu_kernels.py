@@ -1,0 +1,195 @@
+"""GPU parity of the single kernels against the CPU oracle, through the C ABI.
+
+Bit-exact: MXFP4 -> BF16 dequant, FP8 128x128 dequant, the MX activation quantiser (codes
+and scales) and the routing permutation. The block-scaled GEMM is compared with the exact
+product (one BF16 rounding plus the float32 accumulation allowance), first on structured
+inputs that isolate the data path (all scales 1) and the scale-factor path (all codes
+equal), then on random inputs across tile, stage and ragged-edge boundaries.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import assert_gemm_close, bf16_host, dev, native
+from workloads import f32_to_bf16_bits, make_dequant_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    m = native()
+    assert m.device_status(clear=True) == 0
+    yield m
+    assert m.device_status(clear=True) == 0, "a bounded device wait ran out"
+
+
+def _empty(shape, dtype):
+    import torch
+    return torch.empty(shape, dtype=dtype, device="cuda")
+
+
+# ----------------------------------------------------------------------------- dequant
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (3, 64), (257, 96), (1000, 7168)])
+def test_mxfp4_dequant_bit_exact(mx, rows, cols):
+    import torch
+    rng = np.random.default_rng(rows * 7 + cols)
+    codes = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    sf = rng.integers(0, 256, size=(rows, cols // 32), dtype=np.uint8)   # every scale byte incl. 0, 255
+    out = _empty((rows, cols), torch.bfloat16)
+    mx.mxfp4_dequant(dev(codes), dev(sf), out)
+    np.testing.assert_array_equal(bf16_host(out), oracle.mxfp4_dequant(codes, sf))
+
+
+def test_mxfp4_dequant_all_code_scale_pairs(mx):
+    import torch
+    codes = np.tile(np.arange(256, dtype=np.uint8).reshape(16, 16), (256, 1))  # 4096 rows x 32 cols
+    sf = np.repeat(np.arange(256, dtype=np.uint8), 16).reshape(4096, 1)
+    out = _empty((4096, 32), torch.bfloat16)
+    mx.mxfp4_dequant(dev(codes), dev(sf), out)
+    np.testing.assert_array_equal(bf16_host(out), oracle.mxfp4_dequant(codes, sf))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (130, 272), (300, 1040)])
+def test_fp8_dequant_bit_exact(mx, rows, cols):
+    import torch
+    rng = np.random.default_rng(rows + cols)
+    q = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)          # includes NaN codes
+    sf = rng.integers(0, 256, size=((rows + 127) // 128, (cols + 127) // 128), dtype=np.uint8)
+    out = _empty((rows, cols), torch.bfloat16)
+    mx.fp8_block_dequant_128x128(dev(q), dev(sf), out)
+    np.testing.assert_array_equal(bf16_host(out), oracle.fp8_block_dequant_128x128(q, sf))
+
+
+def test_dequant_sweep_full_size_sampled(mx):
+    """The full dequant workload (48 experts, FP8 [7168, 7168]); sampled rows vs the oracle."""
+    import torch
+    w13, s13, w2, s2, q, fsf = make_dequant_inputs()
+    rng = np.random.default_rng(99)
+    for codes, sf in ((w13, s13), (w2, s2)):
+        R, half = codes.shape
+        out = _empty((R, 2 * half), torch.bfloat16)
+        mx.mxfp4_dequant(dev(codes), dev(sf), out)
+        rows = np.unique(np.concatenate([rng.integers(0, R, 48), [0, R - 1]]))
+        got = bf16_host(out[torch.from_numpy(rows).cuda()])
+        np.testing.assert_array_equal(got, oracle.mxfp4_dequant(codes[rows], sf[rows]))
+        del out
+    out = _empty(q.shape, torch.bfloat16)
+    mx.fp8_block_dequant_128x128(dev(q), dev(fsf), out)
+    rows = np.unique(np.concatenate([rng.integers(0, q.shape[0], 64), [0, q.shape[0] - 1]]))
+    ref = oracle.fp8_block_dequant_128x128(q, fsf)[rows]
+    np.testing.assert_array_equal(bf16_host(out)[rows], ref)
+
+
+# ----------------------------------------------------------------------------- act quant
+
+@pytest.mark.parametrize("M,K", [(1, 32), (5, 96), (300, 7168), (2048, 3072)])
+def test_act_quant_bit_exact(mx, M, K):
+    import torch
+    rng = np.random.default_rng(M * 3 + K)
+    x = rng.standard_normal((M, K)).astype(np.float32) * np.float32(2.0)
+    x[rng.random((M, K)) < 0.01] *= 1000.0
+    xb = f32_to_bf16_bits(x)
+    specials = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x7F7F, 0xFF7F, 0x3E80, 0x3F40,
+                         0x3FA0, 0x3FE0, 0x4020, 0x4060, 0x40A0], dtype=np.uint16)
+    flat = xb.reshape(-1)
+    flat[: min(flat.size, 4096)][rng.random(min(flat.size, 4096)) < 0.2] = rng.choice(specials)
+    if M >= 5:
+        xb[1, :32] = 0                     # all-zero block
+        xb[2, :32] = 0x8000                # all -0 block
+        xb[3, 3] = 0x7FC0                  # NaN block
+        xb[4, 40] = 0xFF80                 # -inf block
+    codes = _empty((M, K // 2), torch.uint8)
+    sf = _empty((M, K // 32), torch.uint8)
+    mx.act_quant_mxfp4(dev(xb).view(torch.bfloat16), codes, sf)
+    ref_c, ref_s = oracle.act_quant_mxfp4(xb)
+    np.testing.assert_array_equal(sf.cpu().numpy(), ref_s)
+    np.testing.assert_array_equal(codes.cpu().numpy(), ref_c)
+
+
+# ----------------------------------------------------------------------------- GEMM
+
+def _gemm_case(mx, a, sa, b, sb, what):
+    import torch
+    M, N = a.shape[0], b.shape[0]
+    d = _empty((M, N), torch.bfloat16)
+    mx.mxfp4_gemm_bf16(dev(a), dev(sa), dev(b), dev(sb), d)
+    A = oracle.mxfp4_values(a, sa)
+    B = oracle.mxfp4_values(b, sb)
+    exact = A @ B.T
+    absdot = np.abs(A) @ np.abs(B).T
+    assert_gemm_close(bf16_host(d), exact, absdot, what)
+
+
+def test_gemm_data_path_unit_scales(mx):
+    """All scales 1: isolates operand layout, swizzle, nibble order and K advance."""
+    rng = np.random.default_rng(1)
+    M, N, K = 128, 256, 256
+    a = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = np.full((M, K // 32), 127, np.uint8)
+    sb = np.full((N, K // 32), 127, np.uint8)
+    _gemm_case(mx, a, sa, b, sb, "unit scales")
+
+
+def test_gemm_one_hot_k(mx):
+    """A single nonzero K column: checks which element of the byte the tensor core reads
+    first (lower nibble = even column) and the K position of every MMA of a stage."""
+    M, N, K = 128, 256, 256
+    for k in (0, 1, 63, 64, 127, 130, 255):
+        a = np.zeros((M, K // 2), np.uint8)
+        b = np.zeros((N, K // 2), np.uint8)
+        code = 0x02 if k % 2 == 0 else 0x20              # value 1.0 in column k
+        a[:, k // 2] = code
+        b[:, k // 2] = code
+        b[::3, k // 2] = 0x04 if k % 2 == 0 else 0x40    # 2.0 on every third B row
+        sa = np.full((M, K // 32), 127, np.uint8)
+        sb = np.full((N, K // 32), 127, np.uint8)
+        _gemm_case(mx, a, sa, b, sb, f"one-hot k={k}")
+
+
+def test_gemm_scale_path_constant_codes(mx):
+    """All codes 1.0: D[m, n] = 32 * sum_kb 2^(sa[m,kb] + sb[n,kb] - 254) isolates the
+    scale-factor layout (rows, K blocks, sf ids)."""
+    rng = np.random.default_rng(2)
+    M, N, K = 128, 256, 512
+    a = np.full((M, K // 2), 0x22, np.uint8)
+    b = np.full((N, K // 2), 0x22, np.uint8)
+    sa = rng.integers(117, 138, size=(M, K // 32), dtype=np.uint8)
+    sb = rng.integers(117, 138, size=(N, K // 32), dtype=np.uint8)
+    _gemm_case(mx, a, sa, b, sb, "constant codes")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (128, 256, 128), (77, 256, 1024), (300, 512, 2048),
+                                   (129, 272, 384), (1000, 1024, 7168), (513, 7168, 3072)])
+def test_gemm_random(mx, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    a = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = rng.integers(115, 135, size=(M, K // 32), dtype=np.uint8)
+    sb = rng.integers(118, 125, size=(N, K // 32), dtype=np.uint8)
+    _gemm_case(mx, a, sa, b, sb, f"random {M}x{N}x{K}")
+
+
+# ----------------------------------------------------------------------------- routing
+
+@pytest.mark.parametrize("T,K,E", [(1, 1, 1), (100, 4, 5), (3000, 8, 48), (8192, 8, 48), (513, 6, 300)])
+def test_route_bit_exact(mx, T, K, E):
+    import torch
+    rng = np.random.default_rng(T + K + E)
+    ids = rng.integers(-1, E + 1, size=(T, K)).astype(np.int32)      # includes dropped ids
+    if T >= 100:
+        ids[: T // 2, 0] = 0                                          # one expert with many tiles
+    ws = torch.empty(mx.moe_mxfp4_workspace_size(T, 128, 128, E, K, True), dtype=torch.uint8, device="cuda")
+    counts = _empty((E,), torch.int32)
+    offsets = _empty((E + 1,), torch.int32)
+    row_of = _empty((T, K), torch.int32)
+    mx.moe_mxfp4_route(dev(ids), E, counts, offsets, row_of, ws)
+    rc, ro, rr, _ = oracle.moe_route(ids, E)
+    np.testing.assert_array_equal(counts.cpu().numpy(), rc)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), ro)
+    np.testing.assert_array_equal(row_of.cpu().numpy(), rr)
