@@ -1,0 +1,442 @@
+"""Benchmark of the MXFP4 MoE expert FFN on GB300 (one JSON line on stdout).
+
+A step is one routed MoE forward (routing permutation, MX quantisation of x, L1 grouped
+GEMM with fused SiLU-gate + re-quant, L2 grouped GEMM, top-k weighted combine) over the
+prefill workload: 8192 tokens, hidden 7168, intermediate 3072, 48 experts, top-8 with
+Zipf(1.0)-skewed routing, MXFP4 weights (1.68 GB), synthetic seeded inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (one process per GPU under torchrun, weak scaling):
+each rank processes its own batch; the timed region is bracketed by a barrier and a
+device synchronisation and the slowest rank's time is used.
+
+`value` is the algorithmic TFLOP/s of the forward (132,120,576 FLOP per routed pair) with
+every input resident in HBM; `e2e` is the same metric through the C ABI with the step's
+inputs copied from pinned host memory and the output copied back inside the timed region.
+`roofline` reports the L1 GEMM, timed live with CUDA events recorded by the library at
+its phase boundaries. `cpu_baseline` times the CPU oracle on a small token sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+# The oracle is timed on one host core: pin BLAS before numpy loads.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, make_config_inputs, make_dequant_inputs, make_moe_inputs  # noqa: E402
+
+METRIC = "MoE fwd TFLOP/s (MXFP4 grouped GEMM) & dequant GB/s, % of roofline, 1 GB300"
+WORKLOAD = ("routed MoE prefill forward: T=8192 tokens, hidden 7168, intermediate 3072, 48 experts, "
+            "top-8, Zipf(1.0) expert skew, MXFP4 (E2M1 + E8M0/32) weights")
+FP4_OVER_BF16 = 13.5 / 2.25       # nominal dense FP4 : BF16 tensor-core ratio on GB300
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "l1_gemm_prefill_traffic.json")
+GEMM_SRC = os.path.join(ROOT, "fp4_block_scaled_mxfp4_gb300", "csrc", "mx_gemm.cu")
+
+
+def flops_per_pair(H, I):
+    return 2 * H * 2 * I + 2 * I * H
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def l1_traffic_per_launch():
+    """DRAM bytes per L1 launch from the committed ncu summary, if it matches this kernel."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    with open(GEMM_SRC, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if d.get("kernel_source_sha256") != sha:
+        return None
+    return d.get("dram_bytes_per_full_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_oracle_sample(inp, tokens):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.moe_forward(inp.x, inp.topk_ids, inp.topk_w, inp.w13, inp.s13, inp.w2, inp.s2, inp.I,
+                       tokens=tokens)
+    dt = time.perf_counter() - t0
+    ids = inp.topk_ids[tokens]
+    pairs = int(((ids >= 0) & (ids < inp.E)).sum())
+    return dt, pairs
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, one token of the workload per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    c = CONFIGS["prefill"]
+    inp = make_config_inputs("prefill")
+    fpp = flops_per_pair(c["H"], c["I"])
+    rng = np.random.default_rng(1234)
+    for _ in range(args.warmup):
+        time_oracle_sample(inp, [int(rng.integers(inp.T))])
+    total_t, total_pairs = 0.0, 0
+    for _ in range(args.steps):
+        dt, pairs = time_oracle_sample(inp, [int(rng.integers(inp.T))])
+        total_t += dt
+        total_pairs += pairs
+    value = total_pairs * fpp / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "one token (its 8 routed pairs) per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": "one prefill token (8 routed pairs) per step, numpy float64, 1 thread"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from fp4_block_scaled_mxfp4_gb300 import build as _build
+    _build.build()
+    import fp4_block_scaled_mxfp4_gb300 as mx
+
+    c = dict(CONFIGS["prefill"])
+    if args.tokens:
+        c["T"] = args.tokens
+    T, H, I, E, K = c["T"], c["H"], c["I"], c["E"], c["K"]
+    inp = make_moe_inputs(**c) if args.tokens else make_config_inputs("prefill")
+    pairs = int(((inp.topk_ids >= 0) & (inp.topk_ids < E)).sum())
+    flop_step = pairs * flops_per_pair(H, I)
+    flop_l1 = pairs * 2 * H * 2 * I
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    x = d(inp.x).view(torch.bfloat16)
+    ids = d(inp.topk_ids)
+    w = d(inp.topk_w)
+    w13, s13, w2, s2 = (d(a) for a in (inp.w13, inp.s13, inp.w2, inp.s2))
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mx.moe_mxfp4_workspace_size(T, H, I, E, K, True), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    n_phase = 6
+
+    def step(evs=None):
+        mx.moe_mxfp4_forward(x, ids, w, w13, s13, w2, s2, out, ws, stream=stream, events=evs)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    if mx.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---------------- device-resident timed region ----------------
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_phase)] for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for row in ev:
+            for e in row:
+                e.record(stream)          # create the underlying CUDA events
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                step(ev[i])
+            stop.record(stream)
+        torch.cuda.synchronize()
+    elapsed_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    if mx.device_status() != 0:
+        raise RuntimeError("device status set during the timed region")
+    phase_names = ["route", "quant_gather", "l1_gemm", "l2_gemm", "combine"]
+    phase_ms = {n: 0.0 for n in phase_names}
+    for row in ev:
+        for j, n in enumerate(phase_names):
+            phase_ms[n] += row[j].elapsed_time(row[j + 1])
+    phase_ms = {n: v / args.steps for n, v in phase_ms.items()}
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flop_step / (ms_per_step * 1e-3) / 1e12
+
+    # ---------------- end-to-end through the C ABI with host buffers ----------------
+    e2e_steps = max(3, min(args.steps, 20))
+    hx = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    hx.view(torch.int16).numpy()[:] = inp.x.view(np.int16)
+    hids = torch.from_numpy(inp.topk_ids.copy()).pin_memory()
+    hw = torch.from_numpy(inp.topk_w.copy()).pin_memory()
+    hout = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    xin = torch.empty_like(x)
+    idin = torch.empty_like(ids)
+    win = torch.empty_like(w)
+
+    def e2e_step():
+        xin.copy_(hx, non_blocking=True)
+        idin.copy_(hids, non_blocking=True)
+        win.copy_(hw, non_blocking=True)
+        mx.moe_mxfp4_forward(xin, idin, win, w13, s13, w2, s2, out, ws, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = hx.numel() * 2 + hids.numel() * 4 + hw.numel() * 4
+    d2h = hout.numel() * 2
+
+    # ---------------- context figures measured outside the timed step ----------------
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra = measure_extra(mx, torch, dev, stream)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peaks, peak_kind = measured_peaks()
+    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    l1_tflops = flop_l1 / (phase_ms["l1_gemm"] * 1e-3) / 1e12
+    traffic = l1_traffic_per_launch()
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        rng = np.random.default_rng(7)
+        tokens = sorted(rng.choice(T, size=2, replace=False).tolist())
+        dt, p = time_oracle_sample(inp, tokens)
+        cpu = {"value": p * flops_per_pair(H, I) / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(tokens)} prefill tokens ({p} routed pairs), numpy float64, 1 thread, "
+                         f"{dt:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
+        "config": {"workload": WORKLOAD if not args.tokens else WORKLOAD.replace("T=8192", f"T={T}"),
+                   "routed_pairs_per_step": pairs, "flop_per_step": flop_step,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (1.68 GB MXFP4 weights + 117 MB activations per step)"},
+        "roofline": {"kernel": "L1 grouped GEMM (gate/up, fused SiLU + MX re-quant)", "bound": "tensor",
+                     "achieved": l1_tflops, "peak": fp4_peak, "unit": "TFLOP/s", "frac": l1_tflops / fp4_peak,
+                     "traffic": traffic,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
+        "phases_ms": phase_ms,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flop_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clocks.summary(),
+        "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_extra(mx, torch, dev, stream):
+    """Dequant sweep GB/s and the decode / shared-expert forwards (context, same GPU)."""
+    res = {}
+    peaks, _ = measured_peaks()
+    hbm = peaks["hbm_gbs"]
+
+    def timeit(fn, reps=10, warm=3):
+        with torch.cuda.stream(stream):
+            for _ in range(warm):
+                fn()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    w13, s13, w2, s2, q, fsf = make_dequant_inputs()
+    t = {k: torch.from_numpy(v).to(dev) for k, v in (("w13", w13), ("s13", s13), ("w2", w2), ("s2", s2),
+                                                        ("q", q), ("fsf", fsf))}
+    o13 = torch.empty((w13.shape[0], 2 * w13.shape[1]), dtype=torch.bfloat16, device=dev)
+    o2 = torch.empty((w2.shape[0], 2 * w2.shape[1]), dtype=torch.bfloat16, device=dev)
+
+    def deq():
+        mx.mxfp4_dequant(t["w13"], t["s13"], o13, stream=stream)
+        mx.mxfp4_dequant(t["w2"], t["s2"], o2, stream=stream)
+
+    ms = timeit(deq)
+    nbytes = w13.nbytes + s13.nbytes + w2.nbytes + s2.nbytes + (o13.numel() + o2.numel()) * 2
+    res["mxfp4_dequant"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm, "ms": ms,
+                            "bytes": nbytes}
+    del o13, o2
+    of = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    ms = timeit(lambda: mx.fp8_block_dequant_128x128(t["q"], t["fsf"], of, stream=stream), reps=50)
+    nbytes = q.nbytes + fsf.nbytes + of.numel() * 2
+    res["fp8_dequant"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm, "ms": ms,
+                          "bytes": nbytes}
+    del t, of
+    torch.cuda.empty_cache()
+    for name in ("decode", "shared"):
+        inp = make_config_inputs(name)
+        c = CONFIGS[name]
+        x = torch.from_numpy(inp.x).to(dev).view(torch.bfloat16)
+        routed = inp.topk_ids is not None
+        ids = torch.from_numpy(inp.topk_ids).to(dev) if routed else None
+        w = torch.from_numpy(inp.topk_w).to(dev) if routed else None
+        W = [torch.from_numpy(a).to(dev) for a in (inp.w13, inp.s13, inp.w2, inp.s2)]
+        out = torch.empty((c["T"], c["H"]), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(256, mx.moe_mxfp4_workspace_size(c["T"], c["H"], c["I"], c["E"], inp.K, routed)),
+                         dtype=torch.uint8, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def fwd():
+            flush.zero_()          # keep the weights out of L2 between repetitions
+            mx.moe_mxfp4_forward(x, ids, w, *W, out, ws, stream=stream)
+
+        def only_flush():
+            flush.zero_()
+
+        ms = timeit(fwd, reps=20) - timeit(only_flush, reps=20)
+        pairs = int(((inp.topk_ids >= 0) & (inp.topk_ids < c["E"])).sum()) if routed else c["T"]
+        touched = np.unique(inp.topk_ids).size if routed else 1
+        wbytes = touched * (inp.w13[0].nbytes + inp.s13[0].nbytes + inp.w2[0].nbytes + inp.s2[0].nbytes)
+        nbytes = wbytes + inp.x.nbytes * 2
+        res[name] = {"ms": ms, "TFLOP/s": pairs * flops_per_pair(c["H"], c["I"]) / ms / 1e9,
+                     "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm, "algorithmic_bytes": nbytes}
+        del x, ids, w, W, out, ws, flush
+        torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the dequant/decode/shared context figures")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle sample")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="prefill batch size other than 8192 (smaller cases for profiler captures)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -13,6 +13,7 @@ from ._native import (  # noqa: F401
     library_path,
     moe_mxfp4_forward,
     moe_mxfp4_route,
+    moe_mxfp4_workspace_layout,
     moe_mxfp4_workspace_size,
     mxfp4_dequant,
     mxfp4_gemm_bf16,

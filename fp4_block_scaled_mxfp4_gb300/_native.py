@@ -30,6 +30,10 @@ _SIGNATURES = {
     "moe_mxfp4_forward": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
                                          _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
                                          _c_ptr]),
+    "moe_mxfp4_forward_timed": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                               _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
+                                               _c_ptr, _c_ptr]),
+    "moe_mxfp4_workspace_layout": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int, _c_ptr]),
     "moe_mxfp4_route": (ctypes.c_int, [_c_ptr, _c_i64, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
                                        ctypes.c_size_t, _c_ptr]),
 }
@@ -154,8 +158,21 @@ def moe_mxfp4_workspace_size(T: int, H: int, I: int, E: int, K: int, routed: boo
     return int(lib().moe_mxfp4_workspace_size(T, H, I, E, K, 1 if routed else 0))
 
 
-def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, stream=None) -> None:
-    """MoE expert FFN over MXFP4 weights; topk_ids/topk_w None selects the shared expert."""
+def moe_mxfp4_workspace_layout(T: int, H: int, I: int, E: int, K: int, routed: bool = True) -> dict:
+    """Byte offsets of the intermediates a forward leaves in its workspace (see the header)."""
+    buf = (ctypes.c_int64 * 8)()
+    _check(lib().moe_mxfp4_workspace_layout(T, H, I, E, K, 1 if routed else 0, ctypes.addressof(buf)),
+           "moe_mxfp4_workspace_layout")
+    names = ("xq", "xs", "hq", "hs", "y", "row_of", "counts", "offsets")
+    return {n: int(v) for n, v in zip(names, buf)}
+
+
+def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, stream=None, events=None) -> None:
+    """MoE expert FFN over MXFP4 weights; topk_ids/topk_w None selects the shared expert.
+
+    ``events``: optional sequence of 6 torch.cuda.Event (or None) recorded at the phase
+    boundaries (before, after routing, after quantisation, after L1, after L2, after combine).
+    """
     import torch
     T, H = x.shape
     E, twoI, _ = w13.shape
@@ -171,9 +188,15 @@ def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, str
     _need(s2, torch.uint8, (E, H, I // 32), "s2")
     _need(out, out.dtype, (T, H), "out")
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib().moe_mxfp4_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2),
-                                   _ptr(s2), _ptr(out), T, H, I, E, K, _ptr(workspace), ws_bytes,
-                                   _stream(stream)), "moe_mxfp4_forward")
+    if events is None:
+        _check(lib().moe_mxfp4_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2),
+                                       _ptr(s2), _ptr(out), T, H, I, E, K, _ptr(workspace), ws_bytes,
+                                       _stream(stream)), "moe_mxfp4_forward")
+        return
+    evs = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else 0) for e in events])
+    _check(lib().moe_mxfp4_forward_timed(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2),
+                                         _ptr(s2), _ptr(out), T, H, I, E, K, _ptr(workspace), ws_bytes,
+                                         _stream(stream), ctypes.addressof(evs)), "moe_mxfp4_forward_timed")
 
 
 def moe_mxfp4_route(topk_ids, E: int, counts, offsets, row_of, workspace, stream=None) -> None:

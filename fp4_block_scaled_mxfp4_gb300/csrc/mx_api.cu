@@ -269,6 +269,21 @@ size_t moe_mxfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int6
     return ws_layout(T, H, I, E, K, routed != 0).total;
 }
 
+int moe_mxfp4_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed, int64_t* out) {
+    if (!out) return MX_ERR_INVALID_ARG;
+    if (int e = check_moe_dims(T, H, I, E, K, routed != 0)) return e;
+    const WsLayout L = ws_layout(T, H, I, E, K, routed != 0);
+    out[0] = (int64_t)L.xq;
+    out[1] = (int64_t)L.xs;
+    out[2] = (int64_t)L.hq;
+    out[3] = (int64_t)L.hs;
+    out[4] = routed ? (int64_t)L.y : -1;
+    out[5] = routed ? (int64_t)L.row_of : -1;
+    out[6] = routed ? (int64_t)L.counts : -1;
+    out[7] = routed ? (int64_t)L.offsets : -1;
+    return MX_OK;
+}
+
 int moe_mxfp4_route(const int32_t* topk_ids, int64_t T, int64_t K, int64_t E, int32_t* counts, int32_t* offsets,
                     int32_t* row_of, void* workspace, size_t ws_bytes, mx_stream_t stream) {
     if (T < 0 || K <= 0 || E <= 0) return MX_ERR_INVALID_ARG;
@@ -297,6 +312,14 @@ int moe_mxfp4_route(const int32_t* topk_ids, int64_t T, int64_t K, int64_t E, in
 int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
                       const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T, int64_t H,
                       int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream) {
+    return moe_mxfp4_forward_timed(x, topk_ids, topk_w, w13, s13, w2, s2, out, T, H, I, E, K, workspace, ws_bytes,
+                                   stream, nullptr);
+}
+
+int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                            const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T,
+                            int64_t H, int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                            mx_stream_t stream, void* const* events) {
     const bool routed = topk_ids != nullptr;
     if (routed != (topk_w != nullptr)) return MX_ERR_INVALID_ARG;
     if (int e = check_moe_dims(T, H, I, E, K, routed)) return e;
@@ -311,6 +334,9 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
     DeviceInfo* d;
     if (int e = device_info(&d)) return e;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto mark = [&](int i) -> bool {
+        return !(events && events[i]) || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+    };
     uint8_t* xq = at<uint8_t>(workspace, L.xq);
     uint8_t* xs = at<uint8_t>(workspace, L.xs);
     uint8_t* hq = at<uint8_t>(workspace, L.hq);
@@ -320,9 +346,10 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
     GemmArgs g1 = base_args(xs, s13, H, R, E * 2 * I, d->status);
     GemmArgs g2 = base_args(hs, s2, I, R, E * H, d->status);
     RouteBufs rb{};
+    if (!mark(0)) return MX_ERR_CUDA;
     if (routed) {
         rb = route_bufs(workspace, L);
-        if (launch_route(topk_ids, T, K, E, rb, s) != cudaSuccess) return MX_ERR_CUDA;
+        if (launch_route(topk_ids, T, K, E, rb, s) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
         if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s) != cudaSuccess)
             return MX_ERR_CUDA;
         for (GemmArgs* g : {&g1, &g2}) {
@@ -332,6 +359,7 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
             g->num_mtiles_dev = rb.num_mtiles;
         }
     } else {
+        if (!mark(1)) return MX_ERR_CUDA;
         if (launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s) != cudaSuccess)
             return MX_ERR_CUDA;
         for (GemmArgs* g : {&g1, &g2}) {
@@ -339,6 +367,7 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
             g->m_total = T;
         }
     }
+    if (!mark(2)) return MX_ERR_CUDA;
     const int64_t max_mtiles = L.max_mtiles;
 
     // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
@@ -352,7 +381,7 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
     g1.hs = hs;
     g1.ld_hq = I / 2;
     g1.ld_hs = I / 32;
-    if (launch_gemm_l1(ta1, tb1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), s) != cudaSuccess)
+    if (launch_gemm_l1(ta1, tb1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), s) != cudaSuccess || !mark(3))
         return MX_ERR_CUDA;
 
     // L2: [R, I] x [H, I]^T per expert, BF16 out (to `out` directly without routing).
@@ -362,7 +391,7 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
     g2.n_valid = H;
     g2.y = routed ? at<uint16_t>(workspace, L.y) : static_cast<uint16_t*>(out);
     g2.ld_y = H;
-    if (launch_gemm_l2(ta2, tb2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), s) != cudaSuccess)
+    if (launch_gemm_l2(ta2, tb2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), s) != cudaSuccess || !mark(4))
         return MX_ERR_CUDA;
 
     if (routed) {
@@ -370,7 +399,7 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
                            d->num_sms, s) != cudaSuccess)
             return MX_ERR_CUDA;
     }
-    return MX_OK;
+    return mark(5) ? MX_OK : MX_ERR_CUDA;
 }
 
 }  // extern "C"

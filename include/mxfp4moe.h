@@ -118,6 +118,22 @@ size_t moe_mxfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int6
                                 int routed);
 
 /*
+ * moe_mxfp4_workspace_layout -- byte offsets, inside that workspace, of the intermediate
+ * tensors a moe_mxfp4_forward call leaves behind (for inspection and tests; the layout may
+ * change between library versions). R = T*K when routed, T otherwise. Writes 8 values:
+ *   out[0] xq  uint8  [R, H/2]   MX-quantised x (routed: rows in expert-grouped order)
+ *   out[1] xs  uint8  [R, H/32]  its E8M0 scales
+ *   out[2] hq  uint8  [R, I/2]   MX-re-quantised h = bf16(silu(g) * u)
+ *   out[3] hs  uint8  [R, I/32]  its E8M0 scales
+ *   out[4] y   uint16 [R, H]     BF16 L2 output (routed mode; -1 otherwise)
+ *   out[5] row_of int32 [T, K], out[6] counts int32 [E], out[7] offsets int32 [E+1]
+ *          (routed mode; -1 otherwise)
+ * Returns MX_OK, or the status moe_mxfp4_forward would return for these sizes.
+ */
+int moe_mxfp4_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed,
+                               int64_t* out);
+
+/*
  * moe_mxfp4_forward -- the MoE expert FFN over MXFP4 weights ([PIPE], [BF16]):
  *   xq = act_quant(x);
  *   for each routed pair (t, k) with e = topk_ids[t, k] in [0, E):
@@ -141,6 +157,20 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
                       const uint8_t* s2, void* out, int64_t T, int64_t H, int64_t I,
                       int64_t E, int64_t K, void* workspace, size_t ws_bytes,
                       mx_stream_t stream);
+
+/*
+ * moe_mxfp4_forward_timed -- moe_mxfp4_forward that also records caller-created
+ * cudaEvent_t handles on `stream` at its phase boundaries, for profiling:
+ *   events[0] before the first launch, events[1] after the routing permutation,
+ *   events[2] after the MX quantisation of x, events[3] after the L1 GEMM,
+ *   events[4] after the L2 GEMM, events[5] after the weighted combine.
+ * `events` may be NULL and any entry may be NULL. Same arguments and errors otherwise.
+ */
+int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float* topk_w,
+                            const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
+                            const uint8_t* s2, void* out, int64_t T, int64_t H, int64_t I,
+                            int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                            mx_stream_t stream, void* const* events);
 
 /*
  * moe_mxfp4_route -- the routing permutation step of moe_mxfp4_forward on its own

@@ -17,8 +17,12 @@ from .mxfp4_oracle import (  # noqa: F401
     mxfp4_gemm_blockint,
     mxfp4_gemm_bf16,
     mxfp4_values,
+    moe_combine,
     moe_forward,
+    moe_l1_exact,
+    moe_l2_bf16,
     moe_route,
+    swiglu_bf16,
     moe_flops_per_pair,
     unpack_nibbles,
 )

@@ -65,7 +65,7 @@ __all__ = [
     "e2m1_decode", "e8m0_decode", "e4m3fn_decode", "bf16_bits_from_f64", "bf16_bits_to_f64",
     "unpack_nibbles", "mxfp4_values", "mxfp4_dequant", "fp8_block_dequant_128x128",
     "act_quant_mxfp4", "mxfp4_gemm_bf16", "mxfp4_gemm_blockint", "moe_route", "moe_forward",
-    "moe_flops_per_pair",
+    "moe_flops_per_pair", "moe_l1_exact", "swiglu_bf16", "moe_l2_bf16", "moe_combine",
 ]
 
 # --------------------------------------------------------------------------------------
@@ -319,17 +319,47 @@ def _silu(z):
     return z / (1.0 + np.exp(-z))
 
 
-def _expert_ffn(xq_vals, w13_e, s13_e, w2_e, s2_e, I):
-    """One expert on a block of rows: returns y as float64 values of BF16 numbers."""
+def moe_l1_exact(xq_vals, w13_e, s13_e, I: int):
+    """Exact L1 of one expert: (g, u) as float64 [n, I] each, gate = rows [0, I) (R4)."""
     W13 = mxfp4_values(w13_e, s13_e)                     # [2I, H]
     gu = xq_vals @ W13.T                                 # exact
-    g = bf16_bits_to_f64(bf16_bits_from_f64(gu[:, :I]))  # gate = rows [0, I)   (R4)
-    u = bf16_bits_to_f64(bf16_bits_from_f64(gu[:, I:]))  # up   = rows [I, 2I)
+    return gu[:, :I], gu[:, I:]
+
+
+def swiglu_bf16(g, u):
+    """h = bf16( silu(bf16(g)) * bf16(u) ) from exact g, u (R3); BF16 bits [n, I]."""
+    gb = bf16_bits_to_f64(bf16_bits_from_f64(g))
+    ub = bf16_bits_to_f64(bf16_bits_from_f64(u))
     with np.errstate(over="ignore"):
-        h_bits = bf16_bits_from_f64(_silu(g) * u)        # BF16 activation      (R3)
-    hq, hs = act_quant_mxfp4(h_bits)                     # re-quant             (R2)
+        return bf16_bits_from_f64(_silu(gb) * ub)
+
+
+def moe_l2_bf16(hq, hs, w2_e, s2_e):
+    """y = bf16( hq . w2^T ) exactly rounded (R3); BF16 bits [n, H]."""
     W2 = mxfp4_values(w2_e, s2_e)                        # [H, I]
-    return bf16_bits_to_f64(bf16_bits_from_f64(mxfp4_values(hq, hs) @ W2.T))
+    return bf16_bits_from_f64(mxfp4_values(hq, hs) @ W2.T)
+
+
+def moe_combine(y_slots, ids, wts, E: int):
+    """out[t] = bf16( sum_k w[t, k] * y[t, k] ) over valid slots, float64 sum (R5).
+
+    y_slots float64 [n, K, H] (values of BF16 numbers), ids int [n, K], wts float32 [n, K].
+    """
+    ids = np.asarray(ids, dtype=np.int64)
+    wts = np.asarray(wts, dtype=np.float32).astype(np.float64)
+    n, K = ids.shape
+    acc = np.zeros((n, y_slots.shape[-1]), dtype=np.float64)
+    for k in range(K):                                   # slot order
+        live = (ids[:, k] >= 0) & (ids[:, k] < E)
+        acc += np.where(live[:, None], wts[:, k:k + 1] * y_slots[:, k], 0.0)
+    return bf16_bits_from_f64(acc)
+
+
+def _expert_ffn(xq_vals, w13_e, s13_e, w2_e, s2_e, I):
+    """One expert on a block of rows: returns y as float64 values of BF16 numbers."""
+    g, u = moe_l1_exact(xq_vals, w13_e, s13_e, I)
+    hq, hs = act_quant_mxfp4(swiglu_bf16(g, u))          # re-quant             (R2)
+    return bf16_bits_to_f64(moe_l2_bf16(hq, hs, w2_e, s2_e))
 
 
 def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, I: int, tokens=None):
@@ -352,7 +382,6 @@ def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, I: int, tokens=None)
         y = _expert_ffn(xv, w13[0], s13[0], w2[0], s2[0], I)
         return bf16_bits_from_f64(y)
     ids = np.asarray(topk_ids, dtype=np.int64)[tok]
-    wts = np.asarray(topk_w, dtype=np.float32)[tok].astype(np.float64)
     n, K = ids.shape
     Y = np.zeros((n, K, H), dtype=np.float64)
     for e in range(E):
@@ -360,8 +389,4 @@ def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, I: int, tokens=None)
         if sel.size == 0:
             continue
         Y[sel[:, 0], sel[:, 1]] = _expert_ffn(xv[sel[:, 0]], w13[e], s13[e], w2[e], s2[e], I)
-    acc = np.zeros((n, H), dtype=np.float64)
-    for k in range(K):                                   # slot order          (R5)
-        live = (ids[:, k] >= 0) & (ids[:, k] < E)
-        acc += np.where(live[:, None], wts[:, k:k + 1] * Y[:, k], 0.0)
-    return bf16_bits_from_f64(acc)
+    return moe_combine(Y, ids, np.asarray(topk_w, dtype=np.float32)[tok], E)

@@ -1,0 +1,157 @@
+"""Step-by-step parity of a moe_mxfp4_forward run against the oracle.
+
+The forward leaves its intermediates in the workspace (moe_mxfp4_workspace_layout), so
+every step is checked where it happens:
+
+1. the first MX quantisation of x (xq, xs): bit-exact;
+2. the re-quantisation of h = bf16(silu(g) * u): the GPU accumulates g and u in float32,
+   the oracle exactly, so an h that sits within that rounding of a BF16 or E2M1 decision
+   boundary may legitimately land on either side. Each GPU block (scale + 32 codes) must be
+   the MX quantisation of some h' whose elements lie in the interval that the float32
+   accumulation allowance and float32 SiLU allow around the oracle's h (decisions that
+   the oracle pins uniquely must match exactly);
+3. y (L2, BF16): within one BF16 rounding plus the float32 accumulation allowance of the
+   exact product of the GPU's own hq with w2;
+4. out: per element |err| <= 2e-2 * max|ref| + 1e-3 and cosine >= 0.9999 against the
+   oracle run on the same decisions (the GPU's hq), and cosine >= 0.9999 against the
+   unconditioned oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from oracle.mxfp4_oracle import _e2m1_round_magnitude
+from gpu_util import MOE_COS, assert_gemm_close, assert_moe_close, bf16_host, bits_to_f64, cosine
+
+ACC_ALLOW = 2.0 ** -14      # float32 accumulation allowance, relative to sum |a||b|
+SILU_ALLOW = 2.0 ** -20     # float32 SiLU / product allowance, relative
+
+
+def _ws_view(ws, off, rows, cols, dtype=None):
+    import torch
+    t = ws[off: off + rows * cols * (2 if dtype == "bf16" else 4 if dtype == "i32" else 1)]
+    if dtype == "bf16":
+        return t.view(torch.int16).view(rows, cols).cpu().numpy().view(np.uint16)
+    if dtype == "i32":
+        return t.view(torch.int32).view(rows, cols).cpu().numpy()
+    return t.view(rows, cols).cpu().numpy()
+
+
+def _signed_code_value(mag_code, neg):
+    return np.where(neg, -1.0, 1.0) * oracle.e2m1_decode(mag_code.astype(np.int64))
+
+
+def check_requant_decisions(g, u, absg, absu, hq_gpu, hs_gpu):
+    """Step 2. Returns (blocks, blocks differing from the oracle's own decision)."""
+    n, I = g.shape
+    to = oracle.bf16_bits_to_f64
+    fr = oracle.bf16_bits_from_f64
+    eg, eu = absg * ACC_ALLOW, absu * ACC_ALLOW
+    gs = [to(fr(g - eg)), to(fr(g + eg))]
+    us = [to(fr(u - eu)), to(fr(u + eu))]
+    with np.errstate(over="ignore"):
+        corners = np.stack([gg / (1.0 + np.exp(-gg)) * uu for gg in gs for uu in us])
+    lo = corners.min(0)
+    hi = corners.max(0)
+    lo = lo - np.abs(lo) * SILU_ALLOW
+    hi = hi + np.abs(hi) * SILU_ALLOW
+    h_lo, h_hi = to(fr(lo)), to(fr(hi))                 # extreme BF16 candidates of h
+    # scale byte range over the candidates
+    mag_lo = np.where((h_lo <= 0) & (h_hi >= 0), 0.0, np.minimum(np.abs(h_lo), np.abs(h_hi)))
+    mag_hi = np.maximum(np.abs(h_lo), np.abs(h_hi))
+    nb = I // 32
+
+    def scale_byte(amax):
+        _, e = np.frexp(amax)
+        return np.where(amax > 0, np.clip(e - 1 - 2 + 127, 0, 254), 0)
+
+    E_lo = scale_byte(mag_lo.reshape(n, nb, 32).max(-1))
+    E_hi = scale_byte(mag_hi.reshape(n, nb, 32).max(-1))
+    hs = hs_gpu.astype(np.int64)
+    bad_scale = (hs < E_lo) | (hs > E_hi) | (hs == 255)
+    assert not bad_scale.any(), (f"re-quant scale outside the admissible range at "
+                                 f"{np.argwhere(bad_scale)[0].tolist()}")
+    mult = np.repeat(np.ldexp(1.0, 127 - hs), 32, axis=1)
+    nib = oracle.unpack_nibbles(hq_gpu)
+    v_gpu = _signed_code_value(nib & 7, (nib >> 3).astype(bool))
+
+    def qv(h):
+        s = h * mult
+        return _signed_code_value(_e2m1_round_magnitude(np.minimum(np.abs(s), 6.0)), np.signbit(s))
+
+    v_lo, v_hi = qv(h_lo), qv(h_hi)
+    bad = (v_gpu < np.minimum(v_lo, v_hi)) | (v_gpu > np.maximum(v_lo, v_hi))
+    assert not bad.any(), (f"re-quant code outside the admissible range at {np.argwhere(bad)[0].tolist()}: "
+                           f"gpu {v_gpu[bad][0]}, admissible [{v_lo[bad][0]}, {v_hi[bad][0]}]")
+    ref_q, ref_s = oracle.act_quant_mxfp4(oracle.swiglu_bf16(g, u))
+    differ = (ref_s != hs_gpu) | (oracle.unpack_nibbles(ref_q).reshape(n, nb, 32) !=
+                                  nib.reshape(n, nb, 32)).any(-1)
+    return n * nb, int(differ.sum())
+
+
+def check_moe_run(mx, d, tokens=None) -> dict:
+    """d: a test `Dev` holding the device inputs, output and workspace of a finished run."""
+    inp = d.inp
+    T, H, I, E, K = inp.T, inp.H, inp.I, inp.E, inp.K
+    routed = inp.topk_ids is not None
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    L = mx.moe_mxfp4_workspace_layout(T, H, I, E, K, routed)
+    R = T * K if routed else T
+    out_gpu = bf16_host(d.out)[tok]
+    ids = inp.topk_ids[tok].astype(np.int64) if routed else np.zeros((tok.size, 1), np.int64)
+    if routed:
+        row_of = _ws_view(d.ws, L["row_of"], T, K, "i32")[tok]
+    else:
+        row_of = tok[:, None]
+
+    # 1. first quantisation, bit-exact
+    xq_ref, xs_ref = oracle.act_quant_mxfp4(inp.x[tok])
+    xq_all = _ws_view(d.ws, L["xq"], R, H // 2)
+    xs_all = _ws_view(d.ws, L["xs"], R, H // 32)
+    hq_all = _ws_view(d.ws, L["hq"], R, I // 2)
+    hs_all = _ws_view(d.ws, L["hs"], R, I // 32)
+    y_all = _ws_view(d.ws, L["y"], R, H, "bf16") if routed else None
+    for j in range(ids.shape[1]):
+        live = (ids[:, j] >= 0) & (ids[:, j] < E)
+        rows = row_of[live, j]
+        np.testing.assert_array_equal(xq_all[rows], xq_ref[live], err_msg="xq")
+        np.testing.assert_array_equal(xs_all[rows], xs_ref[live], err_msg="xs")
+    xv = oracle.mxfp4_values(xq_ref, xs_ref)
+
+    blocks = differ = 0
+    y_cond = np.zeros((tok.size, ids.shape[1], H))
+    for e in range(E):
+        sel = np.argwhere((ids == e))
+        if sel.size == 0:
+            continue
+        i_s, k_s = sel[:, 0], sel[:, 1]
+        rows = row_of[i_s, k_s]
+        W13 = oracle.mxfp4_values(inp.w13[e], inp.s13[e])
+        gu = xv[i_s] @ W13.T
+        agu = np.abs(xv[i_s]) @ np.abs(W13).T
+        del W13
+        b, dff = check_requant_decisions(gu[:, :I], gu[:, I:], agu[:, :I], agu[:, I:], hq_all[rows], hs_all[rows])
+        blocks += b
+        differ += dff
+        # 3. L2 on the GPU's own decisions
+        W2 = oracle.mxfp4_values(inp.w2[e], inp.s2[e])
+        hv = oracle.mxfp4_values(hq_all[rows], hs_all[rows])
+        exact = hv @ W2.T
+        if routed:
+            assert_gemm_close(y_all[rows], exact, np.abs(hv) @ np.abs(W2).T, f"L2 expert {e}")
+        y_cond[i_s, k_s] = oracle.bf16_bits_to_f64(oracle.bf16_bits_from_f64(exact))
+    # 4. output against the oracle on the same decisions
+    if routed:
+        ref_cond = oracle.moe_combine(y_cond, ids, inp.topk_w[tok], E)
+        stats = assert_moe_close(out_gpu, ref_cond, "out vs oracle on the GPU's re-quant decisions")
+    else:
+        stats = assert_moe_close(out_gpu, oracle.bf16_bits_from_f64(y_cond[:, 0]),
+                                 "out vs oracle on the GPU's re-quant decisions")
+    ref = oracle.moe_forward(inp.x, inp.topk_ids, inp.topk_w, inp.w13, inp.s13, inp.w2, inp.s2, I, tokens=tok)
+    cos = cosine(bits_to_f64(out_gpu), bits_to_f64(ref))
+    assert cos >= MOE_COS, f"cosine vs the unconditioned oracle {cos:.6f} < {MOE_COS}"
+    err = np.abs(bits_to_f64(out_gpu) - bits_to_f64(ref))
+    stats.update(requant_blocks=blocks, requant_blocks_differing=differ, e2e_cos=cos,
+                 e2e_max_err=float(err.max()), e2e_bound=float(2e-2 * np.abs(bits_to_f64(ref)).max() + 1e-3))
+    return stats

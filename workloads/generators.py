@@ -48,17 +48,22 @@ CONFIGS = {
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 draws to bfloat16 (nearest, ties to even) and return the bit patterns."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    nan = np.isnan(x)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    out = u.astype(np.uint16)
-    out[nan] = 0x7FC0
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    r = (u >> 16) & 1                      # finite values never overflow 32 bits below
+    r += 0x7FFF
+    r += u
+    r >>= 16
+    out = r.astype(np.uint16)
+    out[np.isnan(x)] = 0x7FC0
     return out
 
 
 def _uniform_bytes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Uniform bytes: the generator's raw 64-bit outputs, little-endian, 8 bytes each."""
     n = int(np.prod(shape))
-    return np.frombuffer(rng.bytes(n), dtype=np.uint8).reshape(shape).copy()
+    raw = rng.bit_generator.random_raw((n + 7) // 8).astype("<u8", copy=False)
+    return raw.view(np.uint8)[:n].reshape(shape)
 
 
 def _softmax_f32(logits: np.ndarray) -> np.ndarray:
