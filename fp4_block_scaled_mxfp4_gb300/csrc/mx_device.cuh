@@ -225,6 +225,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+// Arrive on `bar` once every cp.async this thread issued before has completed; the
+// arrival counts toward the barrier's expected count (which must include it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

@@ -16,7 +16,9 @@
 //   warp 1      allocates 512 TMEM columns; lane 0 moves the stage's scale factors from
 //               shared to tensor memory (tcgen05.cp) and issues 4 MMAs of K = 64.
 //   warps 2, 3  scale-factor loaders for A and B: cp.async from the plain row-major
-//               [rows, K/32] scale tensors into the 32-lane x 16-byte blocks tcgen05.cp reads.
+//               [rows, K/32] scale tensors into the 32-lane x 16-byte blocks tcgen05.cp reads;
+//               each lane's copies arrive on the stage's full barrier when they land
+//               (cp.async.mbarrier.arrive), so the loaders never block on completion.
 //   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, each owning half of the
 //               columns; they drain the accumulator to registers, release it, then compute.
 // TMEM: columns [0, 256) accumulator; [256 + 24 s, 256 + 24 s + 24) the scale factors of
@@ -38,7 +40,7 @@ constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 51 KB
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemBase = 256;
 constexpr int kSfColsPerStage = 24;
-constexpr int kSfLag = kStages - 1;                    // scale stages in flight per loader
+constexpr uint32_t kFullArrivals = 1 + 2 * 32;         // producer + every scale-loader lane
 constexpr uint32_t kIdesc = idesc_mxf4(kBM, kBN);
 static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&ctl->full[s]), 3);   // TMA producer + two scale loaders
+            mbar_init(smem_u32(&ctl->full[s]), kFullArrivals);
             mbar_init(smem_u32(&ctl->empty[s]), 1);  // MMA commit
         }
         mbar_init(smem_u32(&ctl->tmem_full), 1);
@@ -184,6 +186,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                // the scale tiles were written by cp.async (generic proxy); tcgen05.cp
+                // reads them through the async proxy
+                fence_proxy_async_smem();
                 if (lane == 0) {
                     const bool half = args.k_tail_half && (kt == k_tiles - 1);
                     const int nwords = half ? 1 : 2;
@@ -272,22 +277,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                     }
                 }
-                cp_async_commit();
-                if (it >= (uint32_t)kSfLag) {
-                    cp_async_wait<kSfLag>();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctl->full[(it - kSfLag) % kStages]));
-                }
+                cp_async_arrive_noinc(smem_u32(&ctl->full[s]));
             }
         }
         cp_async_wait<0>();
-        fence_proxy_async_smem();
         __syncwarp();
-        if (!aborted && !*abort_flag && lane == 0) {
-            const uint32_t first = it > (uint32_t)kSfLag ? it - kSfLag : 0;
-            for (uint32_t i = first; i < it; ++i) mbar_arrive(smem_u32(&ctl->full[i % kStages]));
-        }
     } else {
         // ---------------- epilogue warps 4..11 ----------------
         const int q = warp & 3;              // TMEM lane quarter this warp may access
