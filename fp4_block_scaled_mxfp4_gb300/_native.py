@@ -33,6 +33,8 @@ _SIGNATURES = {
     "moe_mxfp4_forward_timed": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
                                                _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
                                                _c_ptr, _c_ptr]),
+    "moe_mxfp4_forward_noalloc": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                                 _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr]),
     "moe_mxfp4_workspace_layout": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int, _c_ptr]),
     "moe_mxfp4_route": (ctypes.c_int, [_c_ptr, _c_i64, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
                                        ctypes.c_size_t, _c_ptr]),

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build", "mxfp4moe")
 LIB_PATH = os.path.join(PKG_DIR, "libmxfp4moe.so")
-SOURCES = ["mx_api.cu", "mx_gemm.cu", "mx_elementwise.cu", "mx_route.cu"]
+SOURCES = ["mx_api.cu", "mx_gemm.cu", "mx_elementwise.cu", "mx_route.cu", "mx_noalloc.cu"]
 HEADERS = ["mx_device.cuh", "mx_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -184,6 +184,36 @@ int moe_mxfp4_route(const int32_t* topk_ids, int64_t T, int64_t K, int64_t E,
                     int32_t* counts, int32_t* offsets, int32_t* row_of,
                     void* workspace, size_t ws_bytes, mx_stream_t stream);
 
+/* Bytes of the static device scratch area moe_mxfp4_forward_noalloc runs on (per device). */
+#define MXFP4MOE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * moe_mxfp4_forward_noalloc -- moe_mxfp4_forward for callers that cannot allocate device
+ * memory. The pages have no counterpart of this call; it exists for callers that receive
+ * only their input and output buffers and may not allocate any device memory themselves:
+ * a plugin or custom-op interface whose host framework owns every allocation and offers no
+ * workspace, code that must not pay cudaMalloc's implicit device-wide synchronisation, or
+ * a process whose device memory is entirely reserved by another allocator.
+ *   Same arguments, results and errors as moe_mxfp4_forward, minus the workspace: the
+ * call runs on a scratch area of MXFP4MOE_NOALLOC_SCRATCH_BYTES (32 MiB) that is a static
+ * array inside the library, present on every device that loads it until the process
+ * exits. The call itself allocates nothing.
+ *   Limit: when moe_mxfp4_workspace_size(T, H, I, E, K, topk_ids != NULL) exceeds
+ * MXFP4MOE_NOALLOC_SCRATCH_BYTES the call returns MX_ERR_WORKSPACE and launches nothing
+ * (for H = 7168, I = 3072, top-8 that is about 200 routed tokens; use moe_mxfp4_forward
+ * with a caller workspace for larger batches).
+ *   The first call on each device looks up the scratch area's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture. All calls on a device share the one scratch area and it keeps the last call's
+ * contents (no result depends on them): calls that may overlap on the GPU (different
+ * streams, or different host threads without ordering) race on it and must be serialised
+ * by the caller.
+ */
+int moe_mxfp4_forward_noalloc(const void* x, const int32_t* topk_ids, const float* topk_w,
+                              const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
+                              const uint8_t* s2, void* out, int64_t T, int64_t H, int64_t I,
+                              int64_t E, int64_t K, mx_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
