@@ -12,7 +12,8 @@ each rank processes its own batch; the timed region is bracketed by a barrier an
 device synchronisation and the slowest rank's time is used.
 
 `value` is the algorithmic TFLOP/s of the forward (132,120,576 FLOP per routed pair) with
-every input resident in HBM; `e2e` is the same metric through the C ABI with the step's
+every input resident in HBM and the weight scales in the GEMM's tile layout (converted
+once, at weight load, like the weights themselves); `e2e` is the same metric through the C ABI with the step's
 inputs copied from pinned host memory and the output copied back inside the timed region.
 `roofline` reports the L1 GEMM, timed live with CUDA events recorded by the library at
 its phase boundaries. `cpu_baseline` times the CPU oracle on a small token sample.
@@ -211,9 +212,18 @@ def run_ours(args):
     ws = torch.empty(mx.moe_mxfp4_workspace_size(T, H, I, E, K, True), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     n_phase = 6
+    # weight load: the weight scales go into the tile layout once (a weight-format transform)
+    s13t = torch.empty(mx.mxfp4_tiled_scales_bytes(E * 2 * I, H), dtype=torch.uint8, device=dev)
+    s2t = torch.empty(mx.mxfp4_tiled_scales_bytes(E * H, I), dtype=torch.uint8, device=dev)
+    mx.mxfp4_scales_to_tiled(s13.view(-1, H // 32), s13t)
+    mx.mxfp4_scales_to_tiled(s2.view(-1, I // 32), s2t)
 
-    def step(evs=None):
-        mx.moe_mxfp4_forward(x, ids, w, w13, s13, w2, s2, out, ws, stream=stream, events=evs)
+    def step(evs=None, tiled=True):
+        if tiled:
+            mx.moe_mxfp4_forward(x, ids, w, w13, s13t, w2, s2t, out, ws, stream=stream, events=evs,
+                                 scales_tiled=True)
+        else:
+            mx.moe_mxfp4_forward(x, ids, w, w13, s13, w2, s2, out, ws, stream=stream, events=evs)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -272,7 +282,7 @@ def run_ours(args):
         xin.copy_(hx, non_blocking=True)
         idin.copy_(hids, non_blocking=True)
         win.copy_(hw, non_blocking=True)
-        mx.moe_mxfp4_forward(xin, idin, win, w13, s13, w2, s2, out, ws, stream=stream)
+        mx.moe_mxfp4_forward(xin, idin, win, w13, s13t, w2, s2t, out, ws, stream=stream, scales_tiled=True)
         hout.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -299,6 +309,17 @@ def run_ours(args):
 
     # ---------------- context figures measured outside the timed step ----------------
     extra = {}
+    if rank == 0:
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            step(tiled=False)
+            p0.record(stream)
+            for _ in range(10):
+                step(tiled=False)
+            p1.record(stream)
+        torch.cuda.synchronize()
+        extra["forward_row_major_scales_ms"] = p0.elapsed_time(p1) / 10
     if rank == 0 and not args.no_extra:
         extra = measure_extra(mx, torch, dev, stream)
 
@@ -395,6 +416,11 @@ def measure_extra(mx, torch, dev, stream):
         ids = torch.from_numpy(inp.topk_ids).to(dev) if routed else None
         w = torch.from_numpy(inp.topk_w).to(dev) if routed else None
         W = [torch.from_numpy(a).to(dev) for a in (inp.w13, inp.s13, inp.w2, inp.s2)]
+        s13t = torch.empty(mx.mxfp4_tiled_scales_bytes(c["E"] * 2 * c["I"], c["H"]), dtype=torch.uint8, device=dev)
+        s2t = torch.empty(mx.mxfp4_tiled_scales_bytes(c["E"] * c["H"], c["I"]), dtype=torch.uint8, device=dev)
+        mx.mxfp4_scales_to_tiled(W[1].view(-1, c["H"] // 32), s13t)
+        mx.mxfp4_scales_to_tiled(W[3].view(-1, c["I"] // 32), s2t)
+        W = [W[0], s13t, W[2], s2t]
         out = torch.empty((c["T"], c["H"]), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(max(256, mx.moe_mxfp4_workspace_size(c["T"], c["H"], c["I"], c["E"], inp.K, routed)),
                          dtype=torch.uint8, device=dev)
@@ -402,7 +428,7 @@ def measure_extra(mx, torch, dev, stream):
 
         def fwd():
             flush.zero_()          # keep the weights out of L2 between repetitions
-            mx.moe_mxfp4_forward(x, ids, w, *W, out, ws, stream=stream)
+            mx.moe_mxfp4_forward(x, ids, w, *W, out, ws, stream=stream, scales_tiled=True)
 
         def only_flush():
             flush.zero_()

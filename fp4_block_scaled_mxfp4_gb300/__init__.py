@@ -17,5 +17,7 @@ from ._native import (  # noqa: F401
     moe_mxfp4_workspace_size,
     mxfp4_dequant,
     mxfp4_gemm_bf16,
+    mxfp4_scales_to_tiled,
+    mxfp4_tiled_scales_bytes,
     status_string,
 )

@@ -25,6 +25,8 @@ _SIGNATURES = {
     "mxfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "fp8_block_dequant_128x128": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "act_quant_mxfp4": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "mxfp4_tiled_scales_bytes": (ctypes.c_size_t, [_c_i64, _c_i64]),
+    "mxfp4_scales_to_tiled": (ctypes.c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "mxfp4_gemm_bf16": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_ptr]),
     "moe_mxfp4_workspace_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
     "moe_mxfp4_forward": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
@@ -32,7 +34,10 @@ _SIGNATURES = {
                                          _c_ptr]),
     "moe_mxfp4_forward_timed": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
                                                _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
-                                               _c_ptr, _c_ptr]),
+                                               _c_ptr, _c_ptr, ctypes.c_int]),
+    "moe_mxfp4_forward_tiled": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                               _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
+                                               _c_ptr]),
     "moe_mxfp4_forward_noalloc": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
                                                  _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr]),
     "moe_mxfp4_workspace_layout": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int, _c_ptr]),
@@ -141,8 +146,24 @@ def act_quant_mxfp4(x, codes, sf, stream=None) -> None:
     _check(lib().act_quant_mxfp4(_ptr(x), _ptr(codes), _ptr(sf), M, K, _stream(stream)), "act_quant_mxfp4")
 
 
-def mxfp4_gemm_bf16(a, sa, b, sb, d, stream=None) -> None:
-    """d = bf16(A . B^T) for MXFP4 A [M, K] (a u8 [M, K/2], sa [M, K/32]) and B [N, K]."""
+def mxfp4_tiled_scales_bytes(rows: int, cols: int) -> int:
+    return int(lib().mxfp4_tiled_scales_bytes(rows, cols))
+
+
+def mxfp4_scales_to_tiled(sf, out, stream=None) -> None:
+    """Scale tensor u8 [rows, cols/32] -> tile layout (u8, mxfp4_tiled_scales_bytes bytes)."""
+    import torch
+    rows, kb = sf.shape
+    _need(sf, torch.uint8, (rows, kb), "sf")
+    if out.dtype != torch.uint8 or out.numel() < mxfp4_tiled_scales_bytes(rows, 32 * kb) or not out.is_cuda:
+        raise ValueError("out: too small for the tile layout")
+    _check(lib().mxfp4_scales_to_tiled(_ptr(sf), _ptr(out), rows, 32 * kb, _stream(stream)),
+           "mxfp4_scales_to_tiled")
+
+
+def mxfp4_gemm_bf16(a, sa, b, sb_tiled, d, stream=None) -> None:
+    """d = bf16(A . B^T) for MXFP4 A [M, K] (a u8 [M, K/2], sa [M, K/32]) and B [N, K]
+    (b u8 [N, K/2], sb_tiled = mxfp4_scales_to_tiled of B's [N, K/32] scales)."""
     import torch
     M, half = a.shape
     N = b.shape[0]
@@ -150,7 +171,9 @@ def mxfp4_gemm_bf16(a, sa, b, sb, d, stream=None) -> None:
     _need(a, torch.uint8, (M, half), "a")
     _need(sa, torch.uint8, (M, K // 32), "sa")
     _need(b, torch.uint8, (N, half), "b")
-    _need(sb, torch.uint8, (N, K // 32), "sb")
+    sb = sb_tiled
+    if sb.dtype != torch.uint8 or sb.numel() < mxfp4_tiled_scales_bytes(N, K) or not sb.is_cuda:
+        raise ValueError("sb_tiled: expected the tile layout of B's scales")
     _need(d, d.dtype, (M, N), "d")
     _check(lib().mxfp4_gemm_bf16(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(d), M, N, K, _stream(stream)),
            "mxfp4_gemm_bf16")
@@ -169,11 +192,15 @@ def moe_mxfp4_workspace_layout(T: int, H: int, I: int, E: int, K: int, routed: b
     return {n: int(v) for n, v in zip(names, buf)}
 
 
-def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, stream=None, events=None) -> None:
+def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, stream=None, events=None,
+                      scales_tiled=False) -> None:
     """MoE expert FFN over MXFP4 weights; topk_ids/topk_w None selects the shared expert.
 
-    ``events``: optional sequence of 6 torch.cuda.Event (or None) recorded at the phase
-    boundaries (before, after routing, after quantisation, after L1, after L2, after combine).
+    s13 / s2: the row-major E8M0 scales ([E, 2I, H/32], [E, H, I/32]), or with
+    scales_tiled=True their tile layout (mxfp4_scales_to_tiled; any uint8 buffer of that
+    size). ``events``: optional sequence of 6 torch.cuda.Event (or None) recorded at the
+    phase boundaries (before, after routing, after quantisation, after L1, after L2, after
+    combine).
     """
     import torch
     T, H = x.shape
@@ -185,20 +212,26 @@ def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, str
         _need(topk_ids, torch.int32, (T, K), "topk_ids")
         _need(topk_w, torch.float32, (T, K), "topk_w")
     _need(w13, torch.uint8, (E, 2 * I, H // 2), "w13")
-    _need(s13, torch.uint8, (E, 2 * I, H // 32), "s13")
     _need(w2, torch.uint8, (E, H, I // 2), "w2")
-    _need(s2, torch.uint8, (E, H, I // 32), "s2")
+    if scales_tiled:
+        for t, r, c, n in ((s13, E * 2 * I, H, "s13"), (s2, E * H, I, "s2")):
+            if t.dtype != torch.uint8 or t.numel() < mxfp4_tiled_scales_bytes(r, c) or not t.is_cuda:
+                raise ValueError(f"{n}: expected the tile layout of the scales")
+    else:
+        _need(s13, torch.uint8, (E, 2 * I, H // 32), "s13")
+        _need(s2, torch.uint8, (E, H, I // 32), "s2")
     _need(out, out.dtype, (T, H), "out")
     ws_bytes = workspace.numel() * workspace.element_size()
-    if events is None:
-        _check(lib().moe_mxfp4_forward(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2),
-                                       _ptr(s2), _ptr(out), T, H, I, E, K, _ptr(workspace), ws_bytes,
-                                       _stream(stream)), "moe_mxfp4_forward")
-        return
-    evs = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else 0) for e in events])
-    _check(lib().moe_mxfp4_forward_timed(_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2),
-                                         _ptr(s2), _ptr(out), T, H, I, E, K, _ptr(workspace), ws_bytes,
-                                         _stream(stream), ctypes.addressof(evs)), "moe_mxfp4_forward_timed")
+    args = (_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(out),
+            T, H, I, E, K, _ptr(workspace), ws_bytes, _stream(stream))
+    if events is not None:
+        evs = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else 0) for e in events])
+        _check(lib().moe_mxfp4_forward_timed(*args, ctypes.addressof(evs), 1 if scales_tiled else 0),
+               "moe_mxfp4_forward_timed")
+    elif scales_tiled:
+        _check(lib().moe_mxfp4_forward_tiled(*args), "moe_mxfp4_forward_tiled")
+    else:
+        _check(lib().moe_mxfp4_forward(*args), "moe_mxfp4_forward")
 
 
 def moe_mxfp4_route(topk_ids, E: int, counts, offsets, row_of, workspace, stream=None) -> None:

@@ -73,6 +73,9 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Bytes of a scale tensor [rows, kb] in the tile layout (128-row groups x 4-byte K-words).
+size_t tiled_bytes(int64_t rows, int64_t kb) { return (size_t)((rows + 127) / 128) * (size_t)(kb / 4) * 512; }
+
 // Workspace layout shared by moe_mxfp4_forward and moe_mxfp4_route.
 struct WsLayout {
     int64_t R = 0, nchunks = 0, max_mtiles = 0;
@@ -157,6 +160,8 @@ GemmArgs base_args(const uint8_t* sfa, const uint8_t* sfb, int64_t K, int64_t a_
     g.ld_sf = K / 32;
     g.a_rows = a_rows;
     g.b_rows = b_rows;
+    g.b_groups = (b_rows + 127) / 128;
+    g.kw = K / 128;
     g.k_tiles = (int32_t)((K + kBK - 1) / kBK);
     g.k_tail_half = (K % kBK) != 0 ? 1 : 0;
     g.status = status;
@@ -239,6 +244,21 @@ int act_quant_mxfp4(const void* x_bf16, uint8_t* codes, uint8_t* sf, int64_t M, 
                                         static_cast<cudaStream_t>(stream)));
 }
 
+size_t mxfp4_tiled_scales_bytes(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols <= 0 || cols % 128) return 0;
+    return tiled_bytes(rows, cols / 32);
+}
+
+int mxfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t cols, mx_stream_t stream) {
+    if (rows < 0 || cols <= 0) return MX_ERR_INVALID_ARG;
+    if (cols % 128) return MX_ERR_UNSUPPORTED;
+    if (rows == 0) return MX_OK;
+    if (!sf || !out) return MX_ERR_INVALID_ARG;
+    if (!aligned16(sf) || !aligned16(out)) return MX_ERR_MISALIGNED;
+    if ((cols / 128 + 31) / 32 > 65535) return MX_ERR_UNSUPPORTED;
+    return cuda_status(launch_sf_tile(sf, out, rows, cols / 32, static_cast<cudaStream_t>(stream)));
+}
+
 int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb, void* d_bf16,
                     int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
     if (M < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
@@ -260,7 +280,7 @@ int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const
     g.n_valid = N;
     g.y = static_cast<uint16_t*>(d_bf16);
     g.ld_y = N;
-    return cuda_status(launch_gemm_l2(ta, tb, g, grid_for((int64_t)g.num_mtiles_host * g.n_tiles, d->num_sms),
+    return cuda_status(launch_gemm_l2(ta, tb, g, grid_for((int64_t)g.num_mtiles_host * g.n_tiles, d->num_sms), true,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -309,17 +329,14 @@ int moe_mxfp4_route(const int32_t* topk_ids, int64_t T, int64_t K, int64_t E, in
     return cuda_status(launch_quant_gather(nullptr, topk_ids, T, K, E, 0, rb, nullptr, nullptr, s));
 }
 
-int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
-                      const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T, int64_t H,
-                      int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream) {
-    return moe_mxfp4_forward_timed(x, topk_ids, topk_w, w13, s13, w2, s2, out, T, H, I, E, K, workspace, ws_bytes,
-                                   stream, nullptr);
-}
+}  // extern "C"
 
-int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
-                            const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T,
-                            int64_t H, int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes,
-                            mx_stream_t stream, void* const* events) {
+namespace {
+
+int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                 const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T, int64_t H,
+                 int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream,
+                 void* const* events, bool scales_tiled) {
     const bool routed = topk_ids != nullptr;
     if (routed != (topk_w != nullptr)) return MX_ERR_INVALID_ARG;
     if (int e = check_moe_dims(T, H, I, E, K, routed)) return e;
@@ -381,7 +398,8 @@ int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float*
     g1.hs = hs;
     g1.ld_hq = I / 2;
     g1.ld_hs = I / 32;
-    if (launch_gemm_l1(ta1, tb1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), s) != cudaSuccess || !mark(3))
+    if (launch_gemm_l1(ta1, tb1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), scales_tiled, s) != cudaSuccess ||
+        !mark(3))
         return MX_ERR_CUDA;
 
     // L2: [R, I] x [H, I]^T per expert, BF16 out (to `out` directly without routing).
@@ -391,7 +409,8 @@ int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float*
     g2.n_valid = H;
     g2.y = routed ? at<uint16_t>(workspace, L.y) : static_cast<uint16_t*>(out);
     g2.ld_y = H;
-    if (launch_gemm_l2(ta2, tb2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), s) != cudaSuccess || !mark(4))
+    if (launch_gemm_l2(ta2, tb2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), scales_tiled, s) != cudaSuccess ||
+        !mark(4))
         return MX_ERR_CUDA;
 
     if (routed) {
@@ -400,6 +419,33 @@ int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float*
             return MX_ERR_CUDA;
     }
     return mark(5) ? MX_OK : MX_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                      const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T, int64_t H,
+                      int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream) {
+    return forward_impl(x, topk_ids, topk_w, w13, s13, w2, s2, out, T, H, I, E, K, workspace, ws_bytes, stream,
+                        nullptr, false);
+}
+
+int moe_mxfp4_forward_tiled(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                            const uint8_t* s13_tiled, const uint8_t* w2, const uint8_t* s2_tiled, void* out,
+                            int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, void* workspace,
+                            size_t ws_bytes, mx_stream_t stream) {
+    return forward_impl(x, topk_ids, topk_w, w13, s13_tiled, w2, s2_tiled, out, T, H, I, E, K, workspace, ws_bytes,
+                        stream, nullptr, true);
+}
+
+int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                            const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T,
+                            int64_t H, int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                            mx_stream_t stream, void* const* events, int scales_tiled) {
+    return forward_impl(x, topk_ids, topk_w, w13, s13, w2, s2, out, T, H, I, E, K, workspace, ws_bytes, stream,
+                        events, scales_tiled != 0);
 }
 
 }  // extern "C"

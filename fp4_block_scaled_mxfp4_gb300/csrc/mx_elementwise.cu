@@ -139,7 +139,40 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
     }
 }
 
+// Scale tensor [rows, kb] (kb = K/32 bytes per row) -> tile layout: for row group g of 128
+// rows and K-word w (4 consecutive scale bytes), 512 bytes at ((g * kw) + w) * 512 holding,
+// at byte l * 16 + j * 4 + b, the scale of row g * 128 + 32 j + l and K block 4 w + b. That
+// is the 32-lane x 16-byte block tcgen05.cp copies into tensor memory. One CTA converts 128
+// rows x 32 K-words through shared memory; rows past the end read as 0.
+constexpr int kTileThreads = 128;
+__global__ void __launch_bounds__(kTileThreads) sf_tile_kernel(const uint8_t* __restrict__ sf,
+                                                               uint8_t* __restrict__ out, int64_t rows,
+                                                               int64_t kb) {
+    __shared__ uint32_t s_rows[128][33];             // 128 rows x 32 words (+1 against conflicts)
+    const int64_t g = blockIdx.x;                    // row group
+    const int64_t wc = (int64_t)blockIdx.y * 32;     // first K-word of this chunk
+    const int64_t kw = kb / 4;
+    const int nw = (int)(kw - wc < 32 ? kw - wc : 32);
+    const int t = threadIdx.x;
+    const int64_t row = g * 128 + t;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(sf + row * kb) + wc;
+    for (int w = 0; w < nw; ++w) s_rows[t][w] = row < rows ? __ldg(src + w) : 0u;
+    __syncthreads();
+    uint4* o = reinterpret_cast<uint4*>(out + ((g * kw) + wc) * 512);
+    for (int u = t; u < nw * 32; u += kTileThreads) {
+        const int w = u >> 5, l = u & 31;
+        o[u] = make_uint4(s_rows[l][w], s_rows[l + 32][w], s_rows[l + 64][w], s_rows[l + 96][w]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    const dim3 grid((unsigned)((rows + 127) / 128), (unsigned)((kb / 4 + 31) / 32));
+    sf_tile_kernel<<<grid, kTileThreads, 0, s>>>(sf, out, rows, kb);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, uint16_t* out, int64_t rows,
                                  int64_t cols, int num_sms, cudaStream_t s) {

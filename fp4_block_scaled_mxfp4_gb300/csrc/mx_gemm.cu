@@ -12,13 +12,20 @@
 //
 // CTA layout (384 threads, one CTA per SM, persistent over the tile list):
 //   warp 0      TMA producer: A tile (128 rows x 128 B) and B tile (256 rows x 128 B) per
-//               K stage of 256 elements, 128-byte swizzle, into a 4-stage ring.
-//   warp 1      allocates 512 TMEM columns; lane 0 moves the stage's scale factors from
-//               shared to tensor memory (tcgen05.cp) and issues 4 MMAs of K = 64.
-//   warps 2, 3  scale-factor loaders for A and B: cp.async from the plain row-major
-//               [rows, K/32] scale tensors into the 32-lane x 16-byte blocks tcgen05.cp reads;
-//               each lane's copies arrive on the stage's full barrier when they land
-//               (cp.async.mbarrier.arrive), so the loaders never block on completion.
+//               K stage of 256 elements, 128-byte swizzle, into a 4-stage ring; with B's
+//               scales in tile layout (kBTiled) also B's scale factors for the stage: two
+//               1 KB bulk copies (one per 128-row group).
+//   warp 1      allocates 512 TMEM columns; lane 0 issues the 4 MMAs (K = 64 each) of a
+//               stage and commits the stage free. Nothing else runs in that thread: the
+//               tensor core's instruction queue is short, and any other work between two
+//               MMAs leaves the pipe idle.
+//   warp 2      scale-factor loader: cp.async from the plain row-major [rows, K/32] scales
+//               of A (and of B when they are not in tile layout) into the 32-lane x 16-byte
+//               blocks tcgen05.cp reads; each lane's copies arrive on the stage's scale
+//               barrier when they land (cp.async.mbarrier.arrive), so it never blocks.
+//   warp 3      scale-factor copier: lane 0 waits for a stage's operands and scale tiles,
+//               moves the scales into that stage's TMEM slot (tcgen05.cp) and commits the
+//               copies to the stage's ready barrier, which the MMA thread waits on.
 //   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, each owning half of the
 //               columns; they drain the accumulator to registers, release it, then compute.
 // TMEM: columns [0, 256) accumulator; [256 + 24 s, 256 + 24 s + 24) the scale factors of
@@ -35,21 +42,26 @@ namespace {
 constexpr int kABytes = kBM * kBK / 2;                 // 16 KB
 constexpr int kBBytes = kBN * kBK / 2;                 // 32 KB
 constexpr int kSfaBytes = 2 * 512;                     // 2 K-words x (32 lanes x 16 B)
-constexpr int kSfbBytes = 2 * 2 * 512;                 // 2 K-words x 2 row groups of 128
+constexpr int kSfbBytes = 2 * 2 * 512;                 // 2 row groups of 128 x 2 K-words
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 51 KB, 1024-aligned
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemBase = 256;
 constexpr int kSfColsPerStage = 24;
-constexpr uint32_t kFullArrivals = 1 + 2 * 32;         // producer + every scale-loader lane
+constexpr uint32_t kFullArrivals = 1;                  // producer (TMA + bulk bytes)
+constexpr uint32_t kSfArrivals = 32;                   // every scale-loader lane
+constexpr uint32_t kDescStageStep = kStageBytes >> 4;  // stage stride in descriptor units
 constexpr uint32_t kIdesc = idesc_mxf4(kBM, kBN);
 static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 
 struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t sf_full[kStages];
+    uint64_t ready[kStages];
     uint64_t tmem_full;
     uint64_t tmem_empty;
     uint64_t drain;
+    uint64_t drain_cp;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -97,7 +109,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
-template <bool kL1>
+template <bool kL1, bool kBTiled>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmArgs args) {
@@ -115,10 +127,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), kFullArrivals);
             mbar_init(smem_u32(&ctl->empty[s]), 1);  // MMA commit
+            mbar_init(smem_u32(&ctl->sf_full[s]), kSfArrivals);
+            mbar_init(smem_u32(&ctl->ready[s]), 1);   // scale copier commit
         }
         mbar_init(smem_u32(&ctl->tmem_full), 1);
         mbar_init(smem_u32(&ctl->tmem_empty), 8);    // one arrive per epilogue warp
         mbar_init(smem_u32(&ctl->drain), 1);
+        mbar_init(smem_u32(&ctl->drain_cp), 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -149,7 +164,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         goto producer_done;
                     const uint32_t st = sbase + s * kStageBytes;
                     const uint32_t bar = smem_u32(&ctl->full[s]);
-                    mbar_arrive_expect_tx(bar, kABytes + kBBytes);
+                    // B scale factors: K-words 2kt, 2kt+1 of each 128-row group (one at the K tail)
+                    const uint32_t sf_bytes = (args.k_tail_half && kt == k_tiles - 1) ? 512u : 1024u;
+                    int64_t grp[2];
+                    uint32_t tx = kABytes + kBBytes;
+                    if (kBTiled) {
+                        for (int h = 0; h < 2; ++h) {
+                            grp[h] = b_row<kL1>(args, t.expert, nt, h) / 128;
+                            if (grp[h] < args.b_groups) tx += sf_bytes;
+                        }
+                    }
+                    mbar_arrive_expect_tx(bar, tx);
+                    if (kBTiled) {
+                        for (int h = 0; h < 2; ++h)
+                            if (grp[h] < args.b_groups)
+                                bulk_load(st + kABytes + kBBytes + kSfaBytes + h * 1024,
+                                          args.sfb + (grp[h] * args.kw + 2 * kt) * 512, sf_bytes, bar);
+                    }
                     tma_load_2d(st, &tmA, kt * (kBK / 2), (int32_t)t.row0, bar);
                     if (kL1) {
                         tma_load_2d(st + kABytes, &tmB, kt * (kBK / 2), (int32_t)b_row<true>(args, t.expert, nt, 0), bar);
@@ -172,65 +203,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        uint32_t it = 0, tc = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            if (!warp_wait(smem_u32(&ctl->tmem_empty), (tc & 1u) ^ 1u, abort_flag, args.status, kErrWaitTmemEmpty))
-                break;
-            tc_fence_after();
-            bool ok = true;
-            for (int kt = 0; kt < k_tiles; ++kt, ++it) {
-                const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-                if (!warp_wait(smem_u32(&ctl->full[s]), ph, abort_flag, args.status, kErrWaitFull)) {
-                    ok = false;
+        // ---------------- MMA issuer (one thread) ----------------
+        if (lane == 0) {
+            const uint64_t adesc0 = desc_sw128(sbase);
+            const uint64_t bdesc0 = desc_sw128(sbase + kABytes);
+            const uint32_t sf0 = tmem + kSfTmemBase;
+            uint32_t it = 0, tc = 0;
+            for (int w = blockIdx.x; w < total; w += gridDim.x) {
+                if (!mbar_wait(smem_u32(&ctl->tmem_empty), (tc & 1u) ^ 1u, abort_flag, args.status,
+                               kErrWaitTmemEmpty))
                     break;
-                }
                 tc_fence_after();
-                // the scale tiles were written by cp.async (generic proxy); tcgen05.cp
-                // reads them through the async proxy
-                fence_proxy_async_smem();
-                if (lane == 0) {
-                    const bool half = args.k_tail_half && (kt == k_tiles - 1);
-                    const int nwords = half ? 1 : 2;
-                    const int nmma = half ? 2 : 4;
-                    const uint32_t st = sbase + s * kStageBytes;
-                    const uint32_t sfa_s = st + kABytes + kBBytes;
-                    const uint32_t sfb_s = sfa_s + kSfaBytes;
-                    const uint32_t sfa_t = tmem + kSfTmemBase + s * kSfColsPerStage;
-                    const uint32_t sfb_t = sfa_t + 8;
-                    for (int wd = 0; wd < nwords; ++wd) {
-                        tc_cp_32x128b_x4(sfa_t + 4 * wd, desc_sf(sfa_s + wd * 512));
-                        tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 1024));
-                        tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + wd * 1024 + 512));
+                bool ok = true;
+                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                    if (!mbar_wait(smem_u32(&ctl->ready[s]), ph, abort_flag, args.status, kErrWaitFull)) {
+                        ok = false;
+                        break;
                     }
-                    const uint64_t adesc = desc_sw128(st);
-                    const uint64_t bdesc = desc_sw128(st + kABytes);
-                    for (int j = 0; j < nmma; ++j) {
-                        const uint32_t id = 2u * (j & 1);
-                        // advance 64 E2M1 elements (32 bytes) along K inside the swizzle atom
-                        tc_mma_mxf4(tmem, adesc + (uint64_t)(2 * j), bdesc + (uint64_t)(2 * j),
-                                    idesc_with_sf_ids(kIdesc, id, id), sfa_t + 4 * (j >> 1),
-                                    sfb_t + 8 * (j >> 1), (kt | j) != 0);
+                    tc_fence_after();
+                    const uint64_t adesc = adesc0 + (uint64_t)(s * kDescStageStep);
+                    const uint64_t bdesc = bdesc0 + (uint64_t)(s * kDescStageStep);
+                    const uint32_t sfa = sf0 + s * kSfColsPerStage;
+                    const uint32_t sfb = sfa + 8;
+                    const uint32_t acc0 = kt != 0;
+                    // 64 E2M1 elements (32 bytes) of K per MMA, inside the 128-byte swizzle atom
+                    tc_mma_mxf4(tmem, adesc, bdesc, idesc_with_sf_ids(kIdesc, 0, 0), sfa, sfb, acc0);
+                    tc_mma_mxf4(tmem, adesc + 2, bdesc + 2, idesc_with_sf_ids(kIdesc, 2, 2), sfa, sfb, 1);
+                    if (!(args.k_tail_half && kt == k_tiles - 1)) {
+                        tc_mma_mxf4(tmem, adesc + 4, bdesc + 4, idesc_with_sf_ids(kIdesc, 0, 0), sfa + 4, sfb + 8, 1);
+                        tc_mma_mxf4(tmem, adesc + 6, bdesc + 6, idesc_with_sf_ids(kIdesc, 2, 2), sfa + 4, sfb + 8, 1);
                     }
                     tc_commit(smem_u32(&ctl->empty[s]));
                 }
-                __syncwarp();
+                if (!ok) break;
+                tc_commit(smem_u32(&ctl->tmem_full));
+                ++tc;
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(smem_u32(&ctl->tmem_full));
-            __syncwarp();
-            ++tc;
+            if (*abort_flag) {
+                // make sure no MMA still writes tensor memory before it is released
+                tc_commit(smem_u32(&ctl->drain));
+                volatile int never = 0;
+                mbar_wait(smem_u32(&ctl->drain), 0, &never, args.status, kErrWaitDrain);
+            }
         }
-        if (*abort_flag) {
-            // make sure no MMA still writes tensor memory before it is released
-            if (lane == 0) tc_commit(smem_u32(&ctl->drain));
-            __syncwarp();
-            volatile int never = 0;
-            mbar_wait(smem_u32(&ctl->drain), 0, &never, args.status, kErrWaitDrain);
-        }
-    } else if (warp == 2 || warp == 3) {
-        // ---------------- scale-factor loaders (warp 2: A, warp 3: B) ----------------
-        const bool is_a = (warp == 2);
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------- scale-factor loader (A; and B when its scales are row-major) --------
         uint32_t it = 0;
         bool aborted = false;
         for (int w = blockIdx.x; w < total && !aborted; w += gridDim.x) {
@@ -245,7 +264,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const bool half = args.k_tail_half && (kt == k_tiles - 1);
                 const uint32_t st = sbase + s * kStageBytes;
                 const int64_t kcol = (int64_t)kt * 8;   // first 32-element block of this stage
-                if (is_a) {
+                {
                     const uint32_t dst0 = st + kABytes + kBBytes + lane * 16;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -258,7 +277,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             cp_async_4(dst0 + wd * 512 + j * 4, ok ? src + 4 * wd : args.sfa, ok ? 4u : 0u);
                         }
                     }
-                } else {
+                }
+                if (!kBTiled) {
                     const uint32_t dst0 = st + kABytes + kBBytes + kSfaBytes + lane * 16;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -271,16 +291,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                             for (int wd = 0; wd < 2; ++wd) {
                                 const bool ok = valid && (wd == 0 || !half);
-                                cp_async_4(dst0 + wd * 1024 + h * 512 + j * 4, ok ? src + 4 * wd : args.sfb,
+                                cp_async_4(dst0 + h * 1024 + wd * 512 + j * 4, ok ? src + 4 * wd : args.sfb,
                                            ok ? 4u : 0u);
                             }
                         }
                     }
                 }
-                cp_async_arrive_noinc(smem_u32(&ctl->full[s]));
+                cp_async_arrive_noinc(smem_u32(&ctl->sf_full[s]));
             }
         }
         cp_async_wait<0>();
+        __syncwarp();
+    } else if (warp == 3) {
+        // ---------------- scale-factor copier (one thread) ----------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                for (int kt = 0; kt < k_tiles; ++kt, ++it) {
+                    const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+                    if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, args.status, kErrWaitFull) ||
+                        !mbar_wait(smem_u32(&ctl->sf_full[s]), ph, abort_flag, args.status, kErrWaitFull)) {
+                        ok = false;
+                        break;
+                    }
+                    // the scale tiles were written by cp.async (generic proxy); tcgen05.cp
+                    // reads them through the async proxy
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const int nwords = (args.k_tail_half && kt == k_tiles - 1) ? 1 : 2;
+                    const uint32_t sfa_s = sbase + s * kStageBytes + kABytes + kBBytes;
+                    const uint32_t sfb_s = sfa_s + kSfaBytes;
+                    const uint32_t sfa_t = tmem + kSfTmemBase + s * kSfColsPerStage;
+                    const uint32_t sfb_t = sfa_t + 8;
+                    for (int wd = 0; wd < nwords; ++wd) {
+                        tc_cp_32x128b_x4(sfa_t + 4 * wd, desc_sf(sfa_s + wd * 512));
+                        tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 512));          // rows 0-127
+                        tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + 1024 + wd * 512));  // 128-255
+                    }
+                    tc_commit(smem_u32(&ctl->ready[s]));   // arrives once the copies are in TMEM
+                }
+            }
+            if (*abort_flag) {
+                tc_commit(smem_u32(&ctl->drain_cp));
+                volatile int never = 0;
+                mbar_wait(smem_u32(&ctl->drain_cp), 0, &never, args.status, kErrWaitDrain);
+            }
+        }
         __syncwarp();
     } else {
         // ---------------- epilogue warps 4..11 ----------------
@@ -357,19 +414,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <bool kL1>
+template <bool kL1, bool kBTiled>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid, cudaStream_t s) {
     static int configured_mask = 0;   // one bit per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
-        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1, kBTiled>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)kSmemBytes);
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
-    mxf4_gemm_kernel<kL1><<<grid, kGemmThreads, kSmemBytes, s>>>(ta, tb, a);
+    mxf4_gemm_kernel<kL1, kBTiled><<<grid, kGemmThreads, kSmemBytes, s>>>(ta, tb, a);
     return cudaGetLastError();
 }
 
@@ -378,13 +435,13 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs&
 size_t gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                           cudaStream_t s) {
-    return launch<true>(ta, tb, a, grid, s);
+                           bool b_tiled, cudaStream_t s) {
+    return b_tiled ? launch<true, true>(ta, tb, a, grid, s) : launch<true, false>(ta, tb, a, grid, s);
 }
 
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                           cudaStream_t s) {
-    return launch<false>(ta, tb, a, grid, s);
+                           bool b_tiled, cudaStream_t s) {
+    return b_tiled ? launch<false, true>(ta, tb, a, grid, s) : launch<false, false>(ta, tb, a, grid, s);
 }
 
 }  // namespace mx

@@ -22,10 +22,13 @@ constexpr int kMaxTopK = 64;
 // Arguments of the expert GEMM kernels (plain data, copied into the kernel parameters).
 struct GemmArgs {
     const uint8_t* sfa;          // A scales [a_rows, K/32]
-    const uint8_t* sfb;          // B scales [b_rows, K/32]
+    const uint8_t* sfb;          // B scales: row-major [b_rows, K/32], or tile layout
+                                 // [b_rows/128][K/128][512 B] (b_tiled launches)
     int64_t ld_sf;               // K/32: scale bytes per row (A and B share K)
     int64_t a_rows;              // rows of A (bound for scale loads; TMA zero-fills beyond)
     int64_t b_rows;              // rows of the stacked B tensor
+    int64_t b_groups;            // 128-row groups of B's tiled scales
+    int64_t kw;                  // K/128: scale words per row
     int32_t k_tiles;             // ceil(K / 256)
     int32_t k_tail_half;         // 1 when the last stage holds only 128 of K
     // M tiles: from the routing tables (device) or uniform over m_total rows.
@@ -50,11 +53,13 @@ struct GemmArgs {
 
 size_t gemm_smem_bytes();
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                           cudaStream_t s);
+                           bool b_tiled, cudaStream_t s);
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                           cudaStream_t s);
+                           bool b_tiled, cudaStream_t s);
 
 // ---- element-wise kernels ----
+// Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][512 B] (kb % 4 == 0).
+cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s);
 cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, uint16_t* out, int64_t rows,
                                  int64_t cols, int num_sms, cudaStream_t s);
 cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* out, int64_t rows,

@@ -100,9 +100,23 @@ int act_quant_mxfp4(const void* x_bf16, uint8_t* codes, uint8_t* sf,
                     int64_t M, int64_t K, mx_stream_t stream);
 
 /*
+ * Tile layout of a scale tensor (the layout the GEMM's tensor-memory copies read).
+ * A scale tensor sf uint8 [rows, cols/32] (one E8M0 byte per 32 columns) becomes
+ * ceil(rows/128) x (cols/128) blocks of 512 bytes; block (g, w) sits at ((g*(cols/128)) + w)*512
+ * and holds at byte l*16 + j*4 + b the scale of row 128g + 32j + l, column block 4w + b
+ * (rows past the end are 0). The pages keep scales row-major; this is a re-ordering only.
+ *   mxfp4_tiled_scales_bytes: size of the tile layout (0 when cols is not a positive
+ *   multiple of 128). mxfp4_scales_to_tiled: converts on `stream`; cols % 128 == 0.
+ */
+size_t mxfp4_tiled_scales_bytes(int64_t rows, int64_t cols);
+int mxfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t cols,
+                          mx_stream_t stream);
+
+/*
  * mxfp4_gemm_bf16 -- D = bf16(A . B^T) with MXFP4 operands on the tcgen05 tensor cores:
  * the one-group case of the expert GEMM ([PIPE]: "num_groups=1 is just a regular GEMM").
- *   A codes uint8 [M, K/2] + sa [M, K/32]; B codes uint8 [N, K/2] + sb [N, K/32];
+ *   A codes uint8 [M, K/2] + sa [M, K/32] (row-major scales); B codes uint8 [N, K/2] + sb,
+ *   B's scales in the tile layout above (mxfp4_scales_to_tiled of [N, K/32]);
  *   D uint16 [M, N]. Accumulation is float32, the result is rounded once to BF16.
  *   K must be a positive multiple of 128, N a positive multiple of 16; M >= 0.
  */
@@ -159,7 +173,21 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
                       mx_stream_t stream);
 
 /*
- * moe_mxfp4_forward_timed -- moe_mxfp4_forward that also records caller-created
+ * moe_mxfp4_forward_tiled -- moe_mxfp4_forward with the weight scales already in the tile
+ * layout (s13_tiled = mxfp4_scales_to_tiled of s13 viewed as [E*2I, H/32]; s2_tiled of s2
+ * viewed as [E*H, I/32]). A weight-format transform done once when the weights are loaded;
+ * the GEMMs then fetch each stage's weight scales with two bulk copies instead of one small
+ * copy per row. Same arguments, results and errors otherwise.
+ */
+int moe_mxfp4_forward_tiled(const void* x, const int32_t* topk_ids, const float* topk_w,
+                            const uint8_t* w13, const uint8_t* s13_tiled, const uint8_t* w2,
+                            const uint8_t* s2_tiled, void* out, int64_t T, int64_t H, int64_t I,
+                            int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                            mx_stream_t stream);
+
+/*
+ * moe_mxfp4_forward_timed -- moe_mxfp4_forward (scales_tiled == 0) or
+ * moe_mxfp4_forward_tiled (scales_tiled != 0) that also records caller-created
  * cudaEvent_t handles on `stream` at its phase boundaries, for profiling:
  *   events[0] before the first launch, events[1] after the routing permutation,
  *   events[2] after the MX quantisation of x, events[3] after the L1 GEMM,
@@ -170,7 +198,7 @@ int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float*
                             const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
                             const uint8_t* s2, void* out, int64_t T, int64_t H, int64_t I,
                             int64_t E, int64_t K, void* workspace, size_t ws_bytes,
-                            mx_stream_t stream, void* const* events);
+                            mx_stream_t stream, void* const* events, int scales_tiled);
 
 /*
  * moe_mxfp4_route -- the routing permutation step of moe_mxfp4_forward on its own

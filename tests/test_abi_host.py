@@ -68,8 +68,17 @@ def test_dequant_validation(lib):
     assert lib.act_quant_mxfp4(FAKE, None, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
 
 
+def test_tiled_scales_validation(lib):
+    assert lib.mxfp4_tiled_scales_bytes(300, 7168) == 3 * 56 * 512
+    assert lib.mxfp4_tiled_scales_bytes(300, 7200) == 0
+    assert lib.mxfp4_scales_to_tiled(FAKE, FAKE, 4, 96, None) == MX_ERR_UNSUPPORTED
+    assert lib.mxfp4_scales_to_tiled(FAKE, None, 4, 128, None) == MX_ERR_INVALID_ARG
+    assert lib.mxfp4_scales_to_tiled(ODD, FAKE, 4, 128, None) == MX_ERR_MISALIGNED
+    assert lib.mxfp4_scales_to_tiled(FAKE, FAKE, 0, 128, None) == MX_OK
+
+
 def test_gemm_validation(lib):
-    assert lib.mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 192, None) == MX_ERR_UNSUPPORTED
+    assert lib.mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 192, None) == MX_ERR_UNSUPPORTED  # K % 128
     assert lib.mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 250, 256, None) == MX_ERR_UNSUPPORTED
     assert lib.mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 256, 256, None) == MX_OK
     assert lib.mxfp4_gemm_bf16(FAKE, FAKE, None, FAKE, FAKE, 4, 256, 256, None) == MX_ERR_INVALID_ARG

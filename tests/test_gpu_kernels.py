@@ -113,11 +113,38 @@ def test_act_quant_bit_exact(mx, M, K):
 
 # ----------------------------------------------------------------------------- GEMM
 
+def _tiled(mx, sb):
+    import torch
+    rows, kb = sb.shape
+    out = torch.empty(mx.mxfp4_tiled_scales_bytes(rows, 32 * kb), dtype=torch.uint8, device="cuda")
+    mx.mxfp4_scales_to_tiled(dev(sb), out)
+    return out
+
+
+def _tiled_layout_reference(sf):
+    """The tile layout written out with numpy indexing (block (g, w): byte l*16 + j*4 + b is
+    the scale of row 128g + 32j + l, K block 4w + b; rows past the end are 0)."""
+    rows, kb = sf.shape
+    G, KW = (rows + 127) // 128, kb // 4
+    padded = np.zeros((G * 128, kb), np.uint8)
+    padded[:rows] = sf
+    t = padded.reshape(G, 4, 32, KW, 4)          # g, j, l, w, b
+    return t.transpose(0, 3, 2, 1, 4).reshape(-1)  # g, w, l, j, b
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 128), (128, 7168), (300, 3072), (6144, 1024)])
+def test_scales_to_tiled_bit_exact(mx, rows, cols):
+    rng = np.random.default_rng(rows + cols)
+    sf = rng.integers(0, 256, size=(rows, cols // 32), dtype=np.uint8)
+    got = _tiled(mx, sf).cpu().numpy()
+    np.testing.assert_array_equal(got, _tiled_layout_reference(sf))
+
+
 def _gemm_case(mx, a, sa, b, sb, what):
     import torch
     M, N = a.shape[0], b.shape[0]
     d = _empty((M, N), torch.bfloat16)
-    mx.mxfp4_gemm_bf16(dev(a), dev(sa), dev(b), dev(sb), d)
+    mx.mxfp4_gemm_bf16(dev(a), dev(sa), dev(b), _tiled(mx, sb), d)
     A = oracle.mxfp4_values(a, sa)
     B = oracle.mxfp4_values(b, sb)
     exact = A @ B.T

@@ -42,9 +42,22 @@ class Dev:
         n = mx.moe_mxfp4_workspace_size(inp.T, inp.H, inp.I, inp.E, inp.K, self.ids is not None)
         self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
 
-    def run(self, mx, stream=None):
-        mx.moe_mxfp4_forward(self.x, self.ids, self.w, self.w13, self.s13, self.w2, self.s2, self.out,
-                             self.ws, stream=stream)
+    def run(self, mx, stream=None, tiled=False):
+        if tiled:
+            import torch
+            if not hasattr(self, "s13t"):
+                inp = self.inp
+                self.s13t = torch.empty(mx.mxfp4_tiled_scales_bytes(inp.E * 2 * inp.I, inp.H), dtype=torch.uint8,
+                                        device="cuda")
+                self.s2t = torch.empty(mx.mxfp4_tiled_scales_bytes(inp.E * inp.H, inp.I), dtype=torch.uint8,
+                                       device="cuda")
+                mx.mxfp4_scales_to_tiled(self.s13.view(-1, inp.H // 32), self.s13t)
+                mx.mxfp4_scales_to_tiled(self.s2.view(-1, inp.I // 32), self.s2t)
+            mx.moe_mxfp4_forward(self.x, self.ids, self.w, self.w13, self.s13t, self.w2, self.s2t, self.out,
+                                 self.ws, stream=stream, scales_tiled=True)
+        else:
+            mx.moe_mxfp4_forward(self.x, self.ids, self.w, self.w13, self.s13, self.w2, self.s2, self.out,
+                                 self.ws, stream=stream)
         return bf16_host(self.out)
 
 
@@ -105,18 +118,36 @@ def test_graph_replay_and_determinism(mx):
     np.testing.assert_array_equal(bf16_host(d.out), first)
 
 
+@pytest.mark.parametrize("name", ["tiny", "edge", "shared_small"])
+def test_tiled_scales_forward_is_bit_identical(mx, name):
+    """moe_mxfp4_forward_tiled (weight scales prepared once in tile layout) computes exactly
+    what moe_mxfp4_forward computes; only how the GEMMs fetch the weight scales differs."""
+    if name == "tiny":
+        inp = make_config_inputs("tiny")
+    elif name == "edge":
+        inp = make_moe_inputs(T=300, H=384, I=256, E=6, K=4, seed=7, routing="uniform")
+        inp.topk_ids[::7, 1] = -1
+    else:
+        inp = make_moe_inputs(T=200, H=256, I=256, E=1, K=1, seed=300, routing=None)
+    d = Dev(mx, inp)
+    plain = d.run(mx)
+    np.testing.assert_array_equal(d.run(mx, tiled=True), plain)
+
+
 def test_shared_config_full(mx):
     inp = make_config_inputs("shared")
     d = Dev(mx, inp)
-    d.run(mx)
+    plain = d.run(mx)
     print("shared expert T=256", check_moe_run(mx, d))
+    np.testing.assert_array_equal(d.run(mx, tiled=True), plain)
 
 
 def test_decode_config_sampled(mx):
     inp = make_config_inputs("decode")
     d = Dev(mx, inp)
-    d.run(mx)
+    plain = d.run(mx)
     print("decode", check_moe_run(mx, d, tokens=[0, 17, 42, 63]))
+    np.testing.assert_array_equal(d.run(mx, tiled=True), plain)
 
 
 def test_prefill_config_sampled(mx):
@@ -127,3 +158,4 @@ def test_prefill_config_sampled(mx):
     rng = np.random.default_rng(5)
     tokens = np.sort(rng.choice(inp.T, size=6, replace=False))
     print("prefill", check_moe_run(mx, d, tokens=tokens))
+    np.testing.assert_array_equal(d.run(mx, tiled=True), got)
