@@ -69,6 +69,18 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t inner_bytes, int64_t row
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// 2-D BF16 output [rows, cols] written in boxes of 32 rows x 32 columns (no swizzle).
+int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -270,8 +282,9 @@ int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const
         return MX_ERR_MISALIGNED;
     DeviceInfo* d;
     if (int e = device_info(&d)) return e;
-    CUtensorMap ta, tb;
-    if (make_tmap(&ta, a, K / 2, M, 128) || make_tmap(&tb, b, K / 2, N, 256)) return MX_ERR_CUDA;
+    CUtensorMap ta, tb, ty;
+    if (make_tmap(&ta, a, K / 2, M, 128) || make_tmap(&tb, b, K / 2, N, 256) || make_tmap_out(&ty, d_bf16, N, M))
+        return MX_ERR_CUDA;
     GemmArgs g = base_args(sa, sb, K, M, N, d->status);
     g.num_mtiles_host = (int32_t)((M + kBM - 1) / kBM);
     g.m_total = M;
@@ -280,7 +293,7 @@ int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const
     g.n_valid = N;
     g.y = static_cast<uint16_t*>(d_bf16);
     g.ld_y = N;
-    return cuda_status(launch_gemm_l2(ta, tb, g, grid_for((int64_t)g.num_mtiles_host * g.n_tiles, d->num_sms), true,
+    return cuda_status(launch_gemm_l2(ta, tb, ty, g, grid_for((int64_t)g.num_mtiles_host * g.n_tiles, d->num_sms), true,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -388,7 +401,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     const int64_t max_mtiles = L.max_mtiles;
 
     // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
-    CUtensorMap ta1, tb1, ta2, tb2;
+    CUtensorMap ta1, tb1, ta2, tb2, ty2;
     if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap(&tb1, w13, H / 2, E * 2 * I, 128)) return MX_ERR_CUDA;
     g1.n_tiles = (int32_t)(I / 128);
     g1.b_rows_per_expert = 2 * I;
@@ -409,7 +422,8 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     g2.n_valid = H;
     g2.y = routed ? at<uint16_t>(workspace, L.y) : static_cast<uint16_t*>(out);
     g2.ld_y = H;
-    if (launch_gemm_l2(ta2, tb2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), scales_tiled, s) != cudaSuccess ||
+    if (make_tmap_out(&ty2, g2.y, H, R)) return MX_ERR_CUDA;
+    if (launch_gemm_l2(ta2, tb2, ty2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), scales_tiled, s) != cudaSuccess ||
         !mark(4))
         return MX_ERR_CUDA;
 

@@ -49,6 +49,15 @@ __device__ __forceinline__ uint32_t f32_to_bf16(float f) {
 
 __device__ __forceinline__ float round_bf16(float f) { return bf16_to_f32(f32_to_bf16(f)); }
 
+// Two values to packed BF16 (a in the low half), round to nearest even; the hardware
+// conversion, with NaN written as sign | 0x7FC0 like f32_to_bf16.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    if (__builtin_expect(a != a || b != b, 0)) r = f32_to_bf16(a) | (f32_to_bf16(b) << 16);
+    return r;
+}
+
 // ------------------------------------------------------------------------------------
 // MX quantiser: shared exponent and E2M1 code (round to nearest even, saturating at 6)
 // ------------------------------------------------------------------------------------
@@ -219,6 +228,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+
+// 2-D TMA store shared -> global of one box; the shared source is read asynchronously
+// (bulk_wait_read before it is overwritten). Coordinates: x innermost, in elements.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(x),
+                 "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Bulk copy global -> shared (async proxy) completing `bytes` on the mbarrier; both
 // addresses 16-byte aligned, bytes a multiple of 16.

@@ -28,6 +28,10 @@
 //               copies to the stage's ready barrier, which the MMA thread waits on.
 //   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, each owning half of the
 //               columns; they drain the accumulator to registers, release it, then compute.
+//               L2 writes its BF16 output through a 2 KB shared staging block per warp and
+//               an asynchronous TMA store of 32 rows x 32 columns, so the warp never waits
+//               for its stores (32 scattered 16-byte row pieces per store instruction
+//               otherwise); a warp whose 32 rows are not all in the tile stores directly.
 // TMEM: columns [0, 256) accumulator; [256 + 24 s, 256 + 24 s + 24) the scale factors of
 // stage s (A: 2 K-words x 4 columns, B: 2 K-words x 8 columns).
 #include <cuda.h>
@@ -51,6 +55,8 @@ constexpr uint32_t kFullArrivals = 1;                  // producer (TMA + bulk b
 constexpr uint32_t kSfArrivals = 32;                   // every scale-loader lane
 constexpr uint32_t kDescStageStep = kStageBytes >> 4;  // stage stride in descriptor units
 constexpr uint32_t kIdesc = idesc_mxf4(kBM, kBN);
+constexpr int kStagingBytes = 32 * 32 * 2;             // per epilogue warp: 32 rows x 32 BF16
+constexpr int kStagingOff = kStages * kStageBytes;
 static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
 
 struct Ctl {
@@ -66,7 +72,7 @@ struct Ctl {
     int abort_flag;
 };
 
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + sizeof(Ctl) + 1024;
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 8 * kStagingBytes + sizeof(Ctl) + 1024;
 
 struct Tile {
     int32_t expert;
@@ -112,12 +118,12 @@ __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)
 template <bool kL1, bool kBTiled>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmArgs args) {
+                     const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)kStages * kStageBytes);
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)kStagingOff + 8 * kStagingBytes);
     volatile int* abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -138,6 +144,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (!kL1) tma_prefetch_desc(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -345,6 +352,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int hf = (warp - 4) >> 2;      // which half of the columns
         const int row_in_tile = 32 * q + lane;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+        uint8_t* staging = smem + kStagingOff + (warp - 4) * kStagingBytes;
+        const uint32_t staging_s = smem_u32(staging);
         uint32_t tc = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x, ++tc) {
             const Tile t = get_tile(args, w / args.n_tiles);
@@ -365,6 +374,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->tmem_empty));
+            if (!kL1 && 32 * q + 32 <= t.rows) {
+                // all 32 rows of this warp are in the tile: staged TMA stores
+                const int32_t trow = (int32_t)(t.row0 + 32 * q);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t col = (int64_t)nt * kBN + 128 * hf + 32 * i;
+                    if (col >= args.n_valid) break;
+                    uint32_t p[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        p[j] = pack_bf16x2(__uint_as_float(v[i][2 * j]), __uint_as_float(v[i][2 * j + 1]));
+                    if (lane == 0) bulk_wait_read();   // the previous store has read the block
+                    __syncwarp();
+                    uint4* row = reinterpret_cast<uint4*>(staging + lane * 64);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        row[c] = make_uint4(p[4 * c + 0], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+                    fence_proxy_async_smem();          // generic writes -> the TMA engine's reads
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, staging_s, (int32_t)col, trow);
+                        bulk_commit();
+                    }
+                }
+                continue;
+            }
             if (row_in_tile >= t.rows) continue;
             const int64_t grow = t.row0 + row_in_tile;
             if (kL1) {
@@ -390,8 +425,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t p[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        p[j] = f32_to_bf16(__uint_as_float(v[i][2 * j])) |
-                               (f32_to_bf16(__uint_as_float(v[i][2 * j + 1])) << 16);
+                        p[j] = pack_bf16x2(__uint_as_float(v[i][2 * j]), __uint_as_float(v[i][2 * j + 1]));
                     uint16_t* dst = args.y + grow * args.ld_y + col;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -404,6 +438,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
         }
+        if (!kL1 && lane == 0) bulk_wait_all();   // staged stores complete before the CTA exits
     }
 
     tc_fence_before();
@@ -415,7 +450,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <bool kL1, bool kBTiled>
-cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid, cudaStream_t s) {
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a, int grid,
+                   cudaStream_t s) {
     static int configured_mask = 0;   // one bit per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -426,7 +462,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs&
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
-    mxf4_gemm_kernel<kL1, kBTiled><<<grid, kGemmThreads, kSmemBytes, s>>>(ta, tb, a);
+    mxf4_gemm_kernel<kL1, kBTiled><<<grid, kGemmThreads, kSmemBytes, s>>>(ta, tb, ty, a);
     return cudaGetLastError();
 }
 
@@ -436,12 +472,13 @@ size_t gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
                            bool b_tiled, cudaStream_t s) {
-    return b_tiled ? launch<true, true>(ta, tb, a, grid, s) : launch<true, false>(ta, tb, a, grid, s);
+    // no output tensor map: the L1 epilogue writes its codes directly
+    return b_tiled ? launch<true, true>(ta, tb, ta, a, grid, s) : launch<true, false>(ta, tb, ta, a, grid, s);
 }
 
-cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                           bool b_tiled, cudaStream_t s) {
-    return b_tiled ? launch<false, true>(ta, tb, a, grid, s) : launch<false, false>(ta, tb, a, grid, s);
+cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                           int grid, bool b_tiled, cudaStream_t s) {
+    return b_tiled ? launch<false, true>(ta, tb, ty, a, grid, s) : launch<false, false>(ta, tb, ty, a, grid, s);
 }
 
 }  // namespace mx

@@ -54,8 +54,9 @@ struct GemmArgs {
 size_t gemm_smem_bytes();
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
                            bool b_tiled, cudaStream_t s);
-cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                           bool b_tiled, cudaStream_t s);
+// ty: the BF16 output y [rows, ld_y] as a 2-D tensor map with 32 x 32 boxes, no swizzle.
+cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                           int grid, bool b_tiled, cudaStream_t s);
 
 // ---- element-wise kernels ----
 // Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][512 B] (kb % 4 == 0).
