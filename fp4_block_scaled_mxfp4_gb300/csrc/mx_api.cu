@@ -69,13 +69,15 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t inner_bytes, int64_t row
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
-// 2-D BF16 output [rows, cols] written in boxes of 32 rows x 32 columns (no swizzle).
-int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows) {
+// 2-D output [rows, cols] (BF16 or bytes) written in boxes of 32 rows x 32 elements, no
+// swizzle.
+int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool bf16 = true) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * (bf16 ? 2 : 1)};
     cuuint32_t box[2] = {32u, 32u};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+    CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims,
+                          strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
@@ -401,8 +403,10 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     const int64_t max_mtiles = L.max_mtiles;
 
     // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
-    CUtensorMap ta1, tb1, ta2, tb2, ty2;
-    if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap(&tb1, w13, H / 2, E * 2 * I, 128)) return MX_ERR_CUDA;
+    CUtensorMap ta1, tb1, ty1, ta2, tb2, ty2;
+    if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap(&tb1, w13, H / 2, E * 2 * I, 128) ||
+        make_tmap_out(&ty1, hq, I / 2, R, false))
+        return MX_ERR_CUDA;
     g1.n_tiles = (int32_t)(I / 128);
     g1.b_rows_per_expert = 2 * I;
     g1.n_half = I;
@@ -411,7 +415,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     g1.hs = hs;
     g1.ld_hq = I / 2;
     g1.ld_hs = I / 32;
-    if (launch_gemm_l1(ta1, tb1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), scales_tiled, s) != cudaSuccess ||
+    if (launch_gemm_l1(ta1, tb1, ty1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), scales_tiled, s) != cudaSuccess ||
         !mark(3))
         return MX_ERR_CUDA;
 

@@ -71,14 +71,20 @@ __device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
 // 2^(127 - E) as a float for E in [0, 252] (always a normal float).
 __device__ __forceinline__ float mx_inv_scale(uint32_t E) { return __uint_as_float((254u - E) << 23); }
 
-// E2M1 code of a scaled value v (sign in bit 3). Thresholds are the midpoints of the
-// E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}; at a midpoint the even code wins.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-    float a = fabsf(v);
-    uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-                 (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
-                 (uint32_t)(a > 5.0f);
-    return c | ((__float_as_uint(v) >> 28) & 8u);
+// E2M1 codes of eight scaled values, element 0 in the lowest nibble: the hardware
+// conversion rounds to the nearest point of the grid {0, .5, 1, 1.5, 2, 3, 4, 6} (even code
+// at a midpoint), saturates at +-6 and keeps the sign of a value that rounds to zero.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
 }
 
 // Quantise 8 consecutive BF16 values held by one thread; four consecutive lanes hold one
@@ -110,8 +116,10 @@ __device__ __forceinline__ uint32_t mx_quant8_quad(const uint4 xv, uint32_t& sca
         const uint32_t E = mx_scale_byte(amax);
         const float inv = mx_inv_scale(E);
         scale_byte = E;
+        float sv[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) packed |= e2m1_code(f[i] * inv) << (4 * i);
+        for (int i = 0; i < 8; ++i) sv[i] = f[i] * inv;   // exact: inv is a power of two
+        packed = e2m1x8(sv);
     }
     return packed;
 }
@@ -136,7 +144,12 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&f)[32], uint4& code
         E = mx_scale_byte(amax);
         const float inv = mx_inv_scale(E);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i >> 3] |= e2m1_code(f[i] * inv) << (4 * (i & 7));
+        for (int k = 0; k < 4; ++k) {
+            float sv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sv[i] = f[8 * k + i] * inv;   // exact: inv is a power of two
+            w[k] = e2m1x8(sv);
+        }
     }
     codes = make_uint4(w[0], w[1], w[2], w[3]);
     return E;

@@ -28,10 +28,11 @@
 //               copies to the stage's ready barrier, which the MMA thread waits on.
 //   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, each owning half of the
 //               columns; they drain the accumulator to registers, release it, then compute.
-//               L2 writes its BF16 output through a 2 KB shared staging block per warp and
-//               an asynchronous TMA store of 32 rows x 32 columns, so the warp never waits
-//               for its stores (32 scattered 16-byte row pieces per store instruction
-//               otherwise); a warp whose 32 rows are not all in the tile stores directly.
+//               Outputs leave through a 2 KB shared staging block per warp and an
+//               asynchronous TMA store (L2: 32 rows x 32 BF16 columns; L1: 32 rows x 32
+//               bytes of codes), so the warp never waits for its stores (32 scattered
+//               16-byte row pieces per store instruction otherwise); a warp whose 32 rows
+//               are not all in the tile stores directly.
 // TMEM: columns [0, 256) accumulator; [256 + 24 s, 256 + 24 s + 24) the scale factors of
 // stage s (A: 2 K-words x 4 columns, B: 2 K-words x 8 columns).
 #include <cuda.h>
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (!kL1) tma_prefetch_desc(&tmY);
+        tma_prefetch_desc(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -400,6 +401,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 continue;
             }
+            if (kL1 && 32 * q + 32 <= t.rows) {
+                // all 32 rows of this warp are in the tile: codes through a staged TMA store
+                const int64_t grow = t.row0 + row_in_tile;
+                const int64_t col0 = (int64_t)nt * 128 + 64 * hf;   // first column of h
+                uint4 cds[2];
+                uint32_t es[2];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float g = round_bf16(__uint_as_float(v[b][i]));
+                        const float u = round_bf16(__uint_as_float(v[2 + b][i]));
+                        h[i] = round_bf16(silu_f32(g) * u);
+                    }
+                    es[b] = mx_quant32(h, cds[b]);
+                }
+                if (lane == 0) bulk_wait_read();   // the previous store has read the block
+                __syncwarp();
+                uint4* row = reinterpret_cast<uint4*>(staging + lane * 32);
+                row[0] = cds[0];
+                row[1] = cds[1];
+                fence_proxy_async_smem();          // generic writes -> the TMA engine's reads
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmY, staging_s, (int32_t)(col0 / 2), (int32_t)(t.row0 + 32 * q));
+                    bulk_commit();
+                }
+                *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col0 / 32) =
+                    (uint16_t)(es[0] | (es[1] << 8));
+                continue;
+            }
             if (row_in_tile >= t.rows) continue;
             const int64_t grow = t.row0 + row_in_tile;
             if (kL1) {
@@ -438,7 +471,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
         }
-        if (!kL1 && lane == 0) bulk_wait_all();   // staged stores complete before the CTA exits
+        if (lane == 0) bulk_wait_all();   // staged stores complete before the CTA exits
     }
 
     tc_fence_before();
@@ -470,10 +503,9 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
 
 size_t gemm_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                           bool b_tiled, cudaStream_t s) {
-    // no output tensor map: the L1 epilogue writes its codes directly
-    return b_tiled ? launch<true, true>(ta, tb, ta, a, grid, s) : launch<true, false>(ta, tb, ta, a, grid, s);
+cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                           int grid, bool b_tiled, cudaStream_t s) {
+    return b_tiled ? launch<true, true>(ta, tb, ty, a, grid, s) : launch<true, false>(ta, tb, ty, a, grid, s);
 }
 
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,

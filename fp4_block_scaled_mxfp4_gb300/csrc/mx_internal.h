@@ -52,9 +52,10 @@ struct GemmArgs {
 };
 
 size_t gemm_smem_bytes();
-cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                           bool b_tiled, cudaStream_t s);
-// ty: the BF16 output y [rows, ld_y] as a 2-D tensor map with 32 x 32 boxes, no swizzle.
+// ty: the output as a 2-D tensor map with 32 x 32 boxes, no swizzle: L1 the codes hq
+// [rows, ld_hq] (bytes), L2 the BF16 y [rows, ld_y].
+cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                           int grid, bool b_tiled, cudaStream_t s);
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                            int grid, bool b_tiled, cudaStream_t s);
 
