@@ -69,6 +69,21 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t inner_bytes, int64_t row
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// Stacked gate/up weights w13 [E][2I][H/2] viewed as [E][2][I][H/2] (4-D, innermost first
+// in the map): one box of 128 bytes x 128 rows x both halves brings the gate rows of an N
+// tile and the matching up rows in a single TMA load, 128-byte swizzle.
+int make_tmap_w13(CUtensorMap* m, const void* base, int64_t H, int64_t I, int64_t E) {
+    const cuuint64_t row = (cuuint64_t)(H / 2);
+    cuuint64_t dims[4] = {row, (cuuint64_t)I, 2, (cuuint64_t)E};
+    cuuint64_t strides[3] = {row, row * (cuuint64_t)I, row * (cuuint64_t)I * 2};
+    cuuint32_t box[4] = {128u, 128u, 2u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
 // 2-D output [rows, cols] (BF16 or bytes) written in boxes of 32 rows x 32 elements, no
 // swizzle.
 int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool bf16 = true) {
@@ -404,7 +419,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
 
     // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
     CUtensorMap ta1, tb1, ty1, ta2, tb2, ty2;
-    if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap(&tb1, w13, H / 2, E * 2 * I, 128) ||
+    if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap_w13(&tb1, w13, H, I, E) ||
         make_tmap_out(&ty1, hq, I / 2, R, false))
         return MX_ERR_CUDA;
     g1.n_tiles = (int32_t)(I / 128);

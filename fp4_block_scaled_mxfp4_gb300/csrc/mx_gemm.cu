@@ -12,9 +12,10 @@
 //
 // CTA layout (384 threads, one CTA per SM, persistent over the tile list):
 //   warp 0      TMA producer: A tile (128 rows x 128 B) and B tile (256 rows x 128 B) per
-//               K stage of 256 elements, 128-byte swizzle, into a 4-stage ring; with B's
-//               scales in tile layout (kBTiled) also B's scale factors for the stage: two
-//               1 KB bulk copies (one per 128-row group).
+//               K stage of 256 elements, 128-byte swizzle, into a 4-stage ring. Two TMA
+//               instructions per stage (L1's B is one box of a 4-D view of the stacked
+//               gate/up weights holding both halves): issuing one costs the thread ~160
+//               cycles, so more per stage would make this thread the pipeline's limit.
 //   warp 1      allocates 512 TMEM columns; lane 0 issues the 4 MMAs (K = 64 each) of a
 //               stage and commits the stage free. Nothing else runs in that thread: the
 //               tensor core's instruction queue is short, and any other work between two
@@ -22,7 +23,9 @@
 //   warp 2      scale-factor loader: cp.async from the plain row-major [rows, K/32] scales
 //               of A (and of B when they are not in tile layout) into the 32-lane x 16-byte
 //               blocks tcgen05.cp reads; each lane's copies arrive on the stage's scale
-//               barrier when they land (cp.async.mbarrier.arrive), so it never blocks.
+//               barrier when they land (cp.async.mbarrier.arrive), so it never blocks. With
+//               B's scales in tile layout (kBTiled), lane 0 fetches them with two 1 KB bulk
+//               copies (one per 128-row group) on the same barrier.
 //   warp 3      scale-factor copier: lane 0 waits for a stage's operands and scale tiles,
 //               moves the scales into that stage's TMEM slot (tcgen05.cp) and commits the
 //               copies to the stage's ready barrier, which the MMA thread waits on.
@@ -53,7 +56,7 @@ constexpr int kTmemCols = 512;
 constexpr int kSfTmemBase = 256;
 constexpr int kSfColsPerStage = 24;
 constexpr uint32_t kFullArrivals = 1;                  // producer (TMA + bulk bytes)
-constexpr uint32_t kSfArrivals = 32;                   // every scale-loader lane
+constexpr uint32_t kSfArrivals = 32;                   // every scale-loader lane (+1 with bulk copies)
 constexpr uint32_t kDescStageStep = kStageBytes >> 4;  // stage stride in descriptor units
 constexpr uint32_t kIdesc = idesc_mxf4(kBM, kBN);
 constexpr int kStagingBytes = 32 * 32 * 2;             // per epilogue warp: 32 rows x 32 BF16
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), kFullArrivals);
             mbar_init(smem_u32(&ctl->empty[s]), 1);  // MMA commit
-            mbar_init(smem_u32(&ctl->sf_full[s]), kSfArrivals);
+            mbar_init(smem_u32(&ctl->sf_full[s]), kSfArrivals + (kBTiled ? 1 : 0));
             mbar_init(smem_u32(&ctl->ready[s]), 1);   // scale copier commit
         }
         mbar_init(smem_u32(&ctl->tmem_full), 1);
@@ -172,28 +175,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         goto producer_done;
                     const uint32_t st = sbase + s * kStageBytes;
                     const uint32_t bar = smem_u32(&ctl->full[s]);
-                    // B scale factors: K-words 2kt, 2kt+1 of each 128-row group (one at the K tail)
-                    const uint32_t sf_bytes = (args.k_tail_half && kt == k_tiles - 1) ? 512u : 1024u;
-                    int64_t grp[2];
-                    uint32_t tx = kABytes + kBBytes;
-                    if (kBTiled) {
-                        for (int h = 0; h < 2; ++h) {
-                            grp[h] = b_row<kL1>(args, t.expert, nt, h) / 128;
-                            if (grp[h] < args.b_groups) tx += sf_bytes;
-                        }
-                    }
-                    mbar_arrive_expect_tx(bar, tx);
-                    if (kBTiled) {
-                        for (int h = 0; h < 2; ++h)
-                            if (grp[h] < args.b_groups)
-                                bulk_load(st + kABytes + kBBytes + kSfaBytes + h * 1024,
-                                          args.sfb + (grp[h] * args.kw + 2 * kt) * 512, sf_bytes, bar);
-                    }
+                    mbar_arrive_expect_tx(bar, kABytes + kBBytes);
                     tma_load_2d(st, &tmA, kt * (kBK / 2), (int32_t)t.row0, bar);
                     if (kL1) {
-                        tma_load_2d(st + kABytes, &tmB, kt * (kBK / 2), (int32_t)b_row<true>(args, t.expert, nt, 0), bar);
-                        tma_load_2d(st + kABytes + kBBytes / 2, &tmB, kt * (kBK / 2),
-                                    (int32_t)b_row<true>(args, t.expert, nt, 1), bar);
+                        // w13 as [E][2][I][H/2]: 128 gate rows then the matching 128 up rows
+                        tma_load_4d(st + kABytes, &tmB, kt * (kBK / 2), nt * 128, 0, t.expert, bar);
                     } else {
                         tma_load_2d(st + kABytes, &tmB, kt * (kBK / 2), (int32_t)b_row<false>(args, t.expert, nt, 0), bar);
                     }
@@ -272,6 +258,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const bool half = args.k_tail_half && (kt == k_tiles - 1);
                 const uint32_t st = sbase + s * kStageBytes;
                 const int64_t kcol = (int64_t)kt * 8;   // first 32-element block of this stage
+                if (kBTiled && lane == 0) {
+                    // B scales: K-words 2kt, 2kt+1 of each 128-row group (one at the K tail)
+                    const uint32_t sf_bytes = half ? 512u : 1024u;
+                    const uint32_t bar = smem_u32(&ctl->sf_full[s]);
+                    int64_t grp[2];
+                    uint32_t tx = 0;
+                    for (int h = 0; h < 2; ++h) {
+                        grp[h] = b_row<kL1>(args, t.expert, nt, h) / 128;
+                        if (grp[h] < args.b_groups) tx += sf_bytes;
+                    }
+                    mbar_arrive_expect_tx(bar, tx);
+                    for (int h = 0; h < 2; ++h)
+                        if (grp[h] < args.b_groups)
+                            bulk_load(st + kABytes + kBBytes + kSfaBytes + h * 1024,
+                                      args.sfb + (grp[h] * args.kw + 2 * kt) * 512, sf_bytes, bar);
+                }
                 {
                     const uint32_t dst0 = st + kABytes + kBBytes + lane * 16;
 #pragma unroll
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
         cp_async_wait<0>();
+        if (*abort_flag && lane == 0) __nanosleep(20000);   // bulk copies already in flight land
         __syncwarp();
     } else if (warp == 3) {
         // ---------------- scale-factor copier (one thread) ----------------
