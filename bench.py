@@ -58,6 +58,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x, world, device=None):
+    """The slowest rank's figure, on every rank (all-reduce MAX); x itself when world == 1."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flop_per_rank_step, ms_per_step):
+    """Whole-job throughput: every rank runs its own batch (replicas), timed by the slowest."""
+    return world * flop_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -251,11 +266,7 @@ def run_ours(args):
                 step(ev[i])
             stop.record(stream)
         torch.cuda.synchronize()
-    elapsed_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
     if mx.device_status() != 0:
         raise RuntimeError("device status set during the timed region")
     phase_names = ["route", "quant_gather", "l1_gemm", "l2_gemm", "combine"]
@@ -265,7 +276,7 @@ def run_ours(args):
             phase_ms[n] += row[j].elapsed_time(row[j + 1])
     phase_ms = {n: v / args.steps for n, v in phase_ms.items()}
     ms_per_step = elapsed_ms / args.steps
-    value = world * flop_step / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(world, flop_step, ms_per_step)
 
     # ---------------- end-to-end through the C ABI with host buffers ----------------
     e2e_steps = max(3, min(args.steps, 20))
@@ -299,11 +310,7 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     h2d = hx.numel() * 2 + hids.numel() * 4 + hw.numel() * 4
     d2h = hout.numel() * 2
 
@@ -356,7 +363,7 @@ def run_ours(args):
                      "peak_source": f"{peak_kind} bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
         "phases_ms": phase_ms,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * flop_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(world, flop_step, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 6 * args.steps,
         "clocks": clocks.summary(),
