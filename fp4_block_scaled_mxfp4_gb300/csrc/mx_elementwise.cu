@@ -24,25 +24,72 @@ int grid_for(int64_t work_items, int num_sms, int per_sm = 8) {
 
 __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) { return lo | (hi << 16); }
 
-// One group = 8 logical columns = 4 code bytes; groups are contiguous over the whole tensor
-// because cols % 32 == 0, so group g reads codes32[g], scale sf[g / 4] and writes out[g].
+// Four E2M1 codes (16 bits, element 0 lowest) -> four BF16 values (two words, element 0
+// in the low half) times 2^(E-127), for a scale byte E in [2, 252]: every nonzero product is
+// then a normal BF16 whose bits are the code's BF16 bits at scale 1 (a byte table looked up
+// with prmt) with E - 127 added to the exponent field. Exact, like the arithmetic path.
+__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t c16, uint32_t off2, uint32_t& o0, uint32_t& o1) {
+    const uint32_t sel = c16 & 0x7777u;                          // magnitudes 0..7 select table bytes
+    const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, sel);   // high bytes of 0, .5, 1, .. 6
+    const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, sel);   // low bytes
+    uint32_t a = __byte_perm(lo, hi, 0x5140u);                   // elements 0, 1
+    uint32_t b = __byte_perm(lo, hi, 0x7362u);                   // elements 2, 3
+    a = __vadd2(a, off2 & __vcmpne2(a, 0u));                     // scale the nonzero halves
+    b = __vadd2(b, off2 & __vcmpne2(b, 0u));
+    o0 = a | ((c16 & 0x8u) << 12) | ((c16 & 0x80u) << 24);       // signs (bit 3 of each code)
+    o1 = b | ((c16 & 0x800u) << 4) | ((c16 & 0x8000u) << 16);
+}
+
+// Eight codes of one word with scale byte s, any s (255: NaN with the code's sign).
+__device__ __forceinline__ void e2m1x8_to_bf16_any(uint32_t c, uint32_t s, uint32_t (&o)[4]) {
+    if (s >= 2u && s <= 252u) {
+        const uint32_t off2 = (((s - 127u) << 7) & 0xFFFFu) * 0x10001u;
+        e2m1x4_to_bf16(c & 0xFFFFu, off2, o[0], o[1]);
+        e2m1x4_to_bf16(c >> 16, off2, o[2], o[3]);
+    } else if (s == 255u) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = pack2((((c >> (8 * i)) & 8u) << 12) | 0x7FC0u, (((c >> (8 * i + 4)) & 8u) << 12) | 0x7FC0u);
+    } else {
+        const float scale = e8m0_value(s);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = pack2(f32_to_bf16(e2m1_value((c >> (8 * i)) & 15u) * scale),
+                         f32_to_bf16(e2m1_value((c >> (8 * i + 4)) & 15u) * scale));
+    }
+}
+
+// One unit = one 32-element scale block = 16 code bytes (four words) -> 64 output bytes;
+// units are contiguous over the whole tensor because cols % 32 == 0, so unit u reads code
+// words 4u..4u+3 and scale sf[u] and writes output vectors 4u..4u+3. A warp takes 64 units
+// per pass, lane l handling word l % 4 of units 8i + l / 4 (i = 0..7): each load
+// instruction reads 128 contiguous bytes and each store writes 512 contiguous bytes, with
+// eight loads in flight per lane.
+constexpr int kDeqUnitsPerWarp = 64;
 __global__ void __launch_bounds__(kThreads) mxfp4_dequant_kernel(const uint32_t* __restrict__ codes32,
                                                                  const uint8_t* __restrict__ sf,
-                                                                 uint4* __restrict__ out, int64_t groups) {
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < groups; g += stride) {
-        const uint32_t c = __ldg(codes32 + g);
-        const uint32_t s = __ldg(sf + (g >> 2));
-        uint32_t o[8];
-        if (s == 255u) {
+                                                                 uint4* __restrict__ out, int64_t units) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    for (int64_t base = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kDeqUnitsPerWarp;
+         base < units; base += nwarps * kDeqUnitsPerWarp) {
+        uint32_t c[8], sc[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = (((c >> (4 * i)) & 8u) << 12) | 0x7FC0u;
-        } else {
-            const float scale = e8m0_value(s);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = f32_to_bf16(e2m1_value((c >> (4 * i)) & 15u) * scale);
+        for (int i = 0; i < 8; ++i) {
+            const int64_t u = base + 8 * i + (lane >> 2);
+            const bool ok = u < units;
+            c[i] = ok ? __ldg(codes32 + 4 * u + (lane & 3)) : 0u;
+            sc[i] = ok ? __ldg(sf + u) : 127u;
         }
-        out[g] = make_uint4(pack2(o[0], o[1]), pack2(o[2], o[3]), pack2(o[4], o[5]), pack2(o[6], o[7]));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t u = base + 8 * i + (lane >> 2);
+            if (u < units) {
+                uint32_t o[4];
+                e2m1x8_to_bf16_any(c[i], sc[i], o);
+                out[4 * u + (lane & 3)] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
     }
 }
 
@@ -58,32 +105,73 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
     return (b & 0x80u) ? -mag : mag;
 }
 
-// One group = 16 consecutive columns of one row (cols % 16 == 0).
-__global__ void __launch_bounds__(kThreads) fp8_dequant_kernel(const uint4* __restrict__ q16,
-                                                               const uint8_t* __restrict__ sf,
-                                                               uint4* __restrict__ out, int64_t groups,
-                                                               int64_t groups_per_row, int64_t sf_cols) {
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < groups; g += stride) {
-        const int64_t row = g / groups_per_row;
-        const int64_t col = (g - row * groups_per_row) * 16;
-        const uint32_t s = __ldg(sf + (row >> 7) * sf_cols + (col >> 7));
-        const uint4 qv = __ldg(q16 + g);
-        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
-        const float scale = (s == 255u) ? 0.0f : e8m0_value(s);
-        uint32_t o[16];
+// Two E4M3 bytes (first in the low half) -> two BF16 values times 2^(s-127), for s in
+// [10, 246] and no NaN byte: the hardware conversion to FP16 is exact, every value is then
+// a normal FP16 of exponent 6..23, and with the scale a normal BF16 whose exponent is the
+// FP16 exponent + s - 15 and whose mantissa is the FP16's top 7 bits (E4M3 has 3).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16(uint32_t b16, uint32_t off2) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)b16));
+    const uint32_t mag = ((h & 0x7FFF7FFFu) >> 3) & 0x0FFF0FFFu;   // FP16 exponent+mantissa at BF16 places
+    return __vadd2(mag, off2 & __vcmpne2(mag, 0u)) | (h & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t e4m3_to_bf16_slow(uint32_t b, uint32_t s) {
+    if ((b & 0x7Fu) == 0x7Fu || s == 255u) return ((b & 0x80u) << 8) | 0x7FC0u;
+    return f32_to_bf16(e4m3_value(b) * e8m0_value(s));
+}
+
+// 8 E4M3 bytes of one row (one 128-column scale block) -> 16 bytes of BF16.
+__device__ __forceinline__ uint4 fp8x8_to_bf16(const uint2 qv, uint32_t s) {
+    const uint32_t w[2] = {qv.x, qv.y};
+    uint32_t o[4];
+    const uint32_t nan_bytes = __vcmpeq4(w[0] & 0x7F7F7F7Fu, 0x7F7F7F7Fu) | __vcmpeq4(w[1] & 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    if (s >= 10u && s <= 246u && nan_bytes == 0u) {
+        const uint32_t off2 = (((s - 15u) << 7) & 0xFFFFu) * 0x10001u;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t b = (w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-            if ((b & 0x7Fu) == 0x7Fu || s == 255u) {
-                o[i] = ((b & 0x80u) << 8) | 0x7FC0u;
-            } else {
-                o[i] = f32_to_bf16(e4m3_value(b) * scale);
+        for (int i = 0; i < 2; ++i) {
+            o[2 * i] = e4m3x2_to_bf16(w[i] & 0xFFFFu, off2);
+            o[2 * i + 1] = e4m3x2_to_bf16(w[i] >> 16, off2);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t ww = w[i >> 1] >> (16 * (i & 1));
+            o[i] = pack2(e4m3_to_bf16_slow(ww & 0xFFu, s), e4m3_to_bf16_slow((ww >> 8) & 0xFFu, s));
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One CTA per row (grid-stride over rows); lane l of a warp takes the row's 8-column chunks
+// l, l + 32, ...: each load instruction reads 256 contiguous bytes and each store writes 512.
+// Four chunks per thread per pass keep four loads in flight; the 128x128 block scale comes
+// from the row's block row and the chunk's block column.
+constexpr int kFp8ChunksPerPass = 4;
+__global__ void __launch_bounds__(kThreads) fp8_dequant_kernel(const uint8_t* __restrict__ q,
+                                                               const uint8_t* __restrict__ sf,
+                                                               uint16_t* __restrict__ out, int64_t rows,
+                                                               int64_t cols, int64_t sf_cols) {
+    const int chunks = (int)(cols / 8);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const uint2* qr = reinterpret_cast<const uint2*>(q + row * cols);
+        uint4* orow = reinterpret_cast<uint4*>(out + row * cols);
+        const uint8_t* srow = sf + (row >> 7) * sf_cols;
+        for (int c0 = threadIdx.x; c0 < chunks; c0 += kFp8ChunksPerPass * kThreads) {
+            uint2 qv[kFp8ChunksPerPass];
+            uint32_t sv[kFp8ChunksPerPass];
+#pragma unroll
+            for (int i = 0; i < kFp8ChunksPerPass; ++i) {
+                const int c = c0 + i * kThreads;
+                qv[i] = c < chunks ? __ldg(qr + c) : make_uint2(0, 0);
+                sv[i] = c < chunks ? __ldg(srow + (c >> 4)) : 127u;
+            }
+#pragma unroll
+            for (int i = 0; i < kFp8ChunksPerPass; ++i) {
+                const int c = c0 + i * kThreads;
+                if (c < chunks) orow[c] = fp8x8_to_bf16(qv[i], sv[i]);
             }
         }
-        out[2 * g] = make_uint4(pack2(o[0], o[1]), pack2(o[2], o[3]), pack2(o[4], o[5]), pack2(o[6], o[7]));
-        out[2 * g + 1] =
-            make_uint4(pack2(o[8], o[9]), pack2(o[10], o[11]), pack2(o[12], o[13]), pack2(o[14], o[15]));
     }
 }
 
@@ -176,20 +264,19 @@ cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_
 
 cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, uint16_t* out, int64_t rows,
                                  int64_t cols, int num_sms, cudaStream_t s) {
-    const int64_t groups = rows * (cols / 8);
-    if (groups == 0) return cudaSuccess;
-    mxfp4_dequant_kernel<<<grid_for(groups, num_sms), kThreads, 0, s>>>(
-        reinterpret_cast<const uint32_t*>(codes), sf, reinterpret_cast<uint4*>(out), groups);
+    const int64_t units = rows * (cols / 32);
+    if (units == 0) return cudaSuccess;
+    const int64_t warps = (units + kDeqUnitsPerWarp - 1) / kDeqUnitsPerWarp;
+    mxfp4_dequant_kernel<<<grid_for(warps * 32, num_sms), kThreads, 0, s>>>(
+        reinterpret_cast<const uint32_t*>(codes), sf, reinterpret_cast<uint4*>(out), units);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* out, int64_t rows,
                                int64_t cols, int num_sms, cudaStream_t s) {
-    const int64_t gpr = cols / 16;
-    const int64_t groups = rows * gpr;
-    if (groups == 0) return cudaSuccess;
-    fp8_dequant_kernel<<<grid_for(groups, num_sms), kThreads, 0, s>>>(
-        reinterpret_cast<const uint4*>(q), sf, reinterpret_cast<uint4*>(out), groups, gpr, (cols + 127) / 128);
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int64_t grid = rows < (int64_t)num_sms * 8 ? rows : (int64_t)num_sms * 8;
+    fp8_dequant_kernel<<<(unsigned)grid, kThreads, 0, s>>>(q, sf, out, rows, cols, (cols + 127) / 128);
     return cudaGetLastError();
 }
 
