@@ -84,12 +84,12 @@ int make_tmap_w13(CUtensorMap* m, const void* base, int64_t H, int64_t I, int64_
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
-// 2-D output [rows, cols] (BF16 or bytes) written in boxes of 32 rows x 32 elements, no
-// swizzle.
+// 2-D output [rows, cols] written in boxes of 32 rows x 32 bytes (16 BF16 or 32 code
+// bytes), no swizzle.
 int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool bf16 = true) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * (bf16 ? 2 : 1)};
-    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t box[2] = {bf16 ? 16u : 32u, 32u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims,
                           strides, box, estr,

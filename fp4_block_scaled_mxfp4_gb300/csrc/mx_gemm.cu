@@ -31,8 +31,8 @@
 //               copies to the stage's ready barrier, which the MMA thread waits on.
 //   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, each owning half of the
 //               columns; they drain the accumulator to registers, release it, then compute.
-//               Outputs leave through a 2 KB shared staging block per warp and an
-//               asynchronous TMA store (L2: 32 rows x 32 BF16 columns; L1: 32 rows x 32
+//               Outputs leave through a 1 KB shared staging block per warp and an
+//               asynchronous TMA store (L2: 32 rows x 16 BF16 columns; L1: 32 rows x 32
 //               bytes of codes), so the warp never waits for its stores (32 scattered
 //               16-byte row pieces per store instruction otherwise); a warp whose 32 rows
 //               are not all in the tile stores directly.
@@ -49,25 +49,60 @@ namespace {
 
 constexpr int kABytes = kBM * kBK / 2;                 // 16 KB
 constexpr int kBBytes = kBN * kBK / 2;                 // 32 KB
-constexpr int kSfaBytes = 2 * 512;                     // 2 K-words x (32 lanes x 16 B)
-constexpr int kSfbBytes = 2 * 2 * 512;                 // 2 row groups of 128 x 2 K-words
-constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // 51 KB, 1024-aligned
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemBase = 256;
 constexpr int kSfColsPerStage = 24;
 constexpr uint32_t kFullArrivals = 1;                  // producer (TMA + bulk bytes)
 constexpr uint32_t kSfArrivals = 32;                   // every scale-loader lane (+1 with bulk copies)
-constexpr uint32_t kDescStageStep = kStageBytes >> 4;  // stage stride in descriptor units
 constexpr uint32_t kIdesc = idesc_mxf4(kBM, kBN);
-constexpr int kStagingBytes = 32 * 32 * 2;             // per epilogue warp: 32 rows x 32 BF16
-constexpr int kStagingOff = kStages * kStageBytes;
-static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+constexpr int kStagingBytes = 1024;                    // per epilogue warp: 32 rows x 32 bytes
+constexpr int kMaxStages = 4;
+
+// Scale factors reach tensor memory in one of two shared-memory images:
+// Scale factors reach tensor memory by tcgen05.cp. The tensor core reads them per 32-row
+// slice from that slice's own lane quarter: A's scale of row r at lane r, column r / 32
+// (+4 for the stage's second K-word); B's scales, which every slice needs, at every lane of
+// each quarter. So B's come by tcgen05.cp.32x128b.warpx4 from 512-byte blocks (32 lanes x
+// 16 bytes, replicated into the four quarters), and A's by one tcgen05.cp.128x256b for
+// both K-words from a 4 KB image: 128 rows x 32 bytes in 8-row x 16-byte core matrices
+// (8-row groups 256 bytes apart, a row's two 16-byte halves 128 bytes apart), row r's word
+// at byte 4 (r / 32) of each half. A replicating copy costs the tensor pipe ~75 cycles and
+// the 128x256b copy almost nothing, so this takes a stage from six replicating copies to
+// four.
+template <bool kWide>
+struct Cfg {
+    static constexpr int kStages = 4;
+    static constexpr int kSfaBytes = 4096;
+    static constexpr int kSfbBytes = 2 * 2 * 512;
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    static constexpr uint32_t kDescStageStep = kStageBytes >> 4;
+    static constexpr int kStagingOff = kStages * kStageBytes;
+    static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+    static_assert(kStages <= kMaxStages, "barrier arrays");
+    static_assert(kSfTmemBase + kStages * kSfColsPerStage <= kTmemCols, "scale slots must fit in TMEM");
+};
+
+// Descriptor of a wide scale image: core matrices of 8 rows x 16 bytes, the two halves of a
+// row 128 bytes apart (leading offset), 8-row groups 256 bytes apart (stride offset).
+__device__ __forceinline__ uint64_t desc_sf_wide(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(256u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Byte of the wide image holding row r's word for half h: image row r (lane r of tensor
+// memory), word position r / 32.
+__device__ __forceinline__ uint32_t wide_off(int r, int h) {
+    return (uint32_t)((r >> 3) * 256 + h * 128 + (r & 7) * 16 + (r >> 5) * 4);
+}
 
 struct Ctl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t sf_full[kStages];
-    uint64_t ready[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t sf_full[kMaxStages];
+    uint64_t ready[kMaxStages];
     uint64_t tmem_full;
     uint64_t tmem_empty;
     uint64_t drain;
@@ -76,7 +111,10 @@ struct Ctl {
     int abort_flag;
 };
 
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 8 * kStagingBytes + sizeof(Ctl) + 1024;
+template <bool kWide>
+constexpr size_t smem_bytes() {
+    return (size_t)Cfg<kWide>::kStagingOff + 8 * kStagingBytes + sizeof(Ctl) + 1024;
+}
 
 struct Tile {
     int32_t expert;
@@ -123,6 +161,13 @@ template <bool kL1, bool kBTiled>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
+    using C = Cfg<!kBTiled>;
+    constexpr bool kWide = !kBTiled;
+    constexpr int kStages = C::kStages;
+    constexpr int kStageBytes = C::kStageBytes;
+    constexpr int kSfaBytes = C::kSfaBytes;
+    constexpr uint32_t kDescStageStep = C::kDescStageStep;
+    constexpr int kStagingOff = C::kStagingOff;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -274,8 +319,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             bulk_load(st + kABytes + kBBytes + kSfaBytes + h * 1024,
                                       args.sfb + (grp[h] * args.kw + 2 * kt) * 512, sf_bytes, bar);
                 }
+                // Row r = 32 j + lane of a 128-row group. Dense image: 512-byte block per
+                // K-word, byte lane * 16 + j * 4. Wide image: wide_off(r, half), A's halves
+                // its two K-words, B's (one 4 KB image per K-word) its two 128-row halves.
                 {
-                    const uint32_t dst0 = st + kABytes + kBBytes + lane * 16;
+                    const uint32_t sfa_s = st + kABytes + kBBytes;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int64_t grow = t.row0 + 32 * j + lane;
@@ -284,12 +332,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int wd = 0; wd < 2; ++wd) {
                             const bool ok = valid && (wd == 0 || !half);
-                            cp_async_4(dst0 + wd * 512 + j * 4, ok ? src + 4 * wd : args.sfa, ok ? 4u : 0u);
+                            const uint32_t dst = sfa_s + wide_off(32 * j + lane, wd);
+                            cp_async_4(dst, ok ? src + 4 * wd : args.sfa, ok ? 4u : 0u);
                         }
                     }
                 }
                 if (!kBTiled) {
-                    const uint32_t dst0 = st + kABytes + kBBytes + kSfaBytes + lane * 16;
+                    const uint32_t sfb_s = st + kABytes + kBBytes + kSfaBytes;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int64_t rbase = b_row<kL1>(args, t.expert, nt, h);
@@ -301,8 +350,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                             for (int wd = 0; wd < 2; ++wd) {
                                 const bool ok = valid && (wd == 0 || !half);
-                                cp_async_4(dst0 + h * 1024 + wd * 512 + j * 4, ok ? src + 4 * wd : args.sfb,
-                                           ok ? 4u : 0u);
+                                const uint32_t dst = sfb_s + h * 1024 + wd * 512 + lane * 16 + j * 4;
+                                cp_async_4(dst, ok ? src + 4 * wd : args.sfb, ok ? 4u : 0u);
                             }
                         }
                     }
@@ -335,9 +384,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t sfb_s = sfa_s + kSfaBytes;
                     const uint32_t sfa_t = tmem + kSfTmemBase + s * kSfColsPerStage;
                     const uint32_t sfb_t = sfa_t + 8;
+                    tc_cp_128x256b(sfa_t, desc_sf_wide(sfa_s));                                // A, both K-words
                     for (int wd = 0; wd < nwords; ++wd) {
-                        tc_cp_32x128b_x4(sfa_t + 4 * wd, desc_sf(sfa_s + wd * 512));
-                        tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 512));          // rows 0-127
+                        tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 512));          // B rows 0-127
                         tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + 1024 + wd * 512));  // 128-255
                     }
                     tc_commit(smem_u32(&ctl->ready[s]));   // arrives once the copies are in TMEM
@@ -389,17 +438,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         p[j] = pack_bf16x2(__uint_as_float(v[i][2 * j]), __uint_as_float(v[i][2 * j + 1]));
-                    if (lane == 0) bulk_wait_read();   // the previous store has read the block
-                    __syncwarp();
-                    uint4* row = reinterpret_cast<uint4*>(staging + lane * 64);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        row[c] = make_uint4(p[4 * c + 0], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
-                    fence_proxy_async_smem();          // generic writes -> the TMA engine's reads
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmY, staging_s, (int32_t)col, trow);
-                        bulk_commit();
+                    for (int c = 0; c < 2; ++c) {       // 16 columns (32 bytes) per row and store
+                        if (col + 16 * c >= args.n_valid) break;
+                        if (lane == 0) bulk_wait_read();   // the previous store has read the block
+                        __syncwarp();
+                        uint4* row = reinterpret_cast<uint4*>(staging + lane * 32);
+                        row[0] = make_uint4(p[8 * c + 0], p[8 * c + 1], p[8 * c + 2], p[8 * c + 3]);
+                        row[1] = make_uint4(p[8 * c + 4], p[8 * c + 5], p[8 * c + 6], p[8 * c + 7]);
+                        fence_proxy_async_smem();          // generic writes -> the TMA engine's reads
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmY, staging_s, (int32_t)(col + 16 * c), trow);
+                            bulk_commit();
+                        }
                     }
                 }
                 continue;
@@ -494,17 +546,17 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     if (err != cudaSuccess) return err;
     if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
         err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1, kBTiled>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kSmemBytes);
+                                   (int)smem_bytes<!kBTiled>());
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
-    mxf4_gemm_kernel<kL1, kBTiled><<<grid, kGemmThreads, kSmemBytes, s>>>(ta, tb, ty, a);
+    mxf4_gemm_kernel<kL1, kBTiled><<<grid, kGemmThreads, smem_bytes<!kBTiled>(), s>>>(ta, tb, ty, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return kSmemBytes; }
+size_t gemm_smem_bytes() { return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>(); }
 
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                            int grid, bool b_tiled, cudaStream_t s) {

@@ -52,7 +52,7 @@ struct GemmArgs {
 };
 
 size_t gemm_smem_bytes();
-// ty: the output as a 2-D tensor map with 32 x 32 boxes, no swizzle: L1 the codes hq
+// ty: the output as a 2-D tensor map with boxes of 32 rows x 32 bytes, no swizzle: L1 the codes hq
 // [rows, ld_hq] (bytes), L2 the BF16 y [rows, ld_y].
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                            int grid, bool b_tiled, cudaStream_t s);
