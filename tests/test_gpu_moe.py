@@ -134,6 +134,22 @@ def test_tiled_scales_forward_is_bit_identical(mx, name):
     np.testing.assert_array_equal(d.run(mx, tiled=True), plain)
 
 
+@pytest.mark.parametrize("routing", ["uniform", None])
+def test_ragged_k_and_n_tails(mx, routing):
+    """H = 640 leaves L1 a last K stage of 128 and L2 a last N tile of 128 columns; I = 384
+    leaves L2 a last K stage of 128; every expert spans several 128-row M tiles, the last
+    one ragged. Both weight-scale layouts give the same bits."""
+    if routing:
+        inp = make_moe_inputs(T=700, H=640, I=384, E=6, K=4, seed=11, routing="uniform")
+        inp.topk_ids[::9, 3] = -1
+    else:
+        inp = make_moe_inputs(T=600, H=640, I=384, E=1, K=1, seed=12, routing=None)
+    d = Dev(mx, inp)
+    plain = d.run(mx)
+    print(f"ragged K and N tails, routing={routing}", check_moe_run(mx, d))
+    np.testing.assert_array_equal(d.run(mx, tiled=True), plain)
+
+
 def test_shared_config_full(mx):
     inp = make_config_inputs("shared")
     d = Dev(mx, inp)
