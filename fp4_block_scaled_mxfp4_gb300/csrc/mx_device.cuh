@@ -87,43 +87,6 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
     return r;
 }
 
-// Quantise 8 consecutive BF16 values held by one thread; four consecutive lanes hold one
-// 32-element block (so every lane of the warp must call this). Returns the 8 packed codes
-// (element 0 in the lowest nibble) and writes the block's scale byte to `scale_byte`.
-__device__ __forceinline__ uint32_t mx_quant8_quad(const uint4 xv, uint32_t& scale_byte) {
-    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-    float f[8];
-    float amax = 0.0f;
-    uint32_t bad = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
-        bad |= ((lo & 0x7F80u) == 0x7F80u) | ((hi & 0x7F80u) == 0x7F80u);
-        f[2 * i] = bf16_to_f32(lo);
-        f[2 * i + 1] = bf16_to_f32(hi);
-        amax = fmaxf(amax, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
-    }
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, 1);
-    bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, 2);
-    uint32_t packed = 0;
-    if (bad) {
-        scale_byte = 255u;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) packed |= (((__float_as_uint(f[i]) >> 28) & 8u) | 7u) << (4 * i);
-    } else {
-        const uint32_t E = mx_scale_byte(amax);
-        const float inv = mx_inv_scale(E);
-        scale_byte = E;
-        float sv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sv[i] = f[i] * inv;   // exact: inv is a power of two
-        packed = e2m1x8(sv);
-    }
-    return packed;
-}
-
 // Quantise one 32-element block held entirely by this thread (float values that are
 // already BF16 numbers). Writes 16 bytes of codes and returns the scale byte.
 __device__ __forceinline__ uint32_t mx_quant32(const float (&f)[32], uint4& codes) {

@@ -175,23 +175,27 @@ __global__ void __launch_bounds__(kThreads) fp8_dequant_kernel(const uint8_t* __
     }
 }
 
-// One group = 8 elements (16 bytes of BF16); four consecutive lanes form one 32-element
-// block. The loop runs in whole warps so the quad shuffles always have all lanes.
+// One thread per 32-element block: four 16-byte loads, one quantisation, a 16-byte code
+// store and a scale byte (consecutive threads write consecutive codes and scales).
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __restrict__ x8,
-                                                             uint32_t* __restrict__ codes32,
-                                                             uint8_t* __restrict__ sf, int64_t groups) {
-    const int lane = threadIdx.x & 31;
-    const int64_t warp_stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t g0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); g0 < groups; g0 += warp_stride) {
-        const int64_t g = g0 + lane;
-        const bool ok = g < groups;
-        const uint4 xv = ok ? __ldg(x8 + g) : make_uint4(0, 0, 0, 0);
-        uint32_t E;
-        const uint32_t packed = mx_quant8_quad(xv, E);
-        if (ok) {
-            codes32[g] = packed;
-            if ((g & 3) == 0) sf[g >> 2] = (uint8_t)E;
+                                                             uint4* __restrict__ codes16,
+                                                             uint8_t* __restrict__ sf, int64_t blocks) {
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < blocks; b += stride) {
+        float f[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = __ldg(x8 + 4 * b + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[8 * i + 2 * j] = bf16_to_f32(w[j] & 0xFFFFu);
+                f[8 * i + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
+            }
         }
+        uint4 codes;
+        sf[b] = (uint8_t)mx_quant32(f, codes);
+        codes16[b] = codes;
     }
 }
 
@@ -282,10 +286,10 @@ cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* ou
 
 cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
                              int num_sms, cudaStream_t s) {
-    const int64_t groups = M * (K / 8);
-    if (groups == 0) return cudaSuccess;
-    act_quant_kernel<<<grid_for(groups, num_sms), kThreads, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), reinterpret_cast<uint32_t*>(codes), sf, groups);
+    const int64_t blocks = M * (K / 32);
+    if (blocks == 0) return cudaSuccess;
+    act_quant_kernel<<<grid_for(blocks, num_sms), kThreads, 0, s>>>(
+        reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks);
     return cudaGetLastError();
 }
 

@@ -102,12 +102,15 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
 
 constexpr int kGatherThreads = 256;
 
+// One thread per 32-element MX block of the token's row: four 16-byte loads, one
+// quantisation, then per routed copy of the row a 16-byte code store and a scale byte, so a
+// warp writes 512 contiguous code bytes and 32 contiguous scale bytes per destination row.
 __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
-    const uint4* __restrict__ x8, const int32_t* __restrict__ ids, int K, int E, int64_t groups_per_row,
-    RouteBufs rb, uint32_t* __restrict__ xq32, uint8_t* __restrict__ xs) {
+    const uint4* __restrict__ x8, const int32_t* __restrict__ ids, int K, int E, int64_t blocks_per_row,
+    RouteBufs rb, uint4* __restrict__ xq16, uint8_t* __restrict__ xs) {
     __shared__ int32_t s_rows[kMaxTopK];
     const int64_t t = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
     if (tid < K) {
         const int64_t p = t * K + tid;
         const int32_t e = __ldg(ids + p);
@@ -118,20 +121,26 @@ __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
         rb.row_of[p] = row;
     }
     __syncthreads();
-    const uint4* xrow = x8 + t * groups_per_row;
-    for (int64_t g0 = (tid & ~31); g0 < groups_per_row; g0 += kGatherThreads) {
-        const int64_t g = g0 + lane;
-        const bool ok = g < groups_per_row;
-        const uint4 xv = ok ? __ldg(xrow + g) : make_uint4(0, 0, 0, 0);
-        uint32_t E8;
-        const uint32_t packed = mx_quant8_quad(xv, E8);
-        if (ok) {
-            for (int k = 0; k < K; ++k) {
-                const int32_t r = s_rows[k];
-                if (r < 0) continue;
-                xq32[(int64_t)r * groups_per_row + g] = packed;
-                if ((g & 3) == 0) xs[(int64_t)r * (groups_per_row >> 2) + (g >> 2)] = (uint8_t)E8;
+    const uint4* xrow = x8 + t * blocks_per_row * 4;
+    for (int64_t b = tid; b < blocks_per_row; b += kGatherThreads) {
+        float f[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = __ldg(xrow + 4 * b + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[8 * i + 2 * j] = bf16_to_f32(w[j] & 0xFFFFu);
+                f[8 * i + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
             }
+        }
+        uint4 codes;
+        const uint32_t e8 = mx_quant32(f, codes);
+        for (int k = 0; k < K; ++k) {
+            const int32_t r = s_rows[k];
+            if (r < 0) continue;
+            xq16[(int64_t)r * blocks_per_row + b] = codes;
+            xs[(int64_t)r * blocks_per_row + b] = (uint8_t)e8;
         }
     }
 }
@@ -154,8 +163,7 @@ cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T
                                 int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     quant_gather_kernel<<<(unsigned)T, kGatherThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), ids, (int)K,
-                                                               (int)E, H / 8, rb,
-                                                               reinterpret_cast<uint32_t*>(xq), xs);
+                                                               (int)E, H / 32, rb, reinterpret_cast<uint4*>(xq), xs);
     return cudaGetLastError();
 }
 
