@@ -70,13 +70,13 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t inner_bytes, int64_t row
 }
 
 // Stacked gate/up weights w13 [E][2I][H/2] viewed as [E][2][I][H/2] (4-D, innermost first
-// in the map): one box of 128 bytes x 128 rows x both halves brings the gate rows of an N
-// tile and the matching up rows in a single TMA load, 128-byte swizzle.
-int make_tmap_w13(CUtensorMap* m, const void* base, int64_t H, int64_t I, int64_t E) {
+// in the map): one box of 128 bytes x box_rows rows x both halves brings the gate rows of an
+// N tile and the matching up rows in a single TMA load, 128-byte swizzle.
+int make_tmap_w13(CUtensorMap* m, const void* base, int64_t H, int64_t I, int64_t E, uint32_t box_rows) {
     const cuuint64_t row = (cuuint64_t)(H / 2);
     cuuint64_t dims[4] = {row, (cuuint64_t)I, 2, (cuuint64_t)E};
     cuuint64_t strides[3] = {row, row * (cuuint64_t)I, row * (cuuint64_t)I * 2};
-    cuuint32_t box[4] = {128u, 128u, 2u, 1u};
+    cuuint32_t box[4] = {128u, box_rows, 2u, 1u};
     cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -84,12 +84,12 @@ int make_tmap_w13(CUtensorMap* m, const void* base, int64_t H, int64_t I, int64_
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
-// 2-D output [rows, cols] written in boxes of 32 rows x 32 bytes (16 BF16 or 32 code
-// bytes), no swizzle.
-int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool bf16 = true) {
+// 2-D output [rows, cols] written in boxes of 32 rows x box_bytes (32: 16 BF16 or 32 code
+// bytes; 16: 16 code bytes), no swizzle.
+int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool bf16 = true, uint32_t box_bytes = 32) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * (bf16 ? 2 : 1)};
-    cuuint32_t box[2] = {bf16 ? 16u : 32u, 32u};
+    cuuint32_t box[2] = {bf16 ? box_bytes / 2 : box_bytes, 32u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims,
                           strides, box, estr,
@@ -288,6 +288,10 @@ int mxfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t
     return cuda_status(launch_sf_tile(sf, out, rows, cols / 32, static_cast<cudaStream_t>(stream)));
 }
 
+// N tile width for a GEMM whose 256-wide tiling has units256 work units: 128 when those
+// would leave SMs idle.
+int tile_cols(int64_t units256, int num_sms) { return units256 < num_sms ? 128 : kBN; }
+
 int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb, void* d_bf16,
                     int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
     if (M < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
@@ -299,19 +303,21 @@ int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const
         return MX_ERR_MISALIGNED;
     DeviceInfo* d;
     if (int e = device_info(&d)) return e;
+    const int64_t mtiles = (M + kBM - 1) / kBM;
+    const int nw = tile_cols(mtiles * ((N + kBN - 1) / kBN), d->num_sms);
     CUtensorMap ta, tb, ty;
-    if (make_tmap(&ta, a, K / 2, M, 128) || make_tmap(&tb, b, K / 2, N, 256) || make_tmap_out(&ty, d_bf16, N, M))
+    if (make_tmap(&ta, a, K / 2, M, 128) || make_tmap(&tb, b, K / 2, N, (uint32_t)nw) || make_tmap_out(&ty, d_bf16, N, M))
         return MX_ERR_CUDA;
     GemmArgs g = base_args(sa, sb, K, M, N, d->status);
-    g.num_mtiles_host = (int32_t)((M + kBM - 1) / kBM);
+    g.num_mtiles_host = (int32_t)mtiles;
     g.m_total = M;
-    g.n_tiles = (int32_t)((N + kBN - 1) / kBN);
+    g.n_tiles = (int32_t)((N + nw - 1) / nw);
     g.b_rows_per_expert = N;
     g.n_valid = N;
     g.y = static_cast<uint16_t*>(d_bf16);
     g.ld_y = N;
     return cuda_status(launch_gemm_l2(ta, tb, ty, g, grid_for((int64_t)g.num_mtiles_host * g.n_tiles, d->num_sms), true,
-                                      static_cast<cudaStream_t>(stream)));
+                                      nw, static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_mxfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed) {
@@ -417,12 +423,18 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     if (!mark(2)) return MX_ERR_CUDA;
     const int64_t max_mtiles = L.max_mtiles;
 
+    // Tile widths: 256 columns, or 128 where 256-wide tiles would leave SMs idle. Only with
+    // uniform tiling: the routed tile count is known on the device alone, and its bound
+    // max_mtiles counts an extra tile per expert.
+    const int n1 = routed ? kBN : tile_cols(max_mtiles * (I / 128), d->num_sms);
+    const int n2 = routed ? kBN : tile_cols(max_mtiles * ((H + kBN - 1) / kBN), d->num_sms);
+
     // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
     CUtensorMap ta1, tb1, ty1, ta2, tb2, ty2;
-    if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap_w13(&tb1, w13, H, I, E) ||
-        make_tmap_out(&ty1, hq, I / 2, R, false))
+    if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap_w13(&tb1, w13, H, I, E, (uint32_t)(n1 / 2)) ||
+        make_tmap_out(&ty1, hq, I / 2, R, false, n1 == 128 ? 16u : 32u))
         return MX_ERR_CUDA;
-    g1.n_tiles = (int32_t)(I / 128);
+    g1.n_tiles = (int32_t)(I / (n1 / 2));
     g1.b_rows_per_expert = 2 * I;
     g1.n_half = I;
     g1.n_valid = I;
@@ -430,19 +442,21 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     g1.hs = hs;
     g1.ld_hq = I / 2;
     g1.ld_hs = I / 32;
-    if (launch_gemm_l1(ta1, tb1, ty1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), scales_tiled, s) != cudaSuccess ||
+    if (launch_gemm_l1(ta1, tb1, ty1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), scales_tiled, n1, s) !=
+            cudaSuccess ||
         !mark(3))
         return MX_ERR_CUDA;
 
     // L2: [R, I] x [H, I]^T per expert, BF16 out (to `out` directly without routing).
-    if (make_tmap(&ta2, hq, I / 2, R, 128) || make_tmap(&tb2, w2, I / 2, E * H, 256)) return MX_ERR_CUDA;
-    g2.n_tiles = (int32_t)((H + kBN - 1) / kBN);
+    if (make_tmap(&ta2, hq, I / 2, R, 128) || make_tmap(&tb2, w2, I / 2, E * H, (uint32_t)n2)) return MX_ERR_CUDA;
+    g2.n_tiles = (int32_t)((H + n2 - 1) / n2);
     g2.b_rows_per_expert = H;
     g2.n_valid = H;
     g2.y = routed ? at<uint16_t>(workspace, L.y) : static_cast<uint16_t*>(out);
     g2.ld_y = H;
     if (make_tmap_out(&ty2, g2.y, H, R)) return MX_ERR_CUDA;
-    if (launch_gemm_l2(ta2, tb2, ty2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), scales_tiled, s) != cudaSuccess ||
+    if (launch_gemm_l2(ta2, tb2, ty2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), scales_tiled, n2, s) !=
+            cudaSuccess ||
         !mark(4))
         return MX_ERR_CUDA;
 

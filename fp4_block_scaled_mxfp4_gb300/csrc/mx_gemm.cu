@@ -48,15 +48,13 @@ namespace mx {
 namespace {
 
 constexpr int kABytes = kBM * kBK / 2;                 // 16 KB
-constexpr int kBBytes = kBN * kBK / 2;                 // 32 KB
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemBase = 256;
 constexpr int kSfColsPerStage = 24;
 constexpr uint32_t kFullArrivals = 1;                  // producer (TMA + bulk bytes)
 constexpr uint32_t kSfArrivals = 32;                   // every scale-loader lane (+1 with bulk copies)
-constexpr uint32_t kIdesc = idesc_mxf4(kBM, kBN);
 constexpr int kStagingBytes = 1024;                    // per epilogue warp: 32 rows x 32 bytes
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 5;
 
 // Scale factors reach tensor memory in one of two shared-memory images:
 // Scale factors reach tensor memory by tcgen05.cp. The tensor core reads them per 32-row
@@ -69,11 +67,18 @@ constexpr int kMaxStages = 4;
 // at byte 4 (r / 32) of each half. A replicating copy costs the tensor pipe ~75 cycles and
 // the 128x256b copy almost nothing, so this takes a stage from six replicating copies to
 // four.
-template <bool kWide>
+//
+// kN is the tile's width: 256 columns (L1: 128 gate + 128 up) for the routed forward, 128
+// (64 + 64) where a grid of 256-wide tiles would leave SMs idle (the shared expert at a
+// few hundred tokens). The narrower tile halves each CTA's work per stage, doubles the
+// CTAs, and fits a fifth stage.
+template <int kN>
 struct Cfg {
-    static constexpr int kStages = 4;
+    static constexpr int kStages = kN == 256 ? 4 : 5;
+    static constexpr int kBBytes = kN * kBK / 2;                    // 32 or 16 KB
     static constexpr int kSfaBytes = 4096;
-    static constexpr int kSfbBytes = 2 * 2 * 512;
+    static constexpr int kSfbBytes = (kN / 128) * 2 * 512;          // per 128 rows: 2 K-words x 512 B
+    static constexpr uint32_t kIdesc = idesc_mxf4(kBM, kN);
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static constexpr uint32_t kDescStageStep = kStageBytes >> 4;
     static constexpr int kStagingOff = kStages * kStageBytes;
@@ -111,9 +116,9 @@ struct Ctl {
     int abort_flag;
 };
 
-template <bool kWide>
+template <int kN>
 constexpr size_t smem_bytes() {
-    return (size_t)Cfg<kWide>::kStagingOff + 8 * kStagingBytes + sizeof(Ctl) + 1024;
+    return (size_t)Cfg<kN>::kStagingOff + 8 * kStagingBytes + sizeof(Ctl) + 1024;
 }
 
 struct Tile {
@@ -141,11 +146,16 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs& a, int mt) {
     return t;
 }
 
-// First row (in the stacked B tensor) of B tile rows [h*128, h*128 + 128).
-template <bool kL1>
-__device__ __forceinline__ int64_t b_row(const GemmArgs& a, int expert, int nt, int h) {
-    if (kL1) return (int64_t)expert * a.b_rows_per_expert + (h ? a.n_half : 0) + (int64_t)nt * 128;
-    return (int64_t)expert * a.b_rows_per_expert + (int64_t)nt * kBN + h * 128;
+// Row of the stacked B tensor behind row r of N tile nt (L1: the first kN / 2 tile rows
+// are gate rows, the rest the matching up rows).
+template <bool kL1, int kN>
+__device__ __forceinline__ int64_t b_tile_row(const GemmArgs& a, int expert, int nt, int r) {
+    if (kL1) {
+        constexpr int kHalf = kN / 2;
+        return (int64_t)expert * a.b_rows_per_expert + (r < kHalf ? 0 : a.n_half) + (int64_t)nt * kHalf +
+               (r < kHalf ? r : r - kHalf);
+    }
+    return (int64_t)expert * a.b_rows_per_expert + (int64_t)nt * kN + r;
 }
 
 // Every lane polls; the warp proceeds only if all lanes saw the phase complete, so an
@@ -157,12 +167,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
-template <bool kL1, bool kBTiled>
+template <bool kL1, bool kBTiled, int kN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
-    using C = Cfg<!kBTiled>;
-    constexpr bool kWide = !kBTiled;
+    using C = Cfg<kN>;
+    constexpr int kBBytes = C::kBBytes;
+    constexpr uint32_t kIdesc = C::kIdesc;
     constexpr int kStages = C::kStages;
     constexpr int kStageBytes = C::kStageBytes;
     constexpr int kSfaBytes = C::kSfaBytes;
@@ -182,7 +193,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), kFullArrivals);
             mbar_init(smem_u32(&ctl->empty[s]), 1);  // MMA commit
-            mbar_init(smem_u32(&ctl->sf_full[s]), kSfArrivals + (kBTiled ? 1 : 0));
+            mbar_init(smem_u32(&ctl->sf_full[s]), kSfArrivals + (kBTiled && kN == 256 ? 1 : 0));
             mbar_init(smem_u32(&ctl->ready[s]), 1);   // scale copier commit
         }
         mbar_init(smem_u32(&ctl->tmem_full), 1);
@@ -223,10 +234,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive_expect_tx(bar, kABytes + kBBytes);
                     tma_load_2d(st, &tmA, kt * (kBK / 2), (int32_t)t.row0, bar);
                     if (kL1) {
-                        // w13 as [E][2][I][H/2]: 128 gate rows then the matching 128 up rows
-                        tma_load_4d(st + kABytes, &tmB, kt * (kBK / 2), nt * 128, 0, t.expert, bar);
+                        // w13 as [E][2][I][H/2]: kN / 2 gate rows then the matching up rows
+                        tma_load_4d(st + kABytes, &tmB, kt * (kBK / 2), nt * (kN / 2), 0, t.expert, bar);
                     } else {
-                        tma_load_2d(st + kABytes, &tmB, kt * (kBK / 2), (int32_t)b_row<false>(args, t.expert, nt, 0), bar);
+                        tma_load_2d(st + kABytes, &tmB, kt * (kBK / 2),
+                                    (int32_t)b_tile_row<false, kN>(args, t.expert, nt, 0), bar);
                     }
                 }
             }
@@ -303,14 +315,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const bool half = args.k_tail_half && (kt == k_tiles - 1);
                 const uint32_t st = sbase + s * kStageBytes;
                 const int64_t kcol = (int64_t)kt * 8;   // first 32-element block of this stage
-                if (kBTiled && lane == 0) {
-                    // B scales: K-words 2kt, 2kt+1 of each 128-row group (one at the K tail)
+                if (kBTiled && kN == 256 && lane == 0) {
+                    // B scales: K-words 2kt, 2kt+1 of each 128-row group (one at the K tail);
+                    // each 128-row half of the tile is one whole group of the tile layout
                     const uint32_t sf_bytes = half ? 512u : 1024u;
                     const uint32_t bar = smem_u32(&ctl->sf_full[s]);
                     int64_t grp[2];
                     uint32_t tx = 0;
                     for (int h = 0; h < 2; ++h) {
-                        grp[h] = b_row<kL1>(args, t.expert, nt, h) / 128;
+                        grp[h] = b_tile_row<kL1, kN>(args, t.expert, nt, 128 * h) / 128;
                         if (grp[h] < args.b_groups) tx += sf_bytes;
                     }
                     mbar_arrive_expect_tx(bar, tx);
@@ -318,6 +331,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (grp[h] < args.b_groups)
                             bulk_load(st + kABytes + kBBytes + kSfaBytes + h * 1024,
                                       args.sfb + (grp[h] * args.kw + 2 * kt) * 512, sf_bytes, bar);
+                }
+                if (kBTiled && kN == 128) {
+                    // B scales in tile layout for a 128-row tile of two 64-row pieces (L1) that
+                    // need not share a 128-row group: per 32-row chunk c, this lane's word of
+                    // row 32 c + lane, at byte lane * 16 + 4 j of its group's block
+                    const uint32_t sfb_s = st + kABytes + kBBytes + kSfaBytes;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int64_t r0 = b_tile_row<kL1, kN>(args, t.expert, nt, 32 * c);   // multiple of 32
+                        const bool valid = r0 + lane < args.b_rows;
+                        const uint8_t* src = args.sfb + (valid ? ((r0 >> 7) * args.kw + 2 * kt) * 512 + lane * 16 +
+                                                                      ((r0 & 127) >> 5) * 4
+                                                                : 0);
+#pragma unroll
+                        for (int wd = 0; wd < 2; ++wd) {
+                            const bool ok = valid && (wd == 0 || !half);
+                            cp_async_4(sfb_s + wd * 512 + lane * 16 + c * 4, ok ? src + 512 * wd : args.sfb,
+                                       ok ? 4u : 0u);
+                        }
+                    }
                 }
                 // Row r = 32 j + lane of a 128-row group. Dense image: 512-byte block per
                 // K-word, byte lane * 16 + j * 4. Wide image: wide_off(r, half), A's halves
@@ -340,11 +373,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!kBTiled) {
                     const uint32_t sfb_s = st + kABytes + kBBytes + kSfaBytes;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int64_t rbase = b_row<kL1>(args, t.expert, nt, h);
+                    for (int h = 0; h < kN / 128; ++h) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const int64_t brow = rbase + 32 * j + lane;
+                            const int64_t brow = b_tile_row<kL1, kN>(args, t.expert, nt, 128 * h + 32 * j + lane);
                             const bool valid = brow < args.b_rows;
                             const uint8_t* src = args.sfb + (valid ? brow * args.ld_sf + kcol : 0);
 #pragma unroll
@@ -387,7 +419,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_cp_128x256b(sfa_t, desc_sf_wide(sfa_s));                                // A, both K-words
                     for (int wd = 0; wd < nwords; ++wd) {
                         tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 512));          // B rows 0-127
-                        tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + 1024 + wd * 512));  // 128-255
+                        if (kN == 256)
+                            tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + 1024 + wd * 512));  // 128-255
                     }
                     tc_commit(smem_u32(&ctl->ready[s]));   // arrives once the copies are in TMEM
                 }
@@ -413,15 +446,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int nt = w % args.n_tiles;
             if (!warp_wait(smem_u32(&ctl->tmem_full), tc & 1u, abort_flag, args.status, kErrWaitTmemFull)) break;
             tc_fence_after();
+            // Warp (q, hf) owns rows 32 q..32 q + 31 and half hf of the tile's columns. L1: kHB
+            // blocks of 32 columns of h, i.e. gate columns (kN / 4) hf + 32 b and the matching
+            // up columns kN / 2 + (kN / 4) hf + 32 b; L2: kPieces pieces of 32 output columns.
+            constexpr int kHB = kN / 128;
+            constexpr int kPieces = kN / 64;
             uint32_t v[4][32];
             if (kL1) {
-                tc_ld_32x32b_x32(taddr + 64 * hf, v[0]);            // gate, block 0
-                tc_ld_32x32b_x32(taddr + 64 * hf + 32, v[1]);       // gate, block 1
-                tc_ld_32x32b_x32(taddr + 128 + 64 * hf, v[2]);      // up, block 0
-                tc_ld_32x32b_x32(taddr + 128 + 64 * hf + 32, v[3]); // up, block 1
+#pragma unroll
+                for (int b = 0; b < kHB; ++b) {
+                    tc_ld_32x32b_x32(taddr + (kN / 4) * hf + 32 * b, v[b]);               // gate
+                    tc_ld_32x32b_x32(taddr + kN / 2 + (kN / 4) * hf + 32 * b, v[2 + b]);  // up
+                }
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) tc_ld_32x32b_x32(taddr + 128 * hf + 32 * i, v[i]);
+                for (int i = 0; i < kPieces; ++i) tc_ld_32x32b_x32(taddr + (kN / 2) * hf + 32 * i, v[i]);
             }
             tc_wait_ld();
             tc_fence_before();
@@ -431,8 +470,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // all 32 rows of this warp are in the tile: staged TMA stores
                 const int32_t trow = (int32_t)(t.row0 + 32 * q);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int64_t col = (int64_t)nt * kBN + 128 * hf + 32 * i;
+                for (int i = 0; i < kPieces; ++i) {
+                    const int64_t col = (int64_t)nt * kN + (kN / 2) * hf + 32 * i;
                     if (col >= args.n_valid) break;
                     uint32_t p[16];
 #pragma unroll
@@ -458,12 +497,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             if (kL1 && 32 * q + 32 <= t.rows) {
                 // all 32 rows of this warp are in the tile: codes through a staged TMA store
+                // of 32 rows x 16 kHB bytes
                 const int64_t grow = t.row0 + row_in_tile;
-                const int64_t col0 = (int64_t)nt * 128 + 64 * hf;   // first column of h
-                uint4 cds[2];
-                uint32_t es[2];
+                const int64_t col0 = (int64_t)nt * (kN / 2) + (kN / 4) * hf;   // first column of h
+                uint4 cds[kHB];
+                uint32_t es[kHB];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
+                for (int b = 0; b < kHB; ++b) {
                     float h[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -475,24 +515,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 if (lane == 0) bulk_wait_read();   // the previous store has read the block
                 __syncwarp();
-                uint4* row = reinterpret_cast<uint4*>(staging + lane * 32);
-                row[0] = cds[0];
-                row[1] = cds[1];
+                uint4* row = reinterpret_cast<uint4*>(staging + lane * 16 * kHB);
+#pragma unroll
+                for (int b = 0; b < kHB; ++b) row[b] = cds[b];
                 fence_proxy_async_smem();          // generic writes -> the TMA engine's reads
                 __syncwarp();
                 if (lane == 0) {
                     tma_store_2d(&tmY, staging_s, (int32_t)(col0 / 2), (int32_t)(t.row0 + 32 * q));
                     bulk_commit();
                 }
-                *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col0 / 32) =
-                    (uint16_t)(es[0] | (es[1] << 8));
+                if (kHB == 2)
+                    *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col0 / 32) =
+                        (uint16_t)(es[0] | (es[kHB - 1] << 8));
+                else
+                    args.hs[grow * args.ld_hs + col0 / 32] = (uint8_t)es[0];
                 continue;
             }
             if (row_in_tile >= t.rows) continue;
             const int64_t grow = t.row0 + row_in_tile;
             if (kL1) {
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
+                for (int b = 0; b < kHB; ++b) {
                     float h[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -502,14 +545,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     uint4 codes;
                     const uint32_t E = mx_quant32(h, codes);
-                    const int64_t col = (int64_t)nt * 128 + 64 * hf + 32 * b;   // column of h
+                    const int64_t col = (int64_t)nt * (kN / 2) + (kN / 4) * hf + 32 * b;   // column of h
                     *reinterpret_cast<uint4*>(args.hq + grow * args.ld_hq + col / 2) = codes;
                     args.hs[grow * args.ld_hs + col / 32] = (uint8_t)E;
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int64_t col = (int64_t)nt * kBN + 128 * hf + 32 * i;
+                for (int i = 0; i < kPieces; ++i) {
+                    const int64_t col = (int64_t)nt * kN + (kN / 2) * hf + 32 * i;
                     uint32_t p[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
@@ -537,7 +580,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <bool kL1, bool kBTiled>
+template <bool kL1, bool kBTiled, int kN>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a, int grid,
                    cudaStream_t s) {
     static int configured_mask = 0;   // one bit per device
@@ -545,27 +588,35 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
-        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1, kBTiled>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_bytes<!kBTiled>());
+        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1, kBTiled, kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem_bytes<kN>());
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
-    mxf4_gemm_kernel<kL1, kBTiled><<<grid, kGemmThreads, smem_bytes<!kBTiled>(), s>>>(ta, tb, ty, a);
+    mxf4_gemm_kernel<kL1, kBTiled, kN><<<grid, kGemmThreads, smem_bytes<kN>(), s>>>(ta, tb, ty, a);
     return cudaGetLastError();
+}
+
+template <bool kL1>
+cudaError_t launch_any(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                       int grid, bool b_tiled, int n_cols, cudaStream_t s) {
+    if (n_cols == 128)
+        return b_tiled ? launch<kL1, true, 128>(ta, tb, ty, a, grid, s) : launch<kL1, false, 128>(ta, tb, ty, a, grid, s);
+    return b_tiled ? launch<kL1, true, 256>(ta, tb, ty, a, grid, s) : launch<kL1, false, 256>(ta, tb, ty, a, grid, s);
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>(); }
+size_t gemm_smem_bytes() { return smem_bytes<256>() > smem_bytes<128>() ? smem_bytes<256>() : smem_bytes<128>(); }
 
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
-                           int grid, bool b_tiled, cudaStream_t s) {
-    return b_tiled ? launch<true, true>(ta, tb, ty, a, grid, s) : launch<true, false>(ta, tb, ty, a, grid, s);
+                           int grid, bool b_tiled, int n_cols, cudaStream_t s) {
+    return launch_any<true>(ta, tb, ty, a, grid, b_tiled, n_cols, s);
 }
 
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
-                           int grid, bool b_tiled, cudaStream_t s) {
-    return b_tiled ? launch<false, true>(ta, tb, ty, a, grid, s) : launch<false, false>(ta, tb, ty, a, grid, s);
+                           int grid, bool b_tiled, int n_cols, cudaStream_t s) {
+    return launch_any<false>(ta, tb, ty, a, grid, b_tiled, n_cols, s);
 }
 
 }  // namespace mx

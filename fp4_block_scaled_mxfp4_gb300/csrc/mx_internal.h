@@ -9,7 +9,7 @@ namespace mx {
 
 // ---- GEMM tile geometry (tcgen05 kind::mxf4, one CTA per tile, M = 128, N = 256) ----
 constexpr int kBM = 128;           // rows of A per tile (TMEM lanes)
-constexpr int kBN = 256;           // columns of the accumulator (L1: 128 gate + 128 up)
+constexpr int kBN = 256;           // columns of the accumulator (L1: 128 gate + 128 up); 128 for small M
 constexpr int kBK = 256;           // E2M1 elements of K per pipeline stage (128 bytes)
 constexpr int kStages = 4;
 constexpr int kGemmThreads = 384;  // 4 control warps + 8 epilogue warps
@@ -52,12 +52,15 @@ struct GemmArgs {
 };
 
 size_t gemm_smem_bytes();
-// ty: the output as a 2-D tensor map with boxes of 32 rows x 32 bytes, no swizzle: L1 the codes hq
-// [rows, ld_hq] (bytes), L2 the BF16 y [rows, ld_y].
+// n_cols: the tile's width, 256 (L1: 128 gate + 128 up columns) or 128 (64 + 64), used where
+// 256-wide tiles would leave SMs idle. tb: B in boxes of 128 bytes x n_cols rows (L1: the 4-D
+// w13 view with n_cols / 2 rows of each half). ty: the output as a 2-D tensor map, no swizzle,
+// boxes of 32 rows x 32 bytes (L2 BF16; L1 codes with n_cols = 256) or 32 rows x 16 bytes
+// (L1 codes with n_cols = 128): L1 the codes hq [rows, ld_hq], L2 the BF16 y [rows, ld_y].
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
-                           int grid, bool b_tiled, cudaStream_t s);
+                           int grid, bool b_tiled, int n_cols, cudaStream_t s);
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
-                           int grid, bool b_tiled, cudaStream_t s);
+                           int grid, bool b_tiled, int n_cols, cudaStream_t s);
 
 // ---- element-wise kernels ----
 // Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][512 B] (kb % 4 == 0).
