@@ -237,6 +237,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Programmatic dependent launch. A kernel of the forward launched with programmatic stream
+// serialisation may start while the kernel before it in the stream is still finishing: it
+// does its setup, then pdl_wait() until that kernel (and, transitively, every earlier one)
+// has completed and its memory is visible, before touching global memory. Each kernel
+// calls pdl_launch_dependents() once the next kernel may be scheduled. Without the launch
+// attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)

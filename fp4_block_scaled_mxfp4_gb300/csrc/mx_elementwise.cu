@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kThreads) fp8_dequant_kernel(const uint8_t* __
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __restrict__ x8,
                                                              uint4* __restrict__ codes16,
                                                              uint8_t* __restrict__ sf, int64_t blocks) {
+    pdl_wait();
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < blocks; b += stride) {
         float f[32];
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __rest
         sf[b] = (uint8_t)mx_quant32(f, codes);
         codes16[b] = codes;
     }
+    pdl_launch_dependents();
 }
 
 // out[t, c] = bf16( sum_k w[t,k] * y[row_of[t,k], c] ), float32, slot order, no FMA.
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
                                                            const float* __restrict__ w,
                                                            uint4* __restrict__ out8, int64_t groups,
                                                            int64_t groups_per_row, int K) {
+    pdl_wait();
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < groups; g += stride) {
         const int64_t t = g / groups_per_row;
@@ -229,6 +232,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
                              pack2(f32_to_bf16(acc[4]), f32_to_bf16(acc[5])),
                              pack2(f32_to_bf16(acc[6]), f32_to_bf16(acc[7])));
     }
+    pdl_launch_dependents();
 }
 
 // Scale tensor [rows, kb] (kb = K/32 bytes per row) -> tile layout: for row group g of 128
@@ -288,9 +292,8 @@ cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int
                              int num_sms, cudaStream_t s) {
     const int64_t blocks = M * (K / 32);
     if (blocks == 0) return cudaSuccess;
-    act_quant_kernel<<<grid_for(blocks, num_sms), kThreads, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks);
-    return cudaGetLastError();
+    return launch_pdl(act_quant_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
+                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks);
 }
 
 cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,
@@ -298,10 +301,8 @@ cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float
     const int64_t gpr = H / 8;
     const int64_t groups = T * gpr;
     if (groups == 0) return cudaSuccess;
-    combine_kernel<<<grid_for(groups, num_sms), kThreads, 0, s>>>(reinterpret_cast<const uint4*>(y), row_of,
-                                                                  w, reinterpret_cast<uint4*>(out), groups,
-                                                                  gpr, (int)K);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(grid_for(groups, num_sms)), dim3(kThreads), 0, s,
+                      reinterpret_cast<const uint4*>(y), row_of, w, reinterpret_cast<uint4*>(out), groups, gpr, (int)K);
 }
 
 }  // namespace mx

@@ -214,6 +214,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+    // Setup done: wait for the kernels before this one, then let the next one be scheduled
+    // (all of this persistent grid's CTAs are resident already, so it cannot take their SMs).
+    pdl_wait();
+    pdl_launch_dependents();
 
     const int total = num_mtiles(args) * args.n_tiles;
     const int k_tiles = args.k_tiles;
@@ -593,8 +597,8 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
-    mxf4_gemm_kernel<kL1, kBTiled, kN><<<grid, kGemmThreads, smem_bytes<kN>(), s>>>(ta, tb, ty, a);
-    return cudaGetLastError();
+    return launch_pdl(mxf4_gemm_kernel<kL1, kBTiled, kN>, dim3(grid), dim3(kGemmThreads), smem_bytes<kN>(), s, ta, tb, ty,
+                      a);
 }
 
 template <bool kL1>

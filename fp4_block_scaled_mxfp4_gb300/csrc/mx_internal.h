@@ -7,6 +7,24 @@
 
 namespace mx {
 
+// Launch a kernel of the forward with programmatic stream serialisation (see pdl_wait in
+// mx_device.cuh): it may be scheduled before the previous kernel in the stream completes and
+// waits for it on the device.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- GEMM tile geometry (tcgen05 kind::mxf4, one CTA per tile, M = 128, N = 256) ----
 constexpr int kBM = 128;           // rows of A per tile (TMEM lanes)
 constexpr int kBN = 256;           // columns of the accumulator (L1: 128 gate + 128 up); 128 for small M

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kCountThreads) route_count_kernel(const int32_
                                                                     int32_t* __restrict__ local_rank) {
     __shared__ int32_t s_run[kMaxExperts];
     __shared__ int32_t s_warp[kCountWarps][kMaxExperts];
+    pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < E; e += kCountThreads) s_run[e] = 0;
     const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
@@ -55,6 +56,7 @@ __global__ void __launch_bounds__(kCountThreads) route_count_kernel(const int32_
         __syncthreads();
     }
     for (int e = tid; e < E; e += kCountThreads) chunk_counts[(int64_t)blockIdx.x * E + e] = s_run[e];
+    pdl_launch_dependents();
 }
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ chunk_counts,
@@ -62,6 +64,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
     __shared__ int32_t s_cnt[kMaxExperts];
     __shared__ int32_t s_off[kMaxExperts + 1];
     __shared__ int32_t s_toff[kMaxExperts + 1];
+    pdl_wait();
     const int tid = threadIdx.x;
     for (int e = tid; e < E; e += blockDim.x) {
         int32_t run = 0;
@@ -98,6 +101,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
             rb.tile_rows[idx] = min(kBM, s_cnt[e] - m * kBM);
         }
     }
+    pdl_launch_dependents();
 }
 
 constexpr int kGatherThreads = 256;
@@ -109,6 +113,7 @@ __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
     const uint4* __restrict__ x8, const int32_t* __restrict__ ids, int K, int E, int64_t blocks_per_row,
     RouteBufs rb, uint4* __restrict__ xq16, uint8_t* __restrict__ xs) {
     __shared__ int32_t s_rows[kMaxTopK];
+    pdl_wait();
     const int64_t t = blockIdx.x;
     const int tid = threadIdx.x;
     if (tid < K) {
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
             xs[(int64_t)r * blocks_per_row + b] = (uint8_t)e8;
         }
     }
+    pdl_launch_dependents();
 }
 
 }  // namespace
@@ -151,20 +157,18 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, co
                          cudaStream_t s) {
     const int64_t n = T * K;
     if (n == 0) return cudaSuccess;
-    route_count_kernel<<<(unsigned)rb.nchunks, kCountThreads, 0, s>>>(ids, n, (int)E, rb.chunk_counts,
-                                                                       rb.local_rank);
-    cudaError_t err = cudaGetLastError();
+    const cudaError_t err = launch_pdl(route_count_kernel, dim3((unsigned)rb.nchunks), dim3(kCountThreads), 0, s, ids,
+                                       n, (int)E, rb.chunk_counts, rb.local_rank);
     if (err != cudaSuccess) return err;
-    route_scan_kernel<<<1, 1024, 0, s>>>(rb.chunk_counts, rb.nchunks, (int)E, rb);
-    return cudaGetLastError();
+    return launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, rb.chunk_counts, rb.nchunks, (int)E, rb);
 }
 
 cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,
                                 int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    quant_gather_kernel<<<(unsigned)T, kGatherThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), ids, (int)K,
-                                                               (int)E, H / 32, rb, reinterpret_cast<uint4*>(xq), xs);
-    return cudaGetLastError();
+    return launch_pdl(quant_gather_kernel, dim3((unsigned)T), dim3(kGatherThreads), 0, s,
+                      reinterpret_cast<const uint4*>(x), ids, (int)K, (int)E, (int64_t)(H / 32), rb,
+                      reinterpret_cast<uint4*>(xq), xs);
 }
 
 }  // namespace mx
