@@ -191,8 +191,11 @@ def test_gemm_scale_path_constant_codes(mx):
     _gemm_case(mx, a, sa, b, sb, "constant codes")
 
 
+# A GEMM with fewer than 152 work units of 128 x 256 runs 128-column tiles; the last two
+# shapes (160 units) run 256-column tiles.
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (128, 256, 128), (77, 256, 1024), (300, 512, 2048),
-                                   (129, 272, 384), (1000, 1024, 7168), (513, 7168, 3072)])
+                                   (129, 272, 384), (1000, 1024, 7168), (513, 7168, 3072),
+                                   (1280, 4096, 512), (2048, 2560, 384)])
 def test_gemm_random(mx, M, N, K):
     rng = np.random.default_rng(M + N + K)
     a = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
