@@ -1,9 +1,11 @@
 // mx_gemm.cu -- grouped block-scaled MXFP4 GEMM on the sm_103a tensor cores (tcgen05,
 // kind::mxf4, E2M1 x E2M1 with E8M0 scales per 32 elements of K, FP32 accumulation in
 // tensor memory), with the two epilogues of the expert FFN:
-//   L1: D = A . W13^T over a tile of 128 gate + 128 up columns; the epilogue rounds g and u
-//       to BF16, forms h = bf16(silu(g) * u) and re-quantises h to MXFP4 (codes + E8M0).
-//   L2: D = A . W2^T over 256 output columns; the epilogue writes BF16.
+//   L1: D = A . W13^T over a tile of kN / 2 gate + kN / 2 up columns; the epilogue rounds g
+//       and u to BF16, forms h = bf16(silu(g) * u) and re-quantises h to MXFP4 (codes + E8M0).
+//   L2: D = A . W2^T over kN output columns; the epilogue writes BF16.
+// Tiles are 128 rows x kN columns, kN = 256, or 128 where 256-wide tiles would leave SMs
+// idle (see Cfg).
 // The pipeline is the one the pages describe for their CuTeDSL experts kernel ("Current
 // Bug: vLLM produces empty/garbage output", "Phase 1: CuTeDSL Shared Expert Kernel":
 // L1 GEMM -> SiLU -> re-quant -> L2 GEMM; the shared expert is the one-group case), with
@@ -11,11 +13,10 @@
 // weight format confirmed".
 //
 // CTA layout (384 threads, one CTA per SM, persistent over the tile list):
-//   warp 0      TMA producer: A tile (128 rows x 128 B) and B tile (256 rows x 128 B) per
-//               K stage of 256 elements, 128-byte swizzle, into a 4-stage ring. Two TMA
-//               instructions per stage (L1's B is one box of a 4-D view of the stacked
-//               gate/up weights holding both halves): issuing one costs the thread ~160
-//               cycles, so more per stage would make this thread the pipeline's limit.
+//   warp 0      TMA producer: A tile (128 rows x 128 B) and B tile (kN rows x 128 B) per
+//               K stage of 256 elements, 128-byte swizzle, into a 4- or 5-stage ring. Two
+//               TMA instructions per stage: L1's B is one box of a 4-D view of the stacked
+//               gate/up weights holding both halves.
 //   warp 1      allocates 512 TMEM columns; lane 0 issues the 4 MMAs (K = 64 each) of a
 //               stage and commits the stage free. Nothing else runs in that thread: the
 //               tensor core's instruction queue is short, and any other work between two
@@ -24,8 +25,9 @@
 //               of A (and of B when they are not in tile layout) into the 32-lane x 16-byte
 //               blocks tcgen05.cp reads; each lane's copies arrive on the stage's scale
 //               barrier when they land (cp.async.mbarrier.arrive), so it never blocks. With
-//               B's scales in tile layout (kBTiled), lane 0 fetches them with two 1 KB bulk
-//               copies (one per 128-row group) on the same barrier.
+//               B's scales in tile layout (kBTiled) and kN = 256, lane 0 fetches them with
+//               two 1 KB bulk copies (one per 128-row group) on the same barrier; with
+//               kN = 128 each lane copies its 4-byte words.
 //   warp 3      scale-factor copier: lane 0 waits for a stage's operands and scale tiles,
 //               moves the scales into that stage's TMEM slot (tcgen05.cp) and commits the
 //               copies to the stage's ready barrier, which the MMA thread waits on.
@@ -33,11 +35,16 @@
 //               columns; they drain the accumulator to registers, release it, then compute.
 //               Outputs leave through a 1 KB shared staging block per warp and an
 //               asynchronous TMA store (L2: 32 rows x 16 BF16 columns; L1: 32 rows x 32
-//               bytes of codes), so the warp never waits for its stores (32 scattered
-//               16-byte row pieces per store instruction otherwise); a warp whose 32 rows
-//               are not all in the tile stores directly.
-// TMEM: columns [0, 256) accumulator; [256 + 24 s, 256 + 24 s + 24) the scale factors of
+//               bytes of codes, 16 at kN = 128), so the warp never waits for its stores (32
+//               scattered 16-byte row pieces per store instruction otherwise); a warp whose
+//               32 rows are not all in the tile stores directly.
+// TMEM: columns [0, kN) accumulator; [256 + 24 s, 256 + 24 s + 24) the scale factors of
 // stage s (A: 2 K-words x 4 columns, B: 2 K-words x 8 columns).
+//
+// What bounds it, measured on all SMs: one K stage takes ~920 cycles against 512 cycles of
+// MMAs. The tensor pipe executes, per stage, the four MMAs, four replicating B-scale
+// copies (~85 cycles each) and the A-scale copy (~30), ~880 cycles in all. The TMA -> MMA
+// ring alone, with one thread issuing both loads of a stage, settles at ~860.
 #include <cuda.h>
 
 #include "mx_device.cuh"
@@ -51,12 +58,11 @@ constexpr int kABytes = kBM * kBK / 2;                 // 16 KB
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemBase = 256;
 constexpr int kSfColsPerStage = 24;
-constexpr uint32_t kFullArrivals = 1;                  // producer (TMA + bulk bytes)
+constexpr uint32_t kFullArrivals = 1;                  // producer (with the TMA bytes)
 constexpr uint32_t kSfArrivals = 32;                   // every scale-loader lane (+1 with bulk copies)
 constexpr int kStagingBytes = 1024;                    // per epilogue warp: 32 rows x 32 bytes
 constexpr int kMaxStages = 5;
 
-// Scale factors reach tensor memory in one of two shared-memory images:
 // Scale factors reach tensor memory by tcgen05.cp. The tensor core reads them per 32-row
 // slice from that slice's own lane quarter: A's scale of row r at lane r, column r / 32
 // (+4 for the stage's second K-word); B's scales, which every slice needs, at every lane of
@@ -64,9 +70,9 @@ constexpr int kMaxStages = 5;
 // 16 bytes, replicated into the four quarters), and A's by one tcgen05.cp.128x256b for
 // both K-words from a 4 KB image: 128 rows x 32 bytes in 8-row x 16-byte core matrices
 // (8-row groups 256 bytes apart, a row's two 16-byte halves 128 bytes apart), row r's word
-// at byte 4 (r / 32) of each half. A replicating copy costs the tensor pipe ~75 cycles and
-// the 128x256b copy almost nothing, so this takes a stage from six replicating copies to
-// four.
+// at byte 4 (r / 32) of each half. A replicating copy costs the tensor pipe ~85 cycles and
+// the 128x256b copy ~30, so this takes a stage from six replicating copies to four (two at
+// kN = 128).
 //
 // kN is the tile's width: 256 columns (L1: 128 gate + 128 up) for the routed forward, 128
 // (64 + 64) where a grid of 256-wide tiles would leave SMs idle (the shared expert at a
@@ -356,9 +362,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                     }
                 }
-                // Row r = 32 j + lane of a 128-row group. Dense image: 512-byte block per
-                // K-word, byte lane * 16 + j * 4. Wide image: wide_off(r, half), A's halves
-                // its two K-words, B's (one 4 KB image per K-word) its two 128-row halves.
+                // Row r = 32 j + lane of a 128-row group. B's dense blocks: 512 bytes per
+                // K-word, byte lane * 16 + j * 4. A's wide image: wide_off(r, K-word).
                 {
                     const uint32_t sfa_s = st + kABytes + kBBytes;
 #pragma unroll
