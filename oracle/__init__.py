@@ -24,5 +24,7 @@ from .mxfp4_oracle import (  # noqa: F401
     moe_route,
     swiglu_bf16,
     moe_flops_per_pair,
+    nvfp4_dequant,
+    nvfp4_values,
     unpack_nibbles,
 )

@@ -23,6 +23,10 @@ Sources (page title -- section):
        final scatter).
 [DG]   "2026-05-11 -- DeepSeek V4 NVFP4 vLLM Serving: Full End-to-End" -- "What We Fixed",
        item 1: FP8 block scales with quant_block_shape=(128, 128) and use_e8m0=True.
+[NVQ]  "Current Bug: vLLM produces empty/garbage output" -- "What we know", "Confirmed
+       working": all NVFP4 weights dequantise correctly to BF16 (a standalone test).
+[GS]   same page -- "Phase 2: CuTeDSL Attention Kernel": a projection carries a per-tensor
+       global scale (weight_scale_2); the MoE's gate and up carry different ones.
 
 Element formats follow the OCP Microscaling (MX) v1.0 definitions of E2M1, E8M0 and the
 E4M3 ("fn": no infinities, S.1111.111 is NaN) encoding; the pages name the formats but
@@ -50,6 +54,13 @@ R7  A NaN result is written as the quiet NaN 0x7FC0 with the element's sign bit 
     code bit 3, E4M3 bit 7); infinities and overflow follow BF16 round-to-nearest-even.
 R8  The BF16 rounding of an exact value is round-to-nearest, ties to even, with BF16
     subnormals (BF16 has float32's exponent range).
+R11 An NVFP4 tensor ([NVQ], [GS]; the pages print no layout) holds E2M1 codes packed as in
+    MXFP4 (two per byte, lower nibble first), one E4M3 ("fn") scale per 16 columns and one
+    float32 global scale per tensor; its value is LUT[code] * e4m3(scale) * global.
+R12 NVFP4 -> BF16 rounds the exact product once to float32 and then to BF16, both to
+    nearest-even: what float32 arithmetic gives, since LUT[code] * e4m3(scale) is exact in
+    float32. A NaN result (a NaN scale byte, a NaN global, or 0 times an infinite global)
+    is 0x7FC0 with the XOR of the code's, the scale's and the global's sign bits.
 
 Parity status: every function below is pinned by the ``-m "not gpu"`` tests (tables from
 the OCP MX definitions and torch's float8 conversions, one-hot nibble/scale tests, the
@@ -65,6 +76,7 @@ __all__ = [
     "e2m1_decode", "e8m0_decode", "e4m3fn_decode", "bf16_bits_from_f64", "bf16_bits_to_f64",
     "unpack_nibbles", "mxfp4_values", "mxfp4_dequant", "fp8_block_dequant_128x128",
     "act_quant_mxfp4", "mxfp4_gemm_bf16", "mxfp4_gemm_blockint", "moe_route", "moe_forward",
+    "nvfp4_values", "nvfp4_dequant",
     "moe_flops_per_pair", "moe_l1_exact", "swiglu_bf16", "moe_l2_bf16", "moe_combine",
 ]
 
@@ -190,6 +202,39 @@ def fp8_block_dequant_128x128(q, sf) -> np.ndarray:
     scale = np.repeat(np.repeat(s, 128, axis=0), 128, axis=1)[:R, :C]
     vals = e4m3fn_decode(np.arange(256))[q] * scale  # 256-entry E4M3 table, then the block scale
     return bf16_bits_from_f64(vals, nan_sign=(q >> 7).astype(bool))
+
+
+# --------------------------------------------------------------------------------------
+# NVFP4 tensors (readings R11, R12) [NVQ], [GS]
+# --------------------------------------------------------------------------------------
+
+
+def nvfp4_values(codes, sf, global_scale) -> np.ndarray:
+    """Exact float64 value of an NVFP4 tensor (R11): LUT[code(r, c)] * e4m3(sf[r, c // 16])
+    * global. codes uint8 [..., C/2], sf uint8 [..., C/16] (E4M3 bytes), global a float32
+    scalar. Exact: the three factors carry at most 2 + 4 + 24 significant bits."""
+    nib = unpack_nibbles(codes)
+    C = nib.shape[-1]
+    sf = np.asarray(sf, dtype=np.uint8)
+    if sf.shape[-1] * 16 != C:
+        raise ValueError("need one scale per 16 logical columns")
+    lut = e2m1_decode(np.arange(16))
+    e4 = e4m3fn_decode(np.arange(256))
+    g = float(np.float32(global_scale))
+    with np.errstate(invalid="ignore"):
+        return lut[nib] * np.repeat(e4[sf], 16, axis=-1) * g
+
+
+def nvfp4_dequant(codes, sf, global_scale) -> np.ndarray:
+    """NVFP4 -> BF16 bits [R, C] (R12): the exact value rounded to float32, then to BF16."""
+    nib = unpack_nibbles(codes)
+    sf = np.asarray(sf, dtype=np.uint8)
+    vals = nvfp4_values(codes, sf, global_scale)
+    with np.errstate(over="ignore", invalid="ignore"):
+        f32 = vals.astype(np.float32).astype(np.float64)       # IEEE round to nearest even
+    g_neg = bool(np.signbit(np.float32(global_scale)))
+    sign = ((nib >> 3) ^ np.repeat(sf >> 7, 16, axis=-1) ^ np.uint8(g_neg)).astype(bool)
+    return bf16_bits_from_f64(f32, nan_sign=sign)
 
 
 # --------------------------------------------------------------------------------------
