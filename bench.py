@@ -37,7 +37,7 @@ import numpy as np  # noqa: E402
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import CONFIGS, make_config_inputs, make_dequant_inputs, make_moe_inputs  # noqa: E402
+from workloads import CONFIGS, make_config_inputs, make_dequant_inputs, make_moe_inputs, make_nvfp4_scales  # noqa: E402
 
 METRIC = "MoE fwd TFLOP/s (MXFP4 grouped GEMM) & dequant GB/s, % of roofline, 1 GB300"
 WORKLOAD = ("routed MoE prefill forward: T=8192 tokens, hidden 7168, intermediate 3072, 48 experts, "
@@ -432,6 +432,18 @@ def measure_extra(mx, torch, dev, stream):
     ms = timeit(deq)
     nbytes = w13.nbytes + s13.nbytes + w2.nbytes + s2.nbytes + (o13.numel() + o2.numel()) * 2
     res["mxfp4_dequant"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm, "ms": ms,
+                            "bytes": nbytes}
+    # the same expert codes as NVFP4 (E4M3 per 16 columns + float32 global scale)
+    n13, n2, g = make_nvfp4_scales()
+    t["n13"], t["n2"] = torch.from_numpy(n13).to(dev), torch.from_numpy(n2).to(dev)
+
+    def nvdeq():
+        mx.nvfp4_dequant(t["w13"], t["n13"], g, o13, stream=stream)
+        mx.nvfp4_dequant(t["w2"], t["n2"], g, o2, stream=stream)
+
+    ms = timeit(nvdeq)
+    nbytes = w13.nbytes + n13.nbytes + w2.nbytes + n2.nbytes + (o13.numel() + o2.numel()) * 2
+    res["nvfp4_dequant"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm, "ms": ms,
                             "bytes": nbytes}
     del o13, o2
     of = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)

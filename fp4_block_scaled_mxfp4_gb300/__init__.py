@@ -1,8 +1,9 @@
 """GB300 (sm_103a) MXFP4 mixture-of-experts expert FFN.
 
 The compute path is the C-ABI library ``libmxfp4moe.so`` (hand-written CUDA: tcgen05
-block-scaled grouped GEMM, routing, MX quantiser, combine, dequant kernels); this package
-only builds it (``build.build()``) and marshals torch tensors into its calls.
+block-scaled grouped GEMM, routing, MX quantiser, combine, MXFP4 / NVFP4 / FP8 dequant
+kernels); this package only builds it (``build.build()``) and marshals torch tensors into
+its calls.
 """
 from ._native import (  # noqa: F401
     MXError,
@@ -19,5 +20,6 @@ from ._native import (  # noqa: F401
     mxfp4_gemm_bf16,
     mxfp4_scales_to_tiled,
     mxfp4_tiled_scales_bytes,
+    nvfp4_dequant,
     status_string,
 )

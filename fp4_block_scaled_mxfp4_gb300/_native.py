@@ -24,6 +24,7 @@ _SIGNATURES = {
     "mx_device_status": (ctypes.c_int, [ctypes.c_int]),
     "mxfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "fp8_block_dequant_128x128": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "nvfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "act_quant_mxfp4": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "mxfp4_tiled_scales_bytes": (ctypes.c_size_t, [_c_i64, _c_i64]),
     "mxfp4_scales_to_tiled": (ctypes.c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
@@ -121,6 +122,21 @@ def mxfp4_dequant(codes, sf, out, stream=None) -> None:
         raise ValueError("out must be bfloat16 (or its 16-bit bit pattern)")
     _need(out, out.dtype, (R, C), "out")
     _check(lib().mxfp4_dequant(_ptr(codes), _ptr(sf), _ptr(out), R, C, _stream(stream)), "mxfp4_dequant")
+
+
+def nvfp4_dequant(codes, sf, global_scale, out, stream=None) -> None:
+    """out[r, c] = bf16(float32(E2M1(codes) * e4m3(sf[r, c/16]) * global_scale));
+    codes u8 [R, C/2], sf u8 [R, C/16] (E4M3 bytes), global_scale a float, out [R, C]."""
+    import torch
+    R, half = codes.shape
+    C = 2 * half
+    _need(codes, torch.uint8, (R, half), "codes")
+    _need(sf, torch.uint8, (R, C // 16), "sf")
+    if not _bf16_like(out):
+        raise ValueError("out must be bfloat16 (or its 16-bit bit pattern)")
+    _need(out, out.dtype, (R, C), "out")
+    _check(lib().nvfp4_dequant(_ptr(codes), _ptr(sf), float(global_scale), _ptr(out), R, C, _stream(stream)),
+           "nvfp4_dequant")
 
 
 def fp8_block_dequant_128x128(q, sf, out, stream=None) -> None:

@@ -248,6 +248,19 @@ int mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, void* out_bf16, int64
                                             static_cast<cudaStream_t>(stream)));
 }
 
+int nvfp4_dequant(const uint8_t* codes, const uint8_t* sf_e4m3, float global_scale, void* out_bf16, int64_t rows,
+                  int64_t cols, mx_stream_t stream) {
+    if (rows < 0 || cols <= 0) return MX_ERR_INVALID_ARG;
+    if (cols % 16) return MX_ERR_UNSUPPORTED;
+    if (rows == 0) return MX_OK;
+    if (!codes || !sf_e4m3 || !out_bf16) return MX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(codes) & 7u) != 0 || !aligned16(out_bf16)) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_nvfp4_dequant(codes, sf_e4m3, global_scale, static_cast<uint16_t*>(out_bf16), rows,
+                                            cols, d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_block_dequant_128x128(const uint8_t* q, const uint8_t* sf, void* out_bf16, int64_t rows, int64_t cols,
                               mx_stream_t stream) {
     if (rows < 0 || cols <= 0) return MX_ERR_INVALID_ARG;

@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kThreads) mxfp4_dequant_kernel(const uint32_t*
     }
 }
 
-// E4M3 ("fn") byte -> float32, exact. S.1111.111 is NaN.
+// E4M3 ("fn") byte -> float32, exact, for every byte but the NaN ones (S.1111.111), which
+// the callers handle first.
 __device__ __forceinline__ float e4m3_value(uint32_t b) {
     const uint32_t e = (b >> 3) & 15u, m = b & 7u;
     float mag;
@@ -103,6 +104,79 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
         mag = __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) 2^(e-7)
     }
     return (b & 0x80u) ? -mag : mag;
+}
+
+// NVFP4 -> BF16 ("Current Bug: vLLM produces empty/garbage output", "What we know":
+// NVFP4 weights dequantised to BF16; the per-tensor global scale of "Phase 2: CuTeDSL
+// Attention Kernel"): out = bf16(float32(LUT[code] * e4m3(scale) * global)). LUT[code] *
+// e4m3(scale) is exact in float32, so the multiply by the global scale is the one float32
+// rounding, then one BF16 rounding (both to nearest even). A NaN result is 0x7FC0 with the
+// XOR of the code's, the scale's and the global's sign bits.
+//
+// Both roundings are symmetric, so a value is its magnitude's BF16 with the XOR of the
+// three sign bits. A 16-element block has one scale, hence eight possible magnitudes,
+// rounded once per block with the same float32 operations in the same order. Each thread
+// takes one block (8 code bytes in, 32 bytes out): it splits the eight BF16 magnitudes
+// into a high-byte and a low-byte table (two registers each), selects four elements' bytes
+// at once by byte-permute on their 3-bit magnitude codes, puts each element's sign into its
+// high byte and interleaves the bytes into BF16.
+__device__ __forceinline__ uint32_t nv_sel(uint32_t x) {   // bytes' low 3 bits -> 4 selector nibbles
+    x &= 0x07070707u;
+    x = (x | (x >> 4)) & 0x00770077u;
+    return (x | (x >> 8)) & 0x00007777u;
+}
+
+// Eight elements (one code word, lower nibble first) from the block's byte tables.
+__device__ __forceinline__ uint4 nv_lookup8(uint32_t c, uint32_t hi0, uint32_t hi1, uint32_t lo0, uint32_t lo1,
+                                            uint32_t sneg) {
+    // even elements: low nibble of each code byte; odd: high nibble
+    const uint32_t se = nv_sel(c), so = nv_sel(c >> 4);
+    const uint32_t he = __byte_perm(hi0, hi1, se) ^ ((c << 4) & 0x80808080u) ^ sneg;
+    const uint32_t le = __byte_perm(lo0, lo1, se);
+    const uint32_t ho = __byte_perm(hi0, hi1, so) ^ (c & 0x80808080u) ^ sneg;
+    const uint32_t lo = __byte_perm(lo0, lo1, so);
+    // BF16 of elements 0, 2 (ea) / 4, 6 (eb) and 1, 3 (oa) / 5, 7 (ob)
+    const uint32_t ea = __byte_perm(le, he, 0x5140u), eb = __byte_perm(le, he, 0x7362u);
+    const uint32_t oa = __byte_perm(lo, ho, 0x5140u), ob = __byte_perm(lo, ho, 0x7362u);
+    return make_uint4(__byte_perm(ea, oa, 0x5410u), __byte_perm(ea, oa, 0x7632u), __byte_perm(eb, ob, 0x5410u),
+                      __byte_perm(eb, ob, 0x7632u));
+}
+
+__global__ void __launch_bounds__(kThreads) nvfp4_dequant_kernel(const uint2* __restrict__ codes8,
+                                                                 const uint8_t* __restrict__ sf, float g,
+                                                                 uint4* __restrict__ out, int64_t blocks) {
+    const uint32_t gneg = __float_as_uint(g) >> 31;
+    const float ga = fabsf(g);
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < blocks; b += stride) {
+        const uint2 c = __ldg(codes8 + b);           // elements 16b .. 16b + 15
+        const uint32_t sbyte = __ldg(sf + b);
+        const float sa = (sbyte & 0x7Fu) == 0x7Fu ? __uint_as_float(0x7FC00000u) : fabsf(e4m3_value(sbyte));
+        // t[k]: BF16 magnitudes of codes 2k (low half) and 2k + 1 (high half)
+        uint32_t t[4];
+        const float m[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+        if (isfinite(sa) && isfinite(ga)) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                t[k] = pack_bf16x2(__fmul_rn(__fmul_rn(m[2 * k], sa), ga), __fmul_rn(__fmul_rn(m[2 * k + 1], sa), ga));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t hh[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float v = __fmul_rn(__fmul_rn(m[2 * k + j], sa), ga);
+                    hh[j] = v != v ? 0x7FC0u : f32_to_bf16(v);
+                }
+                t[k] = hh[0] | (hh[1] << 16);
+            }
+        }
+        const uint32_t hi0 = __byte_perm(t[0], t[1], 0x7531u), hi1 = __byte_perm(t[2], t[3], 0x7531u);
+        const uint32_t lo0 = __byte_perm(t[0], t[1], 0x6420u), lo1 = __byte_perm(t[2], t[3], 0x6420u);
+        const uint32_t sneg = (((sbyte >> 7) ^ gneg) & 1u) ? 0x80808080u : 0u;
+        out[2 * b] = nv_lookup8(c.x, hi0, hi1, lo0, lo1, sneg);
+        out[2 * b + 1] = nv_lookup8(c.y, hi0, hi1, lo0, lo1, sneg);
+    }
 }
 
 // Two E4M3 bytes (first in the low half) -> two BF16 values times 2^(s-127), for s in
@@ -277,6 +351,15 @@ cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, uint16
     const int64_t warps = (units + kDeqUnitsPerWarp - 1) / kDeqUnitsPerWarp;
     mxfp4_dequant_kernel<<<grid_for(warps * 32, num_sms), kThreads, 0, s>>>(
         reinterpret_cast<const uint32_t*>(codes), sf, reinterpret_cast<uint4*>(out), units);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* sf, float global_scale, uint16_t* out,
+                                 int64_t rows, int64_t cols, int num_sms, cudaStream_t s) {
+    const int64_t blocks = rows * (cols / 16);
+    if (blocks == 0) return cudaSuccess;
+    nvfp4_dequant_kernel<<<grid_for(blocks, num_sms), kThreads, 0, s>>>(
+        reinterpret_cast<const uint2*>(codes), sf, global_scale, reinterpret_cast<uint4*>(out), blocks);
     return cudaGetLastError();
 }
 

@@ -85,6 +85,9 @@ cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const C
 cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s);
 cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, uint16_t* out, int64_t rows,
                                  int64_t cols, int num_sms, cudaStream_t s);
+// NVFP4 codes [rows, cols/2] + E4M3 scales [rows, cols/16] + float32 global -> BF16.
+cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* sf, float global_scale, uint16_t* out,
+                                 int64_t rows, int64_t cols, int num_sms, cudaStream_t s);
 cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* out, int64_t rows,
                                int64_t cols, int num_sms, cudaStream_t s);
 cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,

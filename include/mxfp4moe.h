@@ -78,6 +78,22 @@ int mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, void* out_bf16,
                   int64_t rows, int64_t cols, mx_stream_t stream);
 
 /*
+ * nvfp4_dequant -- NVFP4 -> BF16 ("Current Bug: vLLM produces empty/garbage output",
+ * "What we know": the NVFP4 weights dequantised to BF16; "Phase 2: CuTeDSL Attention
+ * Kernel": one float32 global scale per tensor, weight_scale_2).
+ *   out[r, c] = bf16( float32( E2M1(nibble(codes[r, c/2], c%2)) * e4m3(sf[r, c/16]) * global ) )
+ *   codes uint8 [rows, cols/2] (two E2M1 per byte, lower nibble first), sf uint8
+ *   [rows, cols/16] (E4M3 "fn" bytes), global_scale float32, out uint16 [rows, cols].
+ *   E2M1 * E4M3 is exact in float32; the product with the global scale is rounded once to
+ *   float32 and then to BF16, both to nearest even. A NaN result (NaN scale byte, NaN
+ *   global, or zero times an infinite global) is 0x7FC0 with the XOR of the three sign
+ *   bits. cols must be a positive multiple of 16 (MX_ERR_UNSUPPORTED otherwise); codes
+ *   8-byte and out 16-byte aligned (MX_ERR_MISALIGNED); rows == 0 launches nothing.
+ */
+int nvfp4_dequant(const uint8_t* codes, const uint8_t* sf_e4m3, float global_scale, void* out_bf16,
+                  int64_t rows, int64_t cols, mx_stream_t stream);
+
+/*
  * fp8_block_dequant_128x128 -- FP8 E4M3 x E8M0 128x128 block scale -> BF16 ([DQ] item 1).
  *   out[i, j] = bf16( e4m3(q[i, j]) * 2^(sf[i/128, j/128] - 127) )
  *   q uint8 [rows, cols] (E4M3 "fn" bytes), sf uint8 [ceil(rows/128), ceil(cols/128)],

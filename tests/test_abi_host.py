@@ -64,6 +64,12 @@ def test_dequant_validation(lib):
     assert lib.mxfp4_dequant(ODD, FAKE, FAKE, 4, 64, None) == MX_ERR_MISALIGNED
     assert lib.fp8_block_dequant_128x128(FAKE, FAKE, FAKE, 4, 40, None) == MX_ERR_UNSUPPORTED
     assert lib.fp8_block_dequant_128x128(FAKE, FAKE, ODD, 4, 64, None) == MX_ERR_MISALIGNED
+    assert lib.nvfp4_dequant(FAKE, FAKE, 1.0, FAKE, 4, 40, None) == MX_ERR_UNSUPPORTED     # cols % 16
+    assert lib.nvfp4_dequant(FAKE, FAKE, 1.0, FAKE, -1, 64, None) == MX_ERR_INVALID_ARG
+    assert lib.nvfp4_dequant(FAKE, FAKE, 1.0, FAKE, 0, 64, None) == MX_OK
+    assert lib.nvfp4_dequant(FAKE, None, 1.0, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
+    assert lib.nvfp4_dequant(FAKE + 4, FAKE, 1.0, FAKE, 4, 64, None) == MX_ERR_MISALIGNED  # codes 8-byte
+    assert lib.nvfp4_dequant(FAKE, FAKE, 1.0, ODD, 4, 64, None) == MX_ERR_MISALIGNED        # out 16-byte
     assert lib.act_quant_mxfp4(FAKE, FAKE, FAKE, 4, 40, None) == MX_ERR_UNSUPPORTED
     assert lib.act_quant_mxfp4(FAKE, None, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
 

@@ -1,7 +1,7 @@
 """GPU parity of the single kernels against the CPU oracle, through the C ABI.
 
-Bit-exact: MXFP4 -> BF16 dequant, FP8 128x128 dequant, the MX activation quantiser (codes
-and scales) and the routing permutation. The block-scaled GEMM is compared with the exact
+Bit-exact: MXFP4 -> BF16 dequant, NVFP4 -> BF16 dequant, FP8 128x128 dequant, the MX
+activation quantiser (codes and scales) and the routing permutation. The block-scaled GEMM is compared with the exact
 product (one BF16 rounding plus the float32 accumulation allowance), first on structured
 inputs that isolate the data path (all scales 1) and the scale-factor path (all codes
 equal), then on random inputs across tile, stage and ragged-edge boundaries.
@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 from gpu_util import assert_gemm_close, bf16_host, dev, native
-from workloads import f32_to_bf16_bits, make_dequant_inputs
+from workloads import f32_to_bf16_bits, make_dequant_inputs, make_nvfp4_scales
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +52,43 @@ def test_mxfp4_dequant_all_code_scale_pairs(mx):
     out = _empty((4096, 32), torch.bfloat16)
     mx.mxfp4_dequant(dev(codes), dev(sf), out)
     np.testing.assert_array_equal(bf16_host(out), oracle.mxfp4_dequant(codes, sf))
+
+
+@pytest.mark.parametrize("g", [1.0, 0.000372, -3.5, 2.0 ** -140, 1.0e37, float("inf")])
+def test_nvfp4_dequant_all_code_scale_pairs(mx, g):
+    """Every (code, E4M3 scale byte) pair, including the NaN bytes, at globals that give
+    float32 subnormals (2^-140), overflow (1e37), a negative sign and an infinity."""
+    import torch
+    nib = np.arange(16, dtype=np.uint8)
+    codes = np.tile((nib[0::2] | (nib[1::2] << 4)).astype(np.uint8), (256, 1))   # 256 rows x 16 cols
+    sf = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    out = _empty((256, 16), torch.bfloat16)
+    mx.nvfp4_dequant(dev(codes), dev(sf), g, out)
+    np.testing.assert_array_equal(bf16_host(out), oracle.nvfp4_dequant(codes, sf, g))
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (3, 48), (257, 1040), (2048, 7168)])
+def test_nvfp4_dequant_bit_exact(mx, rows, cols):
+    import torch
+    rng = np.random.default_rng(rows * 11 + cols)
+    codes = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    sf = rng.integers(0, 256, size=(rows, cols // 16), dtype=np.uint8)   # every E4M3 byte incl. NaN
+    out = _empty((rows, cols), torch.bfloat16)
+    mx.nvfp4_dequant(dev(codes), dev(sf), 0.0123, out)
+    np.testing.assert_array_equal(bf16_host(out), oracle.nvfp4_dequant(codes, sf, 0.0123))
+
+
+def test_nvfp4_dequant_full_size_sampled(mx):
+    """The 48 experts' w13 codes with NVFP4 scales, as the bench times them; sampled rows."""
+    import torch
+    w13, _, _, _, _, _ = make_dequant_inputs()
+    n13, _, g = make_nvfp4_scales()
+    R, half = w13.shape
+    out = _empty((R, 2 * half), torch.bfloat16)
+    mx.nvfp4_dequant(dev(w13), dev(n13), g, out)
+    rows = np.unique(np.concatenate([np.random.default_rng(98).integers(0, R, 48), [0, R - 1]]))
+    got = bf16_host(out[torch.from_numpy(rows).cuda()])
+    np.testing.assert_array_equal(got, oracle.nvfp4_dequant(w13[rows], n13[rows], g))
 
 
 @pytest.mark.parametrize("rows,cols", [(1, 16), (130, 272), (300, 1040)])

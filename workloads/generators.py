@@ -136,6 +136,17 @@ def make_config_inputs(name: str) -> MoEInputs:
                            c.pop("seed"), **c)
 
 
+def make_nvfp4_scales(seed=5, experts=48, I=3072, H=7168, lo=0x20, hi=0x5E, global_scale=0.000372):
+    """NVFP4 scales for the dequant sweep's expert weights (the codes of make_dequant_inputs):
+    E4M3 bytes, one per 16 columns, uniform over the finite positive codes [lo, hi]
+    (2^-4 .. 240), and one float32 global scale. Returns (w13 scales [E*2I, H/16],
+    w2 scales [E*H, I/16], global)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s13 = rng.integers(lo, hi + 1, size=(experts * 2 * I, H // 16), dtype=np.uint8)
+    s2 = rng.integers(lo, hi + 1, size=(experts * H, I // 16), dtype=np.uint8)
+    return s13, s2, float(np.float32(global_scale))
+
+
 def make_dequant_inputs(seed=4, experts=48, I=3072, H=7168, fp8_rows=7168, fp8_cols=7168,
                         sf_lo=118, sf_hi=124, fp8_sf_lo=120, fp8_sf_hi=130):
     """Weight dequant sweep: MXFP4 expert weights flattened to rows, plus one FP8 matrix.
