@@ -25,6 +25,8 @@ from .mxfp4_oracle import (  # noqa: F401
     swiglu_bf16,
     moe_flops_per_pair,
     nvfp4_dequant,
+    nvfp4_gemm_bf16,
+    nvfp4_gemm_f64,
     nvfp4_values,
     unpack_nibbles,
 )

@@ -76,7 +76,7 @@ __all__ = [
     "e2m1_decode", "e8m0_decode", "e4m3fn_decode", "bf16_bits_from_f64", "bf16_bits_to_f64",
     "unpack_nibbles", "mxfp4_values", "mxfp4_dequant", "fp8_block_dequant_128x128",
     "act_quant_mxfp4", "mxfp4_gemm_bf16", "mxfp4_gemm_blockint", "moe_route", "moe_forward",
-    "nvfp4_values", "nvfp4_dequant",
+    "nvfp4_values", "nvfp4_dequant", "nvfp4_gemm_f64", "nvfp4_gemm_bf16",
     "moe_flops_per_pair", "moe_l1_exact", "swiglu_bf16", "moe_l2_bf16", "moe_combine",
 ]
 
@@ -322,6 +322,24 @@ def mxfp4_gemm_blockint(a_codes, a_sf, b_codes, b_sf) -> np.ndarray:
     terms = np.ldexp(blk.astype(np.float64), expo)
     terms = np.where((sa[:, None, :] == 255) | (sb[None, :, :] == 255), np.nan, terms)
     return terms.sum(axis=-1)
+
+
+def nvfp4_gemm_f64(a_codes, a_sf, a_global, b_codes, b_sf, b_global) -> np.ndarray:
+    """A . B^T for NVFP4 A [M, K] and B [N, K] (R11) in float64:
+    a_global * b_global * sum_k (LUT * e4m3)_a (LUT * e4m3)_b. The sum of the scaled E2M1
+    products is exact in float64 while the terms span less than ~2^40 (every input here);
+    its product with the two globals is then rounded once to float64."""
+    A = nvfp4_values(a_codes, a_sf, 1.0)
+    B = nvfp4_values(b_codes, b_sf, 1.0)
+    with np.errstate(invalid="ignore", over="ignore"):
+        return (A @ B.T) * (float(np.float32(a_global)) * float(np.float32(b_global)))
+
+
+def nvfp4_gemm_bf16(a_codes, a_sf, a_global, b_codes, b_sf, b_global) -> np.ndarray:
+    """y = bf16(A . B^T) for NVFP4 operands (R11): nvfp4_gemm_f64 rounded once to BF16
+    (the NVFP4 GEMM the pages plan for their attention projections, "Phase 2: CuTeDSL
+    Attention Kernel", with one global scale per operand)."""
+    return bf16_bits_from_f64(nvfp4_gemm_f64(a_codes, a_sf, a_global, b_codes, b_sf, b_global))
 
 
 def moe_flops_per_pair(H: int, I: int) -> int:

@@ -90,3 +90,48 @@ def test_nan_sign_rule():
                           (0x38, -np.inf, False)):
         got = oracle.nvfp4_dequant(codes, np.array([[sbyte]], np.uint8), g)
         assert got[0, 0] == (0xFFC0 if neg else 0x7FC0), (hex(sbyte), g, hex(int(got[0, 0])))
+
+
+def _nv_exact(codes, sf, r, c):
+    """Exact rational value of NVFP4 element (r, c) with global 1, from the bit fields."""
+    from fractions import Fraction
+    byte = int(codes[r, c // 2])
+    n = (byte >> 4) if c % 2 else (byte & 15)
+    s, e, m = n >> 3, (n >> 1) & 3, n & 1
+    mag = Fraction(m, 2) if e == 0 else (1 + Fraction(m, 2)) * Fraction(2) ** (e - 1)
+    sb = int(sf[r, c // 16])
+    se, ee, me = sb >> 7, (sb >> 3) & 15, sb & 7
+    smag = Fraction(me, 8) * Fraction(2) ** -6 if ee == 0 else (1 + Fraction(me, 8)) * Fraction(2) ** (ee - 7)
+    return (-1) ** (s ^ se) * mag * smag
+
+
+def test_gemm_brute_force_exact_rationals():
+    from fractions import Fraction
+    rng = np.random.default_rng(21)
+    M, N, K = 3, 4, 48
+    a = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x08, 0x7E, size=(M, K // 16), dtype=np.uint8)    # finite, positive
+    sb = rng.integers(0x88, 0xFE, size=(N, K // 16), dtype=np.uint8)    # finite, negative
+    ga, gb = np.float32(0.375), np.float32(-1.5e-3)
+    got = oracle.nvfp4_gemm_f64(a, sa, ga, b, sb, gb)
+    for i in range(M):
+        for j in range(N):
+            exact = sum(_nv_exact(a, sa, i, k) * _nv_exact(b, sb, j, k) for k in range(K))
+            exact *= Fraction(float(ga)) * Fraction(float(gb))
+            assert got[i, j] == float(exact)            # the exact value, rounded once
+
+
+def test_gemm_power_of_two_scales_equal_mxfp4():
+    """With E4M3 scales 2^(e-7) (repeated over both 16-column halves of each 32-block) and
+    globals 1, the NVFP4 GEMM is the MXFP4 GEMM with E8M0 bytes 120 + e."""
+    rng = np.random.default_rng(23)
+    M, N, K = 8, 16, 256
+    a = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    ea = rng.integers(1, 15, size=(M, K // 32))
+    eb = rng.integers(1, 15, size=(N, K // 32))
+    got = oracle.nvfp4_gemm_bf16(a, np.repeat((ea << 3).astype(np.uint8), 2, axis=1), 1.0,
+                                 b, np.repeat((eb << 3).astype(np.uint8), 2, axis=1), 1.0)
+    ref = oracle.mxfp4_gemm_bf16(a, (120 + ea).astype(np.uint8), b, (120 + eb).astype(np.uint8))
+    np.testing.assert_array_equal(got, ref)
