@@ -21,5 +21,8 @@ from ._native import (  # noqa: F401
     mxfp4_scales_to_tiled,
     mxfp4_tiled_scales_bytes,
     nvfp4_dequant,
+    nvfp4_gemm_bf16,
+    nvfp4_scales_to_tiled,
+    nvfp4_tiled_scales_bytes,
     status_string,
 )

@@ -25,6 +25,10 @@ _SIGNATURES = {
     "mxfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "fp8_block_dequant_128x128": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "nvfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "nvfp4_tiled_scales_bytes": (ctypes.c_size_t, [_c_i64, _c_i64]),
+    "nvfp4_scales_to_tiled": (ctypes.c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "nvfp4_gemm_bf16": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_ptr, ctypes.c_float, _c_ptr,
+                                       _c_i64, _c_i64, _c_i64, _c_ptr]),
     "act_quant_mxfp4": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "mxfp4_tiled_scales_bytes": (ctypes.c_size_t, [_c_i64, _c_i64]),
     "mxfp4_scales_to_tiled": (ctypes.c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
@@ -137,6 +141,40 @@ def nvfp4_dequant(codes, sf, global_scale, out, stream=None) -> None:
     _need(out, out.dtype, (R, C), "out")
     _check(lib().nvfp4_dequant(_ptr(codes), _ptr(sf), float(global_scale), _ptr(out), R, C, _stream(stream)),
            "nvfp4_dequant")
+
+
+def nvfp4_tiled_scales_bytes(rows: int, cols: int) -> int:
+    return int(lib().nvfp4_tiled_scales_bytes(rows, cols))
+
+
+def nvfp4_scales_to_tiled(sf, out, stream=None) -> None:
+    """NVFP4 scale tensor u8 [rows, cols/16] -> tile layout (u8, nvfp4_tiled_scales_bytes bytes)."""
+    import torch
+    rows, kb = sf.shape
+    _need(sf, torch.uint8, (rows, kb), "sf")
+    if out.dtype != torch.uint8 or out.numel() < nvfp4_tiled_scales_bytes(rows, 16 * kb) or not out.is_cuda:
+        raise ValueError("out: uint8 CUDA buffer of nvfp4_tiled_scales_bytes bytes")
+    _check(lib().nvfp4_scales_to_tiled(_ptr(sf), _ptr(out), rows, 16 * kb, _stream(stream)),
+           "nvfp4_scales_to_tiled")
+
+
+def nvfp4_gemm_bf16(a, sa, a_global, b, sb_tiled, b_global, d, stream=None) -> None:
+    """d = bf16(a_global * b_global * A . B^T) for NVFP4 A (a u8 [M, K/2], sa u8 [M, K/16]) and
+    B (b u8 [N, K/2], sb_tiled = nvfp4_scales_to_tiled of B's [N, K/16] scales)."""
+    import torch
+    M, half = a.shape
+    N = b.shape[0]
+    K = 2 * half
+    _need(a, torch.uint8, (M, half), "a")
+    _need(sa, torch.uint8, (M, K // 16), "sa")
+    _need(b, torch.uint8, (N, half), "b")
+    if sb_tiled.dtype != torch.uint8 or sb_tiled.numel() < nvfp4_tiled_scales_bytes(N, K) or not sb_tiled.is_cuda:
+        raise ValueError("sb_tiled: uint8 CUDA buffer of nvfp4_tiled_scales_bytes(N, K) bytes")
+    if not _bf16_like(d):
+        raise ValueError("d must be bfloat16 (or its 16-bit bit pattern)")
+    _need(d, d.dtype, (M, N), "d")
+    _check(lib().nvfp4_gemm_bf16(_ptr(a), _ptr(sa), float(a_global), _ptr(b), _ptr(sb_tiled), float(b_global),
+                                 _ptr(d), M, N, K, _stream(stream)), "nvfp4_gemm_bf16")
 
 
 def fp8_block_dequant_128x128(q, sf, out, stream=None) -> None:

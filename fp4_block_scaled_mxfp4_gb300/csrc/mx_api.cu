@@ -301,6 +301,50 @@ int mxfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t
     return cuda_status(launch_sf_tile(sf, out, rows, cols / 32, static_cast<cudaStream_t>(stream)));
 }
 
+size_t nvfp4_tiled_scales_bytes(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols <= 0 || cols % 64) return 0;
+    return tiled_bytes(rows, cols / 16);
+}
+
+int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t cols, mx_stream_t stream) {
+    if (rows < 0 || cols <= 0) return MX_ERR_INVALID_ARG;
+    if (cols % 64) return MX_ERR_UNSUPPORTED;
+    if (rows == 0) return MX_OK;
+    if (!sf || !out) return MX_ERR_INVALID_ARG;
+    if (!aligned16(sf) || !aligned16(out)) return MX_ERR_MISALIGNED;
+    if ((cols / 64 + 31) / 32 > 65535) return MX_ERR_UNSUPPORTED;
+    return cuda_status(launch_sf_tile(sf, out, rows, cols / 16, static_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b, const uint8_t* sb_tiled,
+                    float b_global, void* d_bf16, int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (K % 256 || N % 16) return MX_ERR_UNSUPPORTED;
+    if (M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 24)) return MX_ERR_UNSUPPORTED;
+    if (M == 0) return MX_OK;
+    if (!a || !sa || !b || !sb_tiled || !d_bf16) return MX_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(sa) || !aligned16(sb_tiled) || !aligned16(d_bf16))
+        return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    CUtensorMap ta, tb, ty;
+    if (make_tmap(&ta, a, K / 2, M, 128) || make_tmap(&tb, b, K / 2, N, 256) || make_tmap_out(&ty, d_bf16, N, M))
+        return MX_ERR_CUDA;
+    GemmArgs g = base_args(sa, sb_tiled, K, M, N, d->status);
+    g.ld_sf = K / 16;                  // one E4M3 scale per 16 elements
+    g.kw = K / 64;                     // scale words (4 scales) per row
+    g.alpha = a_global * b_global;
+    g.num_mtiles_host = (int32_t)((M + kBM - 1) / kBM);
+    g.m_total = M;
+    g.n_tiles = (int32_t)((N + kBN - 1) / kBN);
+    g.b_rows_per_expert = N;
+    g.n_valid = N;
+    g.y = static_cast<uint16_t*>(d_bf16);
+    g.ld_y = N;
+    return cuda_status(launch_gemm_nvfp4(ta, tb, ty, g, grid_for((int64_t)g.num_mtiles_host * g.n_tiles, d->num_sms),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 // N tile width for a GEMM whose 256-wide tiling has units256 work units: 128 when those
 // would leave SMs idle.
 int tile_cols(int64_t units256, int num_sms) { return units256 < num_sms ? 128 : kBN; }

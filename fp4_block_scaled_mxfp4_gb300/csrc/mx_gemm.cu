@@ -78,19 +78,26 @@ constexpr int kMaxStages = 5;
 // (64 + 64) where a grid of 256-wide tiles would leave SMs idle (the shared expert at a
 // few hundred tokens). The narrower tile halves each CTA's work per stage, doubles the
 // CTAs, and fits a fifth stage.
-template <int kN>
+//
+// kNv: NVFP4 operands (E4M3 scales per 16 elements of K, idesc scale format E4M3): four
+// scale words per row and stage instead of two, so two A images, twice B's blocks and
+// copies, twice the TMEM columns per slot, and three stages.
+template <int kN, bool kNv = false>
 struct Cfg {
-    static constexpr int kStages = kN == 256 ? 4 : 5;
+    static constexpr int kStages = kNv ? 3 : (kN == 256 ? 4 : 5);
     static constexpr int kBBytes = kN * kBK / 2;                    // 32 or 16 KB
-    static constexpr int kSfaBytes = 4096;
-    static constexpr int kSfbBytes = (kN / 128) * 2 * 512;          // per 128 rows: 2 K-words x 512 B
-    static constexpr uint32_t kIdesc = idesc_mxf4(kBM, kN);
+    static constexpr int kWords = kNv ? 4 : 2;                      // scale words per row and stage
+    static constexpr int kSfaBytes = (kWords / 2) * 4096;           // wide images of two words each
+    static constexpr int kSfbBytes = (kN / 128) * kWords * 512;     // per 128 rows: kWords x 512 B
+    static constexpr int kSfCols = kNv ? 48 : kSfColsPerStage;      // A: 4 per word; B: 8 per word
+    static constexpr uint32_t kIdesc = kNv ? (idesc_mxf4(kBM, kN) & ~(1u << 23)) : idesc_mxf4(kBM, kN);
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static constexpr uint32_t kDescStageStep = kStageBytes >> 4;
     static constexpr int kStagingOff = kStages * kStageBytes;
     static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(kStages <= kMaxStages, "barrier arrays");
-    static_assert(kSfTmemBase + kStages * kSfColsPerStage <= kTmemCols, "scale slots must fit in TMEM");
+    static_assert(kSfTmemBase + kStages * kSfCols <= kTmemCols, "scale slots must fit in TMEM");
+    static_assert(!kNv || kN == 256, "NVFP4 runs 256-column tiles");
 };
 
 // Descriptor of a wide scale image: core matrices of 8 rows x 16 bytes, the two halves of a
@@ -122,9 +129,9 @@ struct Ctl {
     int abort_flag;
 };
 
-template <int kN>
+template <int kN, bool kNv = false>
 constexpr size_t smem_bytes() {
-    return (size_t)Cfg<kN>::kStagingOff + 8 * kStagingBytes + sizeof(Ctl) + 1024;
+    return (size_t)Cfg<kN, kNv>::kStagingOff + 8 * kStagingBytes + sizeof(Ctl) + 1024;
 }
 
 struct Tile {
@@ -173,11 +180,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
-template <bool kL1, bool kBTiled, int kN>
+template <bool kL1, bool kBTiled, int kN, bool kNv = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
-    using C = Cfg<kN>;
+    static_assert(!kNv || (!kL1 && kBTiled), "NVFP4: the one-group BF16 GEMM with tile-layout B scales");
+    using C = Cfg<kN, kNv>;
     constexpr int kBBytes = C::kBBytes;
     constexpr uint32_t kIdesc = C::kIdesc;
     constexpr int kStages = C::kStages;
@@ -285,10 +293,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint64_t adesc = adesc0 + (uint64_t)(s * kDescStageStep);
                     const uint64_t bdesc = bdesc0 + (uint64_t)(s * kDescStageStep);
-                    const uint32_t sfa = sf0 + s * kSfColsPerStage;
-                    const uint32_t sfb = sfa + 8;
+                    const uint32_t sfa = sf0 + s * C::kSfCols;
+                    const uint32_t sfb = sfa + (kNv ? 16 : 8);
                     const uint32_t acc0 = kt != 0;
                     // 64 E2M1 elements (32 bytes) of K per MMA, inside the 128-byte swizzle atom
+                    if constexpr (kNv) {
+                        // one scale word per MMA: A's at +4k, B's at +8k
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma_nvf4(tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, sfa + 4 * k, sfb + 8 * k,
+                                        k == 0 ? acc0 : 1u);
+                        tc_commit(smem_u32(&ctl->empty[s]));
+                        continue;
+                    }
                     tc_mma_mxf4(tmem, adesc, bdesc, idesc_with_sf_ids(kIdesc, 0, 0), sfa, sfb, acc0);
                     tc_mma_mxf4(tmem, adesc + 2, bdesc + 2, idesc_with_sf_ids(kIdesc, 2, 2), sfa, sfb, 1);
                     if (!(args.k_tail_half && kt == k_tiles - 1)) {
@@ -324,11 +341,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 const bool half = args.k_tail_half && (kt == k_tiles - 1);
                 const uint32_t st = sbase + s * kStageBytes;
-                const int64_t kcol = (int64_t)kt * 8;   // first 32-element block of this stage
+                const int64_t kcol = (int64_t)kt * 4 * C::kWords;   // first scale byte of this stage
                 if (kBTiled && kN == 256 && lane == 0) {
                     // B scales: K-words 2kt, 2kt+1 of each 128-row group (one at the K tail);
                     // each 128-row half of the tile is one whole group of the tile layout
-                    const uint32_t sf_bytes = half ? 512u : 1024u;
+                    const uint32_t sf_bytes = half ? 512u : (uint32_t)(C::kWords * 512);
                     const uint32_t bar = smem_u32(&ctl->sf_full[s]);
                     int64_t grp[2];
                     uint32_t tx = 0;
@@ -339,8 +356,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive_expect_tx(bar, tx);
                     for (int h = 0; h < 2; ++h)
                         if (grp[h] < args.b_groups)
-                            bulk_load(st + kABytes + kBBytes + kSfaBytes + h * 1024,
-                                      args.sfb + (grp[h] * args.kw + 2 * kt) * 512, sf_bytes, bar);
+                            bulk_load(st + kABytes + kBBytes + kSfaBytes + h * (C::kWords * 512),
+                                      args.sfb + (grp[h] * args.kw + C::kWords * kt) * 512, sf_bytes, bar);
                 }
                 if (kBTiled && kN == 128) {
                     // B scales in tile layout for a 128-row tile of two 64-row pieces (L1) that
@@ -372,9 +389,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const bool valid = grow < args.a_rows;
                         const uint8_t* src = args.sfa + (valid ? grow * args.ld_sf + kcol : 0);
 #pragma unroll
-                        for (int wd = 0; wd < 2; ++wd) {
+                        for (int wd = 0; wd < C::kWords; ++wd) {
                             const bool ok = valid && (wd == 0 || !half);
-                            const uint32_t dst = sfa_s + wide_off(32 * j + lane, wd);
+                            const uint32_t dst = sfa_s + 4096 * (wd >> 1) + wide_off(32 * j + lane, wd & 1);
                             cp_async_4(dst, ok ? src + 4 * wd : args.sfa, ok ? 4u : 0u);
                         }
                     }
@@ -420,16 +437,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // reads them through the async proxy
                     fence_proxy_async_smem();
                     tc_fence_after();
-                    const int nwords = (args.k_tail_half && kt == k_tiles - 1) ? 1 : 2;
+                    const int nwords = (args.k_tail_half && kt == k_tiles - 1) ? 1 : C::kWords;
                     const uint32_t sfa_s = sbase + s * kStageBytes + kABytes + kBBytes;
                     const uint32_t sfb_s = sfa_s + kSfaBytes;
-                    const uint32_t sfa_t = tmem + kSfTmemBase + s * kSfColsPerStage;
-                    const uint32_t sfb_t = sfa_t + 8;
-                    tc_cp_128x256b(sfa_t, desc_sf_wide(sfa_s));                                // A, both K-words
+                    const uint32_t sfa_t = tmem + kSfTmemBase + s * C::kSfCols;
+                    const uint32_t sfb_t = sfa_t + (kNv ? 16 : 8);
+#pragma unroll
+                    for (int i = 0; i < C::kWords / 2; ++i)                                   // A, two K-words each
+                        tc_cp_128x256b(sfa_t + 8 * i, desc_sf_wide(sfa_s + 4096 * i));
                     for (int wd = 0; wd < nwords; ++wd) {
                         tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 512));          // B rows 0-127
-                        if (kN == 256)
-                            tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + 1024 + wd * 512));  // 128-255
+                        if (kN == 256)                                                          // 128-255
+                            tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + C::kWords * 512 + wd * 512));
                     }
                     tc_commit(smem_u32(&ctl->ready[s]));   // arrives once the copies are in TMEM
                 }
@@ -449,6 +468,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
         uint8_t* staging = smem + kStagingOff + (warp - 4) * kStagingBytes;
         const uint32_t staging_s = smem_u32(staging);
+        // L2's output value of an accumulator word (NVFP4: times the two global scales)
+        auto out_value = [&](uint32_t acc) {
+            return kNv ? __fmul_rn(__uint_as_float(acc), args.alpha) : __uint_as_float(acc);
+        };
         uint32_t tc = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x, ++tc) {
             const Tile t = get_tile(args, w / args.n_tiles);
@@ -485,7 +508,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t p[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        p[j] = pack_bf16x2(__uint_as_float(v[i][2 * j]), __uint_as_float(v[i][2 * j + 1]));
+                        p[j] = pack_bf16x2(out_value(v[i][2 * j]), out_value(v[i][2 * j + 1]));
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {       // 16 columns (32 bytes) per row and store
                         if (col + 16 * c >= args.n_valid) break;
@@ -565,7 +588,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t p[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        p[j] = pack_bf16x2(__uint_as_float(v[i][2 * j]), __uint_as_float(v[i][2 * j + 1]));
+                        p[j] = pack_bf16x2(out_value(v[i][2 * j]), out_value(v[i][2 * j + 1]));
                     uint16_t* dst = args.y + grow * args.ld_y + col;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -589,7 +612,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <bool kL1, bool kBTiled, int kN>
+template <bool kL1, bool kBTiled, int kN, bool kNv = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a, int grid,
                    cudaStream_t s) {
     static int configured_mask = 0;   // one bit per device
@@ -597,13 +620,13 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
-        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1, kBTiled, kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_bytes<kN>());
+        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1, kBTiled, kN, kNv>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<kN, kNv>());
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
-    return launch_pdl(mxf4_gemm_kernel<kL1, kBTiled, kN>, dim3(grid), dim3(kGemmThreads), smem_bytes<kN>(), s, ta, tb, ty,
-                      a);
+    return launch_pdl(mxf4_gemm_kernel<kL1, kBTiled, kN, kNv>, dim3(grid), dim3(kGemmThreads), smem_bytes<kN, kNv>(), s,
+                      ta, tb, ty, a);
 }
 
 template <bool kL1>
@@ -616,7 +639,10 @@ cudaError_t launch_any(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return smem_bytes<256>() > smem_bytes<128>() ? smem_bytes<256>() : smem_bytes<128>(); }
+size_t gemm_smem_bytes() {
+    const size_t a = smem_bytes<256>(), b = smem_bytes<128>(), c = smem_bytes<256, true>();
+    return a > b ? (a > c ? a : c) : (b > c ? b : c);
+}
 
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                            int grid, bool b_tiled, int n_cols, cudaStream_t s) {
@@ -626,6 +652,11 @@ cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const C
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                            int grid, bool b_tiled, int n_cols, cudaStream_t s) {
     return launch_any<false>(ta, tb, ty, a, grid, b_tiled, n_cols, s);
+}
+
+cudaError_t launch_gemm_nvfp4(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                              int grid, cudaStream_t s) {
+    return launch<false, true, 256, true>(ta, tb, ty, a, grid, s);
 }
 
 }  // namespace mx

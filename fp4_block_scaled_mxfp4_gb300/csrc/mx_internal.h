@@ -46,7 +46,7 @@ struct GemmArgs {
     int64_t a_rows;              // rows of A (bound for scale loads; TMA zero-fills beyond)
     int64_t b_rows;              // rows of the stacked B tensor
     int64_t b_groups;            // 128-row groups of B's tiled scales
-    int64_t kw;                  // K/128: scale words per row
+    int64_t kw;                  // scale words (4 bytes) per row: K/128 (MXFP4), K/64 (NVFP4)
     int32_t k_tiles;             // ceil(K / 256)
     int32_t k_tail_half;         // 1 when the last stage holds only 128 of K
     // M tiles: from the routing tables (device) or uniform over m_total rows.
@@ -67,6 +67,7 @@ struct GemmArgs {
     uint16_t* y;                 // L2: BF16 output [rows, ld_y]
     int64_t ld_y;
     uint32_t* status;            // device status word
+    float alpha;                 // NVFP4: the product of the two global scales
 };
 
 size_t gemm_smem_bytes();
@@ -79,6 +80,12 @@ cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const C
                            int grid, bool b_tiled, int n_cols, cudaStream_t s);
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                            int grid, bool b_tiled, int n_cols, cudaStream_t s);
+
+// NVFP4 one-group GEMM, BF16 out (times a.alpha): A codes with row-major E4M3 scales per 16
+// (a.sfa, ld_sf = K/16), B codes with E4M3 scales in the tile layout (a.sfb, kw = K/64);
+// tb in boxes of 256 rows; K % 256 == 0.
+cudaError_t launch_gemm_nvfp4(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                              int grid, cudaStream_t s);
 
 // ---- element-wise kernels ----
 // Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][512 B] (kb % 4 == 0).

@@ -94,6 +94,30 @@ int nvfp4_dequant(const uint8_t* codes, const uint8_t* sf_e4m3, float global_sca
                   int64_t rows, int64_t cols, mx_stream_t stream);
 
 /*
+ * nvfp4_tiled_scales_bytes / nvfp4_scales_to_tiled -- the tile layout above for an NVFP4
+ * scale tensor sf uint8 [rows, cols/16] (E4M3 bytes, one per 16 columns): its 4-byte
+ * words (four scales, 64 columns) take the place of the MXFP4 K-words. cols % 64 == 0.
+ */
+size_t nvfp4_tiled_scales_bytes(int64_t rows, int64_t cols);
+int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t cols,
+                          mx_stream_t stream);
+
+/*
+ * nvfp4_gemm_bf16 -- D = bf16(a_global * b_global * A . B^T) with NVFP4 operands on the
+ * tcgen05 tensor cores (kind::mxf4nvf4, scale_vec::4X): the standard NVFP4 GEMM the pages
+ * plan for their attention projections ("Current Bug: vLLM produces empty/garbage
+ * output", "Phase 2: CuTeDSL Attention Kernel", one global scale per operand).
+ *   A codes uint8 [M, K/2] + sa uint8 [M, K/16] (E4M3, row-major); B codes uint8 [N, K/2]
+ *   + its E4M3 scales in the tile layout (nvfp4_scales_to_tiled of [N, K/16]);
+ *   D uint16 [M, N]. The block-scaled products accumulate in float32; the sum is
+ *   multiplied by the float32 product of the globals and rounded once to BF16.
+ *   K must be a positive multiple of 256, N a positive multiple of 16; M >= 0.
+ */
+int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b,
+                    const uint8_t* sb_tiled, float b_global, void* d_bf16, int64_t M, int64_t N,
+                    int64_t K, mx_stream_t stream);
+
+/*
  * fp8_block_dequant_128x128 -- FP8 E4M3 x E8M0 128x128 block scale -> BF16 ([DQ] item 1).
  *   out[i, j] = bf16( e4m3(q[i, j]) * 2^(sf[i/128, j/128] - 127) )
  *   q uint8 [rows, cols] (E4M3 "fn" bytes), sf uint8 [ceil(rows/128), ceil(cols/128)],

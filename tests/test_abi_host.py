@@ -89,6 +89,17 @@ def test_gemm_validation(lib):
     assert lib.mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 256, 256, None) == MX_OK
     assert lib.mxfp4_gemm_bf16(FAKE, FAKE, None, FAKE, FAKE, 4, 256, 256, None) == MX_ERR_INVALID_ARG
     assert lib.mxfp4_gemm_bf16(FAKE, ODD, FAKE, FAKE, FAKE, 4, 256, 256, None) == MX_ERR_MISALIGNED
+    # NVFP4: every call below is rejected (or has M == 0) before anything launches
+    assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, 4, 256, 128, None) == MX_ERR_UNSUPPORTED  # K % 256
+    assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, 4, 250, 256, None) == MX_ERR_UNSUPPORTED
+    assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, 0, 256, 256, None) == MX_OK
+    assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, None, FAKE, 1.0, FAKE, 4, 256, 256, None) == MX_ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, ODD, 1.0, FAKE, 4, 256, 256, None) == MX_ERR_MISALIGNED
+    assert lib.nvfp4_tiled_scales_bytes(300, 7168) == 3 * 112 * 512
+    assert lib.nvfp4_tiled_scales_bytes(300, 7200) == 0
+    assert lib.nvfp4_scales_to_tiled(FAKE, FAKE, 4, 96, None) == MX_ERR_UNSUPPORTED
+    assert lib.nvfp4_scales_to_tiled(ODD, FAKE, 4, 128, None) == MX_ERR_MISALIGNED
+    assert lib.nvfp4_scales_to_tiled(FAKE, FAKE, 0, 128, None) == MX_OK
 
 
 def _fwd(lib, ids=FAKE, w=FAKE, T=16, H=256, I=128, E=4, K=2, ws=FAKE, ws_bytes=None, x=FAKE):

@@ -242,6 +242,55 @@ def test_gemm_random(mx, M, N, K):
     _gemm_case(mx, a, sa, b, sb, f"random {M}x{N}x{K}")
 
 
+def _nv_tiled(mx, sf):
+    import torch
+    rows, kb = sf.shape
+    out = torch.empty(mx.nvfp4_tiled_scales_bytes(rows, 16 * kb), dtype=torch.uint8, device="cuda")
+    mx.nvfp4_scales_to_tiled(dev(sf), out)
+    return out
+
+
+def test_nvfp4_scales_to_tiled_bit_exact(mx):
+    rng = np.random.default_rng(31)
+    sf = rng.integers(0, 256, size=(300, 7168 // 16), dtype=np.uint8)
+    np.testing.assert_array_equal(_nv_tiled(mx, sf).cpu().numpy(), _tiled_layout_reference(sf))
+
+
+# NVFP4 scales are read as unsigned E4M3 by the tensor core: the inputs keep the sign bit clear.
+@pytest.mark.parametrize("M,N,K,ga,gb", [(128, 256, 256, 1.0, 1.0), (77, 272, 512, 0.0123, 2.5),
+                                         (300, 512, 1024, 3.0e-3, -0.7), (1000, 1024, 7168, 0.05, 0.02)])
+def test_nvfp4_gemm_random(mx, M, N, K, ga, gb):
+    import torch
+    rng = np.random.default_rng(M + N + K)
+    a = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x20, 0x50, size=(M, K // 16), dtype=np.uint8)
+    sb = rng.integers(0x28, 0x48, size=(N, K // 16), dtype=np.uint8)
+    d = _empty((M, N), torch.bfloat16)
+    mx.nvfp4_gemm_bf16(dev(a), dev(sa), ga, dev(b), _nv_tiled(mx, sb), gb, d)
+    exact = oracle.nvfp4_gemm_f64(a, sa, ga, b, sb, gb)
+    absdot = np.abs(oracle.nvfp4_values(a, sa, 1.0)) @ np.abs(oracle.nvfp4_values(b, sb, 1.0)).T
+    absdot *= abs(float(np.float32(ga)) * float(np.float32(gb)))
+    assert_gemm_close(bf16_host(d), exact, absdot, f"nvfp4 {M}x{N}x{K}")
+
+
+def test_nvfp4_gemm_scale_words_one_hot(mx):
+    """All codes 1.0 and all scales 1.0 except one E4M3 scale per row of A: D[m, n] picks
+    out which 16-column block (which scale word and which of its four bytes) each MMA
+    reads, for every one of the stage's four words."""
+    import torch
+    M, N, K = 128, 256, 512
+    a = np.full((M, K // 2), 0x22, np.uint8)
+    b = np.full((N, K // 2), 0x22, np.uint8)
+    sa = np.full((M, K // 16), 0x38, np.uint8)
+    sb = np.full((N, K // 16), 0x38, np.uint8)
+    sa[np.arange(M), np.arange(M) % (K // 16)] = 0x40                   # scale 2.0 at block m mod 32
+    sb[np.arange(N), (3 * np.arange(N)) % (K // 16)] = 0x30             # scale 0.5 at block 3n mod 32
+    d = _empty((M, N), torch.bfloat16)
+    mx.nvfp4_gemm_bf16(dev(a), dev(sa), 1.0, dev(b), _nv_tiled(mx, sb), 1.0, d)
+    np.testing.assert_array_equal(bf16_host(d), oracle.nvfp4_gemm_bf16(a, sa, 1.0, b, sb, 1.0))
+
+
 # ----------------------------------------------------------------------------- routing
 
 @pytest.mark.parametrize("T,K,E", [(1, 1, 1), (100, 4, 5), (3000, 8, 48), (8192, 8, 48), (513, 6, 300)])
