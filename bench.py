@@ -37,7 +37,8 @@ import numpy as np  # noqa: E402
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import CONFIGS, make_config_inputs, make_dequant_inputs, make_moe_inputs, make_nvfp4_scales  # noqa: E402
+from workloads import (CONFIGS, make_config_inputs, make_dequant_inputs, make_gemm_inputs,  # noqa: E402
+                       make_moe_inputs, make_nvfp4_scales)
 
 METRIC = "MoE fwd TFLOP/s (MXFP4 grouped GEMM) & dequant GB/s, % of roofline, 1 GB300"
 WORKLOAD = ("routed MoE prefill forward: T=8192 tokens, hidden 7168, intermediate 3072, 48 experts, "
@@ -452,6 +453,25 @@ def measure_extra(mx, torch, dev, stream):
     res["fp8_dequant"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm, "ms": ms,
                           "bytes": nbytes}
     del t, of
+    torch.cuda.empty_cache()
+    # one dense GEMM (a projection) in both formats, against the FP4 tensor peak
+    a, b, mx_sa, mx_sb, nv_sa, nv_sb, ga, gb = make_gemm_inputs()
+    M, N, K = a.shape[0], b.shape[0], 2 * a.shape[1]
+    g = {k: torch.from_numpy(v).to(dev) for k, v in (("a", a), ("b", b), ("mx_sa", mx_sa), ("nv_sa", nv_sa))}
+    g["mx_sbt"] = torch.empty(mx.mxfp4_tiled_scales_bytes(N, K), dtype=torch.uint8, device=dev)
+    mx.mxfp4_scales_to_tiled(torch.from_numpy(mx_sb).to(dev), g["mx_sbt"])
+    g["nv_sbt"] = torch.empty(mx.nvfp4_tiled_scales_bytes(N, K), dtype=torch.uint8, device=dev)
+    mx.nvfp4_scales_to_tiled(torch.from_numpy(nv_sb).to(dev), g["nv_sbt"])
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    fp4_peak = peaks["bf16_tflops_sustained"] * 6.0
+    for name, fn in (("gemm_mxfp4", lambda: mx.mxfp4_gemm_bf16(g["a"], g["mx_sa"], g["b"], g["mx_sbt"], d,
+                                                               stream=stream)),
+                     ("gemm_nvfp4", lambda: mx.nvfp4_gemm_bf16(g["a"], g["nv_sa"], ga, g["b"], g["nv_sbt"], gb, d,
+                                                               stream=stream))):
+        ms = timeit(fn, reps=20)
+        tflops = 2.0 * M * N * K / ms / 1e9
+        res[name] = {"shape": [M, N, K], "ms": ms, "TFLOP/s": tflops, "frac_fp4_peak": tflops / fp4_peak}
+    del g, d
     torch.cuda.empty_cache()
     for name in ("decode", "shared"):
         inp = make_config_inputs(name)

@@ -111,6 +111,9 @@ int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t
  *   + its E4M3 scales in the tile layout (nvfp4_scales_to_tiled of [N, K/16]);
  *   D uint16 [M, N]. The block-scaled products accumulate in float32; the sum is
  *   multiplied by the float32 product of the globals and rounded once to BF16.
+ *   The tensor cores read the scale bytes as unsigned E4M3: every scale byte of A and B
+ *   must lie in 0x00..0x7E (sign bit clear, not NaN). The library cannot check device
+ *   data; a byte outside that range gives a result other than the signed-E4M3 reading.
  *   K must be a positive multiple of 256, N a positive multiple of 16; M >= 0.
  */
 int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b,

@@ -61,6 +61,10 @@ R12 NVFP4 -> BF16 rounds the exact product once to float32 and then to BF16, bot
     nearest-even: what float32 arithmetic gives, since LUT[code] * e4m3(scale) is exact in
     float32. A NaN result (a NaN scale byte, a NaN global, or 0 times an infinite global)
     is 0x7FC0 with the XOR of the code's, the scale's and the global's sign bits.
+R14 The NVFP4 GEMM is the exact sum of the scaled E2M1 products times the product of the
+    two float32 globals, rounded once to BF16 (the pages give one global per operand and
+    do not say where it is applied). R13, the GEMM's unsigned scale bytes, is a limit of
+    the GPU path's inputs; the oracle decodes every byte.
 
 Parity status: every function below is pinned by the ``-m "not gpu"`` tests (tables from
 the OCP MX definitions and torch's float8 conversions, one-hot nibble/scale tests, the

@@ -11,6 +11,7 @@ from .generators import (  # noqa: F401
     f32_to_bf16_bits,
     make_config_inputs,
     make_dequant_inputs,
+    make_gemm_inputs,
     make_nvfp4_scales,
     make_moe_inputs,
 )

@@ -147,6 +147,21 @@ def make_nvfp4_scales(seed=5, experts=48, I=3072, H=7168, lo=0x20, hi=0x5E, glob
     return s13, s2, float(np.float32(global_scale))
 
 
+def make_gemm_inputs(seed=6, M=8192, N=6144, K=7168):
+    """One dense block-scaled GEMM in both formats: uniform code bytes for A [M, K/2] and
+    B [N, K/2]; MXFP4 E8M0 scales uniform over [118, 124] per 32 columns; NVFP4 E4M3 scales
+    uniform over the positive codes [0x28, 0x48] per 16 columns and float32 globals.
+    Returns (a, b, mx_sa, mx_sb, nv_sa, nv_sb, a_global, b_global)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = _uniform_bytes(rng, (M, K // 2))
+    b = _uniform_bytes(rng, (N, K // 2))
+    mx_sa = rng.integers(118, 125, size=(M, K // 32), dtype=np.uint8)
+    mx_sb = rng.integers(118, 125, size=(N, K // 32), dtype=np.uint8)
+    nv_sa = rng.integers(0x28, 0x49, size=(M, K // 16), dtype=np.uint8)
+    nv_sb = rng.integers(0x28, 0x49, size=(N, K // 16), dtype=np.uint8)
+    return a, b, mx_sa, mx_sb, nv_sa, nv_sb, float(np.float32(0.0123)), float(np.float32(0.0457))
+
+
 def make_dequant_inputs(seed=4, experts=48, I=3072, H=7168, fp8_rows=7168, fp8_cols=7168,
                         sf_lo=118, sf_hi=124, fp8_sf_lo=120, fp8_sf_hi=130):
     """Weight dequant sweep: MXFP4 expert weights flattened to rows, plus one FP8 matrix.
