@@ -10,6 +10,7 @@ from .mxfp4_oracle import (  # noqa: F401
     bf16_bits_from_f64,
     bf16_bits_to_f64,
     e2m1_decode,
+    e4m3_round_code,
     e4m3fn_decode,
     e8m0_decode,
     fp8_block_dequant_128x128,
@@ -19,6 +20,7 @@ from .mxfp4_oracle import (  # noqa: F401
     mxfp4_values,
     moe_combine,
     moe_forward,
+    moe_nvfp4_forward,
     moe_l1_exact,
     moe_l2_bf16,
     moe_route,
@@ -27,6 +29,7 @@ from .mxfp4_oracle import (  # noqa: F401
     nvfp4_dequant,
     nvfp4_gemm_bf16,
     nvfp4_gemm_f64,
+    nvfp4_quantize,
     nvfp4_values,
     unpack_nibbles,
 )

@@ -65,6 +65,21 @@ R14 The NVFP4 GEMM is the exact sum of the scaled E2M1 products times the produc
     two float32 globals, rounded once to BF16 (the pages give one global per operand and
     do not say where it is applied). R13, the GEMM's unsigned scale bytes, is a limit of
     the GPU path's inputs; the oracle decodes every byte.
+R15 NVFP4 quantisation of a row with float32 global scale g ("Warmup-based gs
+    computation" in [GS]'s plan: g is fixed before the call, not taken from the data),
+    per 16-column block, every step a float32 operation rounded to nearest even:
+    r = 1 / (6 g); amax = max |x|; S = the E4M3 byte nearest to min(amax * r, 448), ties
+    to the even code; d = e4m3(S) * g; each element's code is E2M1(x * (1 / d)) to nearest,
+    ties to even, saturating at +-6, sign kept. S = 0 gives codes sign|0. A block holding
+    a NaN or an infinity gets S = 0x7F (NaN) and codes sign|7. This is the published NVFP4
+    encoder (scale = amax / 6 per block, relative to the global); the float32 order is a
+    reading, chosen so that both sides take every rounding decision in the same precision.
+R16 The NVFP4 MoE forward is the MXFP4 one (R1, R3-R5) with NVFP4 in every quantised
+    step: x is quantised with the activation global g_x, h with g_h (R15); the gate and up
+    halves of an expert's w13 carry their own globals ([GS]: "gate+up with different gs"),
+    w2 one; L1's g = bf16(sum * g_x * g_gate) and u = bf16(sum * g_x * g_up), L2's
+    y = bf16(sum * g_h * g_w2), each product of two float32 globals exact in float64 and
+    applied once to the exact sum (R14).
 
 Parity status: every function below is pinned by the ``-m "not gpu"`` tests (tables from
 the OCP MX definitions and torch's float8 conversions, one-hot nibble/scale tests, the
@@ -81,6 +96,7 @@ __all__ = [
     "unpack_nibbles", "mxfp4_values", "mxfp4_dequant", "fp8_block_dequant_128x128",
     "act_quant_mxfp4", "mxfp4_gemm_bf16", "mxfp4_gemm_blockint", "moe_route", "moe_forward",
     "nvfp4_values", "nvfp4_dequant", "nvfp4_gemm_f64", "nvfp4_gemm_bf16",
+    "e4m3_round_code", "nvfp4_quantize", "moe_nvfp4_forward",
     "moe_flops_per_pair", "moe_l1_exact", "swiglu_bf16", "moe_l2_bf16", "moe_combine",
 ]
 
@@ -295,6 +311,57 @@ def act_quant_mxfp4(x_bits):
 
 
 # --------------------------------------------------------------------------------------
+# NVFP4 quantisation (reading R15) [GS]
+# --------------------------------------------------------------------------------------
+
+_E4M3_NONNEG = e4m3fn_decode(np.arange(127))          # codes 0..126, increasing, 0 .. 448
+
+
+def e4m3_round_code(a) -> np.ndarray:
+    """Code 0..126 of the E4M3 value nearest to a (float64, 0 <= a <= 448), ties to the
+    even code (the even mantissa)."""
+    a = np.asarray(a, dtype=np.float64)
+    hi = np.clip(np.searchsorted(_E4M3_NONNEG, a, side="left"), 0, 126)   # first value >= a
+    lo = np.clip(hi - 1, 0, 126)
+    dlo = a - _E4M3_NONNEG[lo]
+    dhi = _E4M3_NONNEG[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    return pick.astype(np.uint8)
+
+
+def nvfp4_quantize(x_bits, global_scale):
+    """BF16 [M, K] -> (codes uint8 [M, K/2], sf uint8 [M, K/16] E4M3) by reading R15, with
+    the float32 global scale g (finite, in [2^-117, 2^100] so every step stays normal)."""
+    xb = np.asarray(x_bits, dtype=np.uint16)
+    M, K = xb.shape
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    if M > 256:                                   # bound the memory of the rounding search
+        parts = [nvfp4_quantize(xb[i:i + 256], global_scale) for i in range(0, M, 256)]
+        return (np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]))
+    f32 = np.float32
+    g = f32(global_scale)
+    r = f32(1.0) / (f32(6.0) * g)
+    x = bf16_bits_to_f64(xb).astype(np.float32).reshape(M, K // 16, 16)   # exact
+    finite = np.isfinite(x).all(axis=-1)
+    amax = np.abs(np.where(np.isfinite(x), x, f32(0.0))).max(axis=-1)
+    with np.errstate(over="ignore"):
+        t = np.minimum(amax * r, f32(448.0))                              # float32 product
+    S = e4m3_round_code(t.astype(np.float64))
+    d = e4m3fn_decode(S).astype(np.float32) * g                           # float32 product
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        rd = f32(1.0) / d                                                 # float32 reciprocal
+        v = x * rd[..., None]                                             # float32 products
+    mag = _e2m1_round_magnitude(np.where(np.isfinite(v), np.abs(v), 6.0).astype(np.float64))
+    mag = np.where((S == 0)[..., None], 0, mag)
+    sign = np.signbit(x).astype(np.uint8)
+    code = np.where(finite[..., None], (sign << 3) | mag, (sign << 3) | 7).astype(np.uint8)
+    sf = np.where(finite, S, 0x7F).astype(np.uint8)
+    code = code.reshape(M, K)
+    return (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8), sf
+
+
+# --------------------------------------------------------------------------------------
 # GEMM over MXFP4 operands [PIPE] (L1 / L2 GEMM; one group is a plain GEMM)
 # --------------------------------------------------------------------------------------
 
@@ -456,4 +523,55 @@ def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, I: int, tokens=None)
         if sel.size == 0:
             continue
         Y[sel[:, 0], sel[:, 1]] = _expert_ffn(xv[sel[:, 0]], w13[e], s13[e], w2[e], s2[e], I)
+    return moe_combine(Y, ids, np.asarray(topk_w, dtype=np.float32)[tok], E)
+
+
+# --------------------------------------------------------------------------------------
+# NVFP4 MoE expert FFN (reading R16) [PIPE], [GS]
+# --------------------------------------------------------------------------------------
+
+
+def _g64(v) -> float:
+    return float(np.float32(v))
+
+
+def moe_nvfp4_forward(x_bits, topk_ids, topk_w, w13, s13, g13, w2, s2, g2, x_global, h_global, I: int,
+                      tokens=None):
+    """NVFP4 MoE expert FFN output as BF16 bits [len(tokens), H] (R16).
+
+    As moe_forward, with NVFP4 weights: w13 uint8 [E, 2I, H/2] + s13 [E, 2I, H/16] (E4M3)
+    and g13 float32 [E, 2] (gate, up globals); w2 uint8 [E, H, I/2] + s2 [E, H, I/16] and
+    g2 float32 [E]; x_global and h_global are the float32 globals of the two activation
+    quantisations.
+    """
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    T, H = x_bits.shape
+    E = w13.shape[0]
+    g13 = np.asarray(g13, dtype=np.float32).reshape(E, 2)
+    g2 = np.asarray(g2, dtype=np.float32).reshape(E)
+    gx, gh = _g64(x_global), _g64(h_global)
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    xq, xs = nvfp4_quantize(x_bits[tok], x_global)
+    xv = nvfp4_values(xq, xs, 1.0)                       # the global goes with the weight's
+
+    def ffn(rows, e):
+        gu = xv[rows] @ nvfp4_values(w13[e], s13[e], 1.0).T                 # exact sums
+        g = gu[:, :I] * (gx * float(g13[e, 0]))
+        u = gu[:, I:] * (gx * float(g13[e, 1]))
+        hq, hs = nvfp4_quantize(swiglu_bf16(g, u), h_global)
+        y = (nvfp4_values(hq, hs, 1.0) @ nvfp4_values(w2[e], s2[e], 1.0).T) * (gh * float(g2[e]))
+        return bf16_bits_to_f64(bf16_bits_from_f64(y))
+
+    if topk_ids is None:
+        if E != 1:
+            raise ValueError("the unrouted (shared expert) mode needs exactly one expert")
+        return bf16_bits_from_f64(ffn(np.arange(tok.size), 0))
+    ids = np.asarray(topk_ids, dtype=np.int64)[tok]
+    n, K = ids.shape
+    Y = np.zeros((n, K, H), dtype=np.float64)
+    for e in range(E):
+        sel = np.argwhere(ids == e)
+        if sel.size == 0:
+            continue
+        Y[sel[:, 0], sel[:, 1]] = ffn(sel[:, 0], e)
     return moe_combine(Y, ids, np.asarray(topk_w, dtype=np.float32)[tok], E)

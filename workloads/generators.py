@@ -26,6 +26,14 @@ Recipes (one seed per workload; "N(0, s)" means standard deviation s; an E8M0 ra
                    [7168, 1536] + [7168, 96]), E8M0 uniform [118, 124]; FP8 E4M3
                    [7168, 7168] uniform over the 254 finite codes with E8M0 128x128 block
                    scales [56, 56] uniform [120, 130].
+* NVFP4 MoE (make_nvfp4_moe_inputs; each MoE config above with its own seed, shapes, x
+                   and routing): weight bytes uniform; E4M3 scale bytes uniform over
+                   [0x68, 0x7E] (64 .. 448, the top of the range a per-block amax / 6
+                   scale fills); weight globals 2^-14 * U[1, 2) * sqrt(7168 / H) for gate
+                   and up (drawn separately) and 2^-14 * U[1, 2) * sqrt(3072 / I) for w2,
+                   so the L1 sums have the same spread at every size; the x global is the
+                   warm-up calibration max|x| / (6 * 448) of the batch itself, the h global
+                   the fixed constant 2^-2.
 """
 from __future__ import annotations
 
@@ -180,3 +188,56 @@ def make_dequant_inputs(seed=4, experts=48, I=3072, H=7168, fp8_rows=7168, fp8_c
     fsf = rng.integers(fp8_sf_lo, fp8_sf_hi + 1,
                        size=((fp8_rows + 127) // 128, (fp8_cols + 127) // 128), dtype=np.uint8)
     return w13, s13, w2, s2, q, fsf
+
+
+@dataclass
+class NvMoEInputs:
+    T: int
+    H: int
+    I: int
+    E: int
+    K: int
+    x: np.ndarray                      # uint16 bf16 bits [T, H]
+    topk_ids: Optional[np.ndarray]     # int32 [T, K] or None (shared expert)
+    topk_w: Optional[np.ndarray]       # float32 [T, K] or None
+    w13: np.ndarray                    # uint8 [E, 2I, H/2]  rows [0, I) gate, [I, 2I) up
+    s13: np.ndarray                    # uint8 [E, 2I, H/16] E4M3
+    g13: np.ndarray                    # float32 [E, 2] gate, up globals
+    w2: np.ndarray                     # uint8 [E, H, I/2]
+    s2: np.ndarray                     # uint8 [E, H, I/16] E4M3
+    g2: np.ndarray                     # float32 [E]
+    x_global: float                    # float32 values
+    h_global: float
+
+
+NV_H_GLOBAL = 0.25
+
+
+def make_nvfp4_moe_inputs(T, H, I, E, K, seed, routing="uniform", x_sigma=1.0, outlier_p=0.0,
+                          outlier_scale=20.0, sf_lo=0x68, sf_hi=0x7E, h_global=NV_H_GLOBAL, **_unused):
+    """Draw one NVFP4 MoE workload (recipe in the module docstring). Accepts the keyword
+    arguments of an MXFP4 config (its E8M0 range is ignored)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 100))
+    x = rng.standard_normal((T, H), dtype=np.float32) * np.float32(x_sigma)
+    if outlier_p > 0.0:
+        mask = rng.random((T, H)) < outlier_p
+        x[mask] *= np.float32(outlier_scale)
+    xb = f32_to_bf16_bits(x)
+    ids, w = make_routing(rng, T, E, K, routing)
+    w13 = _uniform_bytes(rng, (E, 2 * I, H // 2))
+    s13 = rng.integers(sf_lo, sf_hi + 1, size=(E, 2 * I, H // 16), dtype=np.uint8)
+    w2 = _uniform_bytes(rng, (E, H, I // 2))
+    s2 = rng.integers(sf_lo, sf_hi + 1, size=(E, H, I // 16), dtype=np.uint8)
+    g13 = (2.0 ** -14 * rng.uniform(1.0, 2.0, size=(E, 2)) * np.sqrt(7168.0 / H)).astype(np.float32)
+    g2 = (2.0 ** -14 * rng.uniform(1.0, 2.0, size=E) * np.sqrt(3072.0 / I)).astype(np.float32)
+    xv = (xb.astype(np.uint32) << 16).view(np.float32)
+    amax = float(np.abs(xv).max()) if T > 0 else 1.0
+    x_global = float(np.float32(np.float32(amax) / np.float32(6 * 448)))
+    return NvMoEInputs(T, H, I, E, (K if routing is not None else 1), xb, ids, w, w13, s13, g13,
+                       w2, s2, g2, x_global, float(np.float32(h_global)))
+
+
+def make_nvfp4_config_inputs(name: str) -> NvMoEInputs:
+    c = dict(CONFIGS[name])
+    return make_nvfp4_moe_inputs(c.pop("T"), c.pop("H"), c.pop("I"), c.pop("E"), c.pop("K"),
+                                 c.pop("seed"), **c)
