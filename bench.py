@@ -38,7 +38,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from workloads import (CONFIGS, make_config_inputs, make_dequant_inputs, make_gemm_inputs,  # noqa: E402
-                       make_moe_inputs, make_nvfp4_scales)
+                       make_moe_inputs, make_nvfp4_config_inputs, make_nvfp4_scales)
 
 METRIC = "MoE fwd TFLOP/s (MXFP4 grouped GEMM) & dequant GB/s, % of roofline, 1 GB300"
 WORKLOAD = ("routed MoE prefill forward: T=8192 tokens, hidden 7168, intermediate 3072, 48 experts, "
@@ -521,7 +521,48 @@ def measure_extra(mx, torch, dev, stream):
         del graphs
         del x, ids, w, W, out, ws, flush
         torch.cuda.empty_cache()
+    res.update(measure_nvfp4_forward(mx, torch, dev, stream, timeit))
     return res
+
+
+def measure_nvfp4_forward(mx, torch, dev, stream, timeit):
+    """The routed prefill forward with NVFP4 weights and activations (the same shapes, routing
+    and x recipe as the MXFP4 step; E4M3 scales per 16, gate/up/down globals)."""
+    inp = make_nvfp4_config_inputs("prefill")
+    c = CONFIGS["prefill"]
+    x = torch.from_numpy(inp.x).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(inp.topk_ids).to(dev)
+    w = torch.from_numpy(inp.topk_w).to(dev)
+    w13, w2, g13, g2 = (torch.from_numpy(a).to(dev) for a in (inp.w13, inp.w2, inp.g13, inp.g2))
+    s13t = torch.empty(mx.nvfp4_tiled_scales_bytes(c["E"] * 2 * c["I"], c["H"]), dtype=torch.uint8, device=dev)
+    s2t = torch.empty(mx.nvfp4_tiled_scales_bytes(c["E"] * c["H"], c["I"]), dtype=torch.uint8, device=dev)
+    mx.nvfp4_scales_to_tiled(torch.from_numpy(inp.s13.reshape(-1, c["H"] // 16)).to(dev), s13t)
+    mx.nvfp4_scales_to_tiled(torch.from_numpy(inp.s2.reshape(-1, c["I"] // 16)).to(dev), s2t)
+    out = torch.empty((c["T"], c["H"]), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mx.moe_nvfp4_workspace_size(c["T"], c["H"], c["I"], c["E"], c["K"], True), dtype=torch.uint8,
+                     device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    def fwd(events=None):
+        mx.moe_nvfp4_forward(x, ids, w, w13, s13t, g13, w2, s2t, g2, inp.x_global, inp.h_global, out, ws,
+                             stream=stream, events=events)
+
+    ms = timeit(fwd, reps=20)
+    fwd(ev)
+    torch.cuda.synchronize()
+    pairs = int(((inp.topk_ids >= 0) & (inp.topk_ids < c["E"])).sum())
+    flop = pairs * flops_per_pair(c["H"], c["I"])
+    l1_ms = ev[2].elapsed_time(ev[3])
+    l1_tflops = pairs * 2 * c["H"] * 2 * c["I"] / l1_ms / 1e9
+    fp4_peak = measured_peaks()[0]["bf16_tflops_sustained"] * 6.0
+    r = {"nvfp4_forward": {"workload": "routed prefill T=8192, H=7168, I=3072, 48 experts, top-8, NVFP4",
+                           "ms": ms, "TFLOP/s": flop / ms / 1e9,
+                           "phases_ms": {k: ev[i].elapsed_time(ev[i + 1]) for i, k in
+                                         enumerate(("route", "quant_gather", "l1_gemm", "l2_gemm", "combine"))},
+                           "l1_TFLOP/s": l1_tflops, "l1_frac_fp4_peak": l1_tflops / fp4_peak}}
+    del x, ids, w, w13, w2, g13, g2, s13t, s2t, out, ws
+    torch.cuda.empty_cache()
+    return r
 
 
 def main():

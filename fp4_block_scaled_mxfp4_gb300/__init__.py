@@ -1,13 +1,14 @@
 """GB300 (sm_103a) MXFP4 mixture-of-experts expert FFN.
 
 The compute path is the C-ABI library ``libmxfp4moe.so`` (hand-written CUDA: tcgen05
-block-scaled grouped GEMM, routing, MX quantiser, combine, MXFP4 / NVFP4 / FP8 dequant
+block-scaled grouped GEMM (MXFP4 and NVFP4), routing, MX / NVFP4 quantisers, combine, MXFP4 / NVFP4 / FP8 dequant
 kernels); this package only builds it (``build.build()``) and marshals torch tensors into
 its calls.
 """
 from ._native import (  # noqa: F401
     MXError,
     act_quant_mxfp4,
+    act_quant_nvfp4,
     device_status,
     fp8_block_dequant_128x128,
     lib,
@@ -16,6 +17,9 @@ from ._native import (  # noqa: F401
     moe_mxfp4_route,
     moe_mxfp4_workspace_layout,
     moe_mxfp4_workspace_size,
+    moe_nvfp4_forward,
+    moe_nvfp4_workspace_layout,
+    moe_nvfp4_workspace_size,
     mxfp4_dequant,
     mxfp4_gemm_bf16,
     mxfp4_scales_to_tiled,

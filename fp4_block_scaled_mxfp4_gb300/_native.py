@@ -30,6 +30,15 @@ _SIGNATURES = {
     "nvfp4_gemm_bf16": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_ptr, ctypes.c_float, _c_ptr,
                                        _c_i64, _c_i64, _c_i64, _c_ptr]),
     "act_quant_mxfp4": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "act_quant_nvfp4": (ctypes.c_int, [_c_ptr, ctypes.c_float, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "moe_nvfp4_workspace_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
+    "moe_nvfp4_workspace_layout": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int, _c_ptr]),
+    "moe_nvfp4_forward": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                         ctypes.c_float, ctypes.c_float, _c_ptr, _c_i64, _c_i64, _c_i64, _c_i64,
+                                         _c_i64, _c_ptr, ctypes.c_size_t, _c_ptr]),
+    "moe_nvfp4_forward_timed": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                               _c_ptr, ctypes.c_float, ctypes.c_float, _c_ptr, _c_i64, _c_i64,
+                                               _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t, _c_ptr, _c_ptr]),
     "mxfp4_tiled_scales_bytes": (ctypes.c_size_t, [_c_i64, _c_i64]),
     "mxfp4_scales_to_tiled": (ctypes.c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "mxfp4_gemm_bf16": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_ptr]),
@@ -200,6 +209,18 @@ def act_quant_mxfp4(x, codes, sf, stream=None) -> None:
     _check(lib().act_quant_mxfp4(_ptr(x), _ptr(codes), _ptr(sf), M, K, _stream(stream)), "act_quant_mxfp4")
 
 
+def act_quant_nvfp4(x, global_scale, codes, sf, stream=None) -> None:
+    """NVFP4 quantisation of BF16 x [M, K] against the float32 global: codes u8 [M, K/2],
+    E4M3 scales u8 [M, K/16]."""
+    import torch
+    M, K = x.shape
+    _need(x, x.dtype, (M, K), "x")
+    _need(codes, torch.uint8, (M, K // 2), "codes")
+    _need(sf, torch.uint8, (M, K // 16), "sf")
+    _check(lib().act_quant_nvfp4(_ptr(x), float(global_scale), _ptr(codes), _ptr(sf), M, K, _stream(stream)),
+           "act_quant_nvfp4")
+
+
 def mxfp4_tiled_scales_bytes(rows: int, cols: int) -> int:
     return int(lib().mxfp4_tiled_scales_bytes(rows, cols))
 
@@ -286,6 +307,53 @@ def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, str
         _check(lib().moe_mxfp4_forward_tiled(*args), "moe_mxfp4_forward_tiled")
     else:
         _check(lib().moe_mxfp4_forward(*args), "moe_mxfp4_forward")
+
+
+def moe_nvfp4_workspace_size(T: int, H: int, I: int, E: int, K: int, routed: bool = True) -> int:
+    return int(lib().moe_nvfp4_workspace_size(T, H, I, E, K, 1 if routed else 0))
+
+
+def moe_nvfp4_workspace_layout(T: int, H: int, I: int, E: int, K: int, routed: bool = True) -> dict:
+    """Byte offsets of the intermediates an NVFP4 forward leaves in its workspace."""
+    buf = (ctypes.c_int64 * 8)()
+    _check(lib().moe_nvfp4_workspace_layout(T, H, I, E, K, 1 if routed else 0, ctypes.addressof(buf)),
+           "moe_nvfp4_workspace_layout")
+    names = ("xq", "xs", "hq", "hs", "y", "row_of", "counts", "offsets")
+    return {n: int(v) for n, v in zip(names, buf)}
+
+
+def moe_nvfp4_forward(x, topk_ids, topk_w, w13, s13_tiled, g13, w2, s2_tiled, g2, x_global, h_global, out,
+                      workspace, stream=None, events=None) -> None:
+    """MoE expert FFN over NVFP4 weights and activations; topk_ids/topk_w None selects the
+    shared expert. s13_tiled / s2_tiled: nvfp4_scales_to_tiled of the E4M3 scales
+    ([E*2I, H/16], [E*H, I/16]); g13 float32 [E, 2] (gate, up) and g2 float32 [E] on the
+    device; x_global / h_global: the activation globals. ``events`` as in moe_mxfp4_forward."""
+    import torch
+    T, H = x.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    K = topk_ids.shape[1] if topk_ids is not None else 1
+    _need(x, x.dtype, (T, H), "x")
+    if topk_ids is not None:
+        _need(topk_ids, torch.int32, (T, K), "topk_ids")
+        _need(topk_w, torch.float32, (T, K), "topk_w")
+    _need(w13, torch.uint8, (E, 2 * I, H // 2), "w13")
+    _need(w2, torch.uint8, (E, H, I // 2), "w2")
+    for t, r, c, n in ((s13_tiled, E * 2 * I, H, "s13_tiled"), (s2_tiled, E * H, I, "s2_tiled")):
+        if t.dtype != torch.uint8 or t.numel() < nvfp4_tiled_scales_bytes(r, c) or not t.is_cuda:
+            raise ValueError(f"{n}: expected the tile layout of the E4M3 scales")
+    _need(g13, torch.float32, (E, 2), "g13")
+    _need(g2, torch.float32, (E,), "g2")
+    _need(out, out.dtype, (T, H), "out")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    args = (_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13_tiled), _ptr(g13), _ptr(w2), _ptr(s2_tiled),
+            _ptr(g2), float(x_global), float(h_global), _ptr(out), T, H, I, E, K, _ptr(workspace), ws_bytes,
+            _stream(stream))
+    if events is not None:
+        evs = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else 0) for e in events])
+        _check(lib().moe_nvfp4_forward_timed(*args, ctypes.addressof(evs)), "moe_nvfp4_forward_timed")
+    else:
+        _check(lib().moe_nvfp4_forward(*args), "moe_nvfp4_forward")
 
 
 def moe_mxfp4_route(topk_ids, E: int, counts, offsets, row_of, workspace, stream=None) -> None:

@@ -105,7 +105,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Bytes of a scale tensor [rows, kb] in the tile layout (128-row groups x 4-byte K-words).
 size_t tiled_bytes(int64_t rows, int64_t kb) { return (size_t)((rows + 127) / 128) * (size_t)(kb / 4) * 512; }
 
-// Workspace layout shared by moe_mxfp4_forward and moe_mxfp4_route.
+// Workspace layout shared by moe_mxfp4_forward, moe_nvfp4_forward (sf_div 16: one scale
+// per 16 columns) and moe_mxfp4_route.
 struct WsLayout {
     int64_t R = 0, nchunks = 0, max_mtiles = 0;
     size_t num_mtiles = 0, counts = 0, offsets = 0, chunk_counts = 0, chunk_base = 0, local_rank = 0,
@@ -113,7 +114,7 @@ struct WsLayout {
            total = 0;
 };
 
-WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool routed) {
+WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool routed, int sf_div = 32) {
     WsLayout L;
     L.R = routed ? T * K : T;
     L.nchunks = routed ? (L.R + kRouteChunk - 1) / kRouteChunk : 0;
@@ -137,9 +138,9 @@ WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool r
         L.tile_rows = take(4 * (size_t)L.max_mtiles);
     }
     L.xq = take((size_t)L.R * (size_t)(H / 2));
-    L.xs = take((size_t)L.R * (size_t)(H / 32));
+    L.xs = take((size_t)L.R * (size_t)(H / sf_div));
     L.hq = take((size_t)L.R * (size_t)(I / 2));
-    L.hs = take((size_t)L.R * (size_t)(I / 32));
+    L.hs = take((size_t)L.R * (size_t)(I / sf_div));
     if (routed) L.y = take((size_t)L.R * (size_t)H * 2);
     L.total = off;
     return L;
@@ -196,6 +197,10 @@ GemmArgs base_args(const uint8_t* sfa, const uint8_t* sfb, int64_t K, int64_t a_
     g.status = status;
     return g;
 }
+
+// A float32 global scale the NVFP4 quantiser accepts: finite and in [2^-117, 2^100], so that
+// 1 / (6 g), e4m3(scale) * g and its reciprocal are normal floats.
+bool nv_global_ok(float g) { return g >= 0x1p-117f && g <= 0x1p100f; }
 
 int grid_for(int64_t work, int num_sms) {
     int64_t g = work < num_sms ? work : num_sms;
@@ -274,6 +279,20 @@ int fp8_block_dequant_128x128(const uint8_t* q, const uint8_t* sf, void* out_bf1
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int act_quant_nvfp4(const void* x_bf16, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
+                    mx_stream_t stream) {
+    if (M < 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (!nv_global_ok(global_scale)) return MX_ERR_INVALID_ARG;
+    if (K % 16) return MX_ERR_UNSUPPORTED;
+    if (M == 0) return MX_OK;
+    if (!x_bf16 || !codes || !sf) return MX_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || (reinterpret_cast<uintptr_t>(codes) & 7u) != 0) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_act_quant_nvfp4(static_cast<const uint16_t*>(x_bf16), global_scale, codes, sf, M, K,
+                                              d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 int act_quant_mxfp4(const void* x_bf16, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K, mx_stream_t stream) {
     if (M < 0 || K <= 0) return MX_ERR_INVALID_ARG;
     if (K % 32) return MX_ERR_UNSUPPORTED;
@@ -319,7 +338,7 @@ int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t
 int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b, const uint8_t* sb_tiled,
                     float b_global, void* d_bf16, int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
     if (M < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
-    if (K % 256 || N % 16) return MX_ERR_UNSUPPORTED;
+    if (K % 128 || N % 16) return MX_ERR_UNSUPPORTED;
     if (M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 24)) return MX_ERR_UNSUPPORTED;
     if (M == 0) return MX_OK;
     if (!a || !sa || !b || !sb_tiled || !d_bf16) return MX_ERR_INVALID_ARG;
@@ -426,19 +445,31 @@ int moe_mxfp4_route(const int32_t* topk_ids, int64_t T, int64_t K, int64_t E, in
 
 namespace {
 
+// The NVFP4 forward's extra inputs: per-expert weight globals (g13 [E][2] gate, up; g2 [E],
+// device float32) and the two activation globals.
+struct NvGlobals {
+    const float* g13;
+    const float* g2;
+    float x_global;
+    float h_global;
+};
+
 int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
                  const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T, int64_t H,
                  int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream,
-                 void* const* events, bool scales_tiled) {
+                 void* const* events, bool scales_tiled, const NvGlobals* nv = nullptr) {
     const bool routed = topk_ids != nullptr;
     if (routed != (topk_w != nullptr)) return MX_ERR_INVALID_ARG;
     if (int e = check_moe_dims(T, H, I, E, K, routed)) return e;
+    if (nv && (!nv_global_ok(nv->x_global) || !nv_global_ok(nv->h_global))) return MX_ERR_INVALID_ARG;
     if (T == 0) return MX_OK;
     if (!x || !w13 || !s13 || !w2 || !s2 || !out) return MX_ERR_INVALID_ARG;
+    if (nv && (!nv->g13 || !nv->g2)) return MX_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w13) || !aligned16(s13) || !aligned16(w2) || !aligned16(s2) ||
         !aligned16(out))
         return MX_ERR_MISALIGNED;
-    const WsLayout L = ws_layout(T, H, I, E, K, routed);
+    const int sf_div = nv ? 16 : 32;
+    const WsLayout L = ws_layout(T, H, I, E, K, routed, sf_div);
     if (!workspace || ws_bytes < L.total) return MX_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
     DeviceInfo* d;
@@ -455,12 +486,25 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
 
     GemmArgs g1 = base_args(xs, s13, H, R, E * 2 * I, d->status);
     GemmArgs g2 = base_args(hs, s2, I, R, E * H, d->status);
+    if (nv) {
+        // one E4M3 scale per 16 elements: four per 4-byte word
+        g1.ld_sf = H / 16;
+        g1.kw = H / 64;
+        g1.alpha = nv->x_global;
+        g1.w_global = nv->g13;
+        g1.q_global = nv->h_global;
+        g2.ld_sf = I / 16;
+        g2.kw = I / 64;
+        g2.alpha = nv->h_global;
+        g2.w_global = nv->g2;
+    }
     RouteBufs rb{};
     if (!mark(0)) return MX_ERR_CUDA;
     if (routed) {
         rb = route_bufs(workspace, L);
         if (launch_route(topk_ids, T, K, E, rb, s) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
-        if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s) != cudaSuccess)
+        if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s, nv != nullptr,
+                                nv ? nv->x_global : 0.0f) != cudaSuccess)
             return MX_ERR_CUDA;
         for (GemmArgs* g : {&g1, &g2}) {
             g->tile_expert = rb.tile_expert;
@@ -470,8 +514,10 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
         }
     } else {
         if (!mark(1)) return MX_ERR_CUDA;
-        if (launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s) != cudaSuccess)
-            return MX_ERR_CUDA;
+        const cudaError_t qe =
+            nv ? launch_act_quant_nvfp4(static_cast<const uint16_t*>(x), nv->x_global, xq, xs, T, H, d->num_sms, s)
+               : launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s);
+        if (qe != cudaSuccess) return MX_ERR_CUDA;
         for (GemmArgs* g : {&g1, &g2}) {
             g->num_mtiles_host = (int32_t)((T + kBM - 1) / kBM);
             g->m_total = T;
@@ -483,8 +529,9 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     // Tile widths: 256 columns, or 128 where 256-wide tiles would leave SMs idle. Only with
     // uniform tiling: the routed tile count is known on the device alone, and its bound
     // max_mtiles counts an extra tile per expert.
-    const int n1 = routed ? kBN : tile_cols(max_mtiles * (I / 128), d->num_sms);
-    const int n2 = routed ? kBN : tile_cols(max_mtiles * ((H + kBN - 1) / kBN), d->num_sms);
+    // NVFP4 runs 256-column tiles only.
+    const int n1 = routed || nv ? kBN : tile_cols(max_mtiles * (I / 128), d->num_sms);
+    const int n2 = routed || nv ? kBN : tile_cols(max_mtiles * ((H + kBN - 1) / kBN), d->num_sms);
 
     // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
     CUtensorMap ta1, tb1, ty1, ta2, tb2, ty2;
@@ -498,9 +545,10 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     g1.hq = hq;
     g1.hs = hs;
     g1.ld_hq = I / 2;
-    g1.ld_hs = I / 32;
-    if (launch_gemm_l1(ta1, tb1, ty1, g1, grid_for(max_mtiles * g1.n_tiles, d->num_sms), scales_tiled, n1, s) !=
-            cudaSuccess ||
+    g1.ld_hs = I / sf_div;
+    const int grid1 = grid_for(max_mtiles * g1.n_tiles, d->num_sms);
+    if ((nv ? launch_gemm_nvfp4_l1(ta1, tb1, ty1, g1, grid1, s) : launch_gemm_l1(ta1, tb1, ty1, g1, grid1, scales_tiled,
+                                                                                  n1, s)) != cudaSuccess ||
         !mark(3))
         return MX_ERR_CUDA;
 
@@ -512,8 +560,9 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     g2.y = routed ? at<uint16_t>(workspace, L.y) : static_cast<uint16_t*>(out);
     g2.ld_y = H;
     if (make_tmap_out(&ty2, g2.y, H, R)) return MX_ERR_CUDA;
-    if (launch_gemm_l2(ta2, tb2, ty2, g2, grid_for(max_mtiles * g2.n_tiles, d->num_sms), scales_tiled, n2, s) !=
-            cudaSuccess ||
+    const int grid2 = grid_for(max_mtiles * g2.n_tiles, d->num_sms);
+    if ((nv ? launch_gemm_nvfp4(ta2, tb2, ty2, g2, grid2, s) : launch_gemm_l2(ta2, tb2, ty2, g2, grid2, scales_tiled,
+                                                                              n2, s)) != cudaSuccess ||
         !mark(4))
         return MX_ERR_CUDA;
 
@@ -550,6 +599,44 @@ int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float*
                             mx_stream_t stream, void* const* events, int scales_tiled) {
     return forward_impl(x, topk_ids, topk_w, w13, s13, w2, s2, out, T, H, I, E, K, workspace, ws_bytes, stream,
                         events, scales_tiled != 0);
+}
+
+size_t moe_nvfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed) {
+    if (check_moe_dims(T, H, I, E, K, routed != 0) != MX_OK) return 0;
+    return ws_layout(T, H, I, E, K, routed != 0, 16).total;
+}
+
+int moe_nvfp4_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed, int64_t* out) {
+    if (!out) return MX_ERR_INVALID_ARG;
+    if (int e = check_moe_dims(T, H, I, E, K, routed != 0)) return e;
+    const WsLayout L = ws_layout(T, H, I, E, K, routed != 0, 16);
+    out[0] = (int64_t)L.xq;
+    out[1] = (int64_t)L.xs;
+    out[2] = (int64_t)L.hq;
+    out[3] = (int64_t)L.hs;
+    out[4] = routed ? (int64_t)L.y : -1;
+    out[5] = routed ? (int64_t)L.row_of : -1;
+    out[6] = routed ? (int64_t)L.counts : -1;
+    out[7] = routed ? (int64_t)L.offsets : -1;
+    return MX_OK;
+}
+
+int moe_nvfp4_forward_timed(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                            const uint8_t* s13_tiled, const float* g13, const uint8_t* w2, const uint8_t* s2_tiled,
+                            const float* g2, float x_global, float h_global, void* out, int64_t T, int64_t H,
+                            int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream,
+                            void* const* events) {
+    const NvGlobals nv{g13, g2, x_global, h_global};
+    return forward_impl(x, topk_ids, topk_w, w13, s13_tiled, w2, s2_tiled, out, T, H, I, E, K, workspace, ws_bytes,
+                        stream, events, true, &nv);
+}
+
+int moe_nvfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                      const uint8_t* s13_tiled, const float* g13, const uint8_t* w2, const uint8_t* s2_tiled,
+                      const float* g2, float x_global, float h_global, void* out, int64_t T, int64_t H, int64_t I,
+                      int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream) {
+    return moe_nvfp4_forward_timed(x, topk_ids, topk_w, w13, s13_tiled, g13, w2, s2_tiled, g2, x_global, h_global,
+                                   out, T, H, I, E, K, workspace, ws_bytes, stream, nullptr);
 }
 
 }  // extern "C"

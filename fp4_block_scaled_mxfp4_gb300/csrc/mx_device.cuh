@@ -118,6 +118,61 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&f)[32], uint4& code
     return E;
 }
 
+// E4M3 byte of a float 0 <= t <= 448: round to nearest, ties to even (the second source
+// of the x2 conversion lands in the low byte).
+__device__ __forceinline__ uint32_t e4m3_rn(float t) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+    return (uint32_t)r & 0xFFu;
+}
+
+// Value of a non-negative finite E4M3 byte (0x00..0x7E), exact in float32.
+__device__ __forceinline__ float e4m3_pos_value(uint32_t s) {
+    const uint32_t e = s >> 3, m = s & 7u;
+    return e == 0 ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// NVFP4 quantisation of one 16-element block held by this thread (float values that are
+// BF16 numbers) against the float32 global g, with r = 1 / (6 g): the scale byte is the
+// E4M3 value nearest min(amax * r, 448), and each element's code the E2M1 value nearest
+// x * (1 / (e4m3(scale) * g)), saturating at 6 and keeping the sign; every step one float32
+// operation rounded to nearest even. A zero scale gives the codes +-0; a block holding a NaN
+// or an infinity gets the NaN scale 0x7F and codes sign|7. Writes 8 bytes of codes and
+// returns the scale byte.
+__device__ __forceinline__ uint32_t nv_quant16(const float* f, float g, float r, uint2& codes) {
+    float amax = 0.0f;
+    uint32_t bad = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        bad |= (uint32_t)((__float_as_uint(f[i]) & 0x7F800000u) == 0x7F800000u);
+        amax = fmaxf(amax, fabsf(f[i]));
+    }
+    uint32_t w[2] = {0, 0};
+    uint32_t S;
+    if (bad) {
+        S = 0x7Fu;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i >> 3] |= (((__float_as_uint(f[i]) >> 28) & 8u) | 7u) << (4 * (i & 7));
+    } else {
+        S = e4m3_rn(fminf(__fmul_rn(amax, r), 448.0f));
+        if (S == 0) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i >> 3] |= ((__float_as_uint(f[i]) >> 28) & 8u) << (4 * (i & 7));
+        } else {
+            const float rd = __frcp_rn(__fmul_rn(e4m3_pos_value(S), g));
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float sv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sv[i] = fminf(fmaxf(__fmul_rn(f[8 * k + i], rd), -6.0f), 6.0f);
+                w[k] = e2m1x8(sv);
+            }
+        }
+    }
+    codes = make_uint2(w[0], w[1]);
+    return S;
+}
+
 // E2M1 magnitude values by code (device constant table used by the dequant kernels).
 __device__ __forceinline__ float e2m1_value(uint32_t code) {
     // magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 built from the bit fields

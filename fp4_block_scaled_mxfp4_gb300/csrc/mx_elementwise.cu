@@ -275,6 +275,34 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __rest
     pdl_launch_dependents();
 }
 
+// NVFP4 activation quantisation (nv_quant16): one thread per 16-element block, two 16-byte
+// loads, 8 bytes of codes and one E4M3 scale byte out.
+__global__ void __launch_bounds__(kThreads) act_quant_nv_kernel(const uint4* __restrict__ x8,
+                                                                uint2* __restrict__ codes8,
+                                                                uint8_t* __restrict__ sf, int64_t blocks,
+                                                                float g) {
+    pdl_wait();
+    const float r = __frcp_rn(__fmul_rn(6.0f, g));
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < blocks; b += stride) {
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint4 v = __ldg(x8 + 2 * b + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[8 * i + 2 * j] = bf16_to_f32(w[j] & 0xFFFFu);
+                f[8 * i + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
+            }
+        }
+        uint2 codes;
+        sf[b] = (uint8_t)nv_quant16(f, g, r, codes);
+        codes8[b] = codes;
+    }
+    pdl_launch_dependents();
+}
+
 // out[t, c] = bf16( sum_k w[t,k] * y[row_of[t,k], c] ), float32, slot order, no FMA.
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ y8,
                                                            const int32_t* __restrict__ row_of,
@@ -377,6 +405,14 @@ cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int
     if (blocks == 0) return cudaSuccess;
     return launch_pdl(act_quant_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
                       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks);
+}
+
+cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M,
+                                   int64_t K, int num_sms, cudaStream_t s) {
+    const int64_t blocks = M * (K / 16);
+    if (blocks == 0) return cudaSuccess;
+    return launch_pdl(act_quant_nv_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
+                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(codes), sf, blocks, global_scale);
 }
 
 cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,

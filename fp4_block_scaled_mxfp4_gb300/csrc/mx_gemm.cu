@@ -2,7 +2,8 @@
 // kind::mxf4, E2M1 x E2M1 with E8M0 scales per 32 elements of K, FP32 accumulation in
 // tensor memory), with the two epilogues of the expert FFN:
 //   L1: D = A . W13^T over a tile of kN / 2 gate + kN / 2 up columns; the epilogue rounds g
-//       and u to BF16, forms h = bf16(silu(g) * u) and re-quantises h to MXFP4 (codes + E8M0).
+//       and u to BF16, forms h = bf16(silu(g) * u) and re-quantises h to MXFP4 (codes + E8M0),
+//       or to NVFP4 in the kNv mode (kind::mxf4nvf4, E4M3 scales per 16 plus global scales).
 //   L2: D = A . W2^T over kN output columns; the epilogue writes BF16.
 // Tiles are 128 rows x kN columns, kN = 256, or 128 where 256-wide tiles would leave SMs
 // idle (see Cfg).
@@ -81,12 +82,15 @@ constexpr int kMaxStages = 5;
 //
 // kNv: NVFP4 operands (E4M3 scales per 16 elements of K, idesc scale format E4M3): four
 // scale words per row and stage instead of two, so two A images, twice B's blocks and
-// copies, twice the TMEM columns per slot, and three stages.
+// copies, twice the TMEM columns per slot, and three stages. The accumulator is scaled by
+// the operands' global scales in the epilogue (L1: per expert, gate and up separately), and
+// L1 re-quantises h to NVFP4 (E4M3 per 16 against h's global).
 template <int kN, bool kNv = false>
 struct Cfg {
     static constexpr int kStages = kNv ? 3 : (kN == 256 ? 4 : 5);
     static constexpr int kBBytes = kN * kBK / 2;                    // 32 or 16 KB
     static constexpr int kWords = kNv ? 4 : 2;                      // scale words per row and stage
+    static constexpr int kWordsHalf = kWords / 2;                   // ... at a K tail of 128
     static constexpr int kSfaBytes = (kWords / 2) * 4096;           // wide images of two words each
     static constexpr int kSfbBytes = (kN / 128) * kWords * 512;     // per 128 rows: kWords x 512 B
     static constexpr int kSfCols = kNv ? 48 : kSfColsPerStage;      // A: 4 per word; B: 8 per word
@@ -184,7 +188,7 @@ template <bool kL1, bool kBTiled, int kN, bool kNv = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
-    static_assert(!kNv || (!kL1 && kBTiled), "NVFP4: the one-group BF16 GEMM with tile-layout B scales");
+    static_assert(!kNv || kBTiled, "NVFP4 weights come with tile-layout scales");
     using C = Cfg<kN, kNv>;
     constexpr int kBBytes = C::kBBytes;
     constexpr uint32_t kIdesc = C::kIdesc;
@@ -298,11 +302,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t acc0 = kt != 0;
                     // 64 E2M1 elements (32 bytes) of K per MMA, inside the 128-byte swizzle atom
                     if constexpr (kNv) {
-                        // one scale word per MMA: A's at +4k, B's at +8k
+                        // one scale word per MMA: A's at +4k, B's at +8k; two MMAs at a K tail
+                        const int nk = (args.k_tail_half && kt == k_tiles - 1) ? 2 : 4;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            tc_mma_nvf4(tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, sfa + 4 * k, sfb + 8 * k,
-                                        k == 0 ? acc0 : 1u);
+                            if (k < nk)
+                                tc_mma_nvf4(tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, sfa + 4 * k, sfb + 8 * k,
+                                            k == 0 ? acc0 : 1u);
                         tc_commit(smem_u32(&ctl->empty[s]));
                         continue;
                     }
@@ -343,9 +349,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t st = sbase + s * kStageBytes;
                 const int64_t kcol = (int64_t)kt * 4 * C::kWords;   // first scale byte of this stage
                 if (kBTiled && kN == 256 && lane == 0) {
-                    // B scales: K-words 2kt, 2kt+1 of each 128-row group (one at the K tail);
-                    // each 128-row half of the tile is one whole group of the tile layout
-                    const uint32_t sf_bytes = half ? 512u : (uint32_t)(C::kWords * 512);
+                    // B scales: the stage's kWords K-words of each 128-row group (half of them at
+                    // the K tail); each 128-row half of the tile is one whole group of the tile
+                    // layout
+                    const uint32_t sf_bytes = (uint32_t)((half ? C::kWordsHalf : C::kWords) * 512);
                     const uint32_t bar = smem_u32(&ctl->sf_full[s]);
                     int64_t grp[2];
                     uint32_t tx = 0;
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint8_t* src = args.sfa + (valid ? grow * args.ld_sf + kcol : 0);
 #pragma unroll
                         for (int wd = 0; wd < C::kWords; ++wd) {
-                            const bool ok = valid && (wd == 0 || !half);
+                            const bool ok = valid && (wd < C::kWordsHalf || !half);
                             const uint32_t dst = sfa_s + 4096 * (wd >> 1) + wide_off(32 * j + lane, wd & 1);
                             cp_async_4(dst, ok ? src + 4 * wd : args.sfa, ok ? 4u : 0u);
                         }
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // reads them through the async proxy
                     fence_proxy_async_smem();
                     tc_fence_after();
-                    const int nwords = (args.k_tail_half && kt == k_tiles - 1) ? 1 : C::kWords;
+                    const int nwords = (args.k_tail_half && kt == k_tiles - 1) ? C::kWordsHalf : C::kWords;
                     const uint32_t sfa_s = sbase + s * kStageBytes + kABytes + kBBytes;
                     const uint32_t sfb_s = sfa_s + kSfaBytes;
                     const uint32_t sfa_t = tmem + kSfTmemBase + s * C::kSfCols;
@@ -468,14 +475,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
         uint8_t* staging = smem + kStagingOff + (warp - 4) * kStagingBytes;
         const uint32_t staging_s = smem_u32(staging);
-        // L2's output value of an accumulator word (NVFP4: times the two global scales)
+        // NVFP4: the tile's global-scale products (L2: alpha_a; L1: gate alpha_a, up alpha_b)
+        // and the re-quantisation global of L1's h with its 1 / (6 g)
+        float alpha_a = 1.0f, alpha_b = 1.0f;
+        const float q_g = kNv ? args.q_global : 0.0f;
+        const float q_r = kNv && kL1 ? __frcp_rn(__fmul_rn(6.0f, q_g)) : 0.0f;
+        // L2's output value of an accumulator word
         auto out_value = [&](uint32_t acc) {
-            return kNv ? __fmul_rn(__uint_as_float(acc), args.alpha) : __uint_as_float(acc);
+            return kNv ? __fmul_rn(__uint_as_float(acc), alpha_a) : __uint_as_float(acc);
+        };
+        // L1's h = bf16(silu(bf16(g)) * bf16(u)) from the gate and up accumulator words
+        auto h_value = [&](uint32_t acc_g, uint32_t acc_u) {
+            const float g = round_bf16(kNv ? __fmul_rn(__uint_as_float(acc_g), alpha_a) : __uint_as_float(acc_g));
+            const float u = round_bf16(kNv ? __fmul_rn(__uint_as_float(acc_u), alpha_b) : __uint_as_float(acc_u));
+            return round_bf16(silu_f32(g) * u);
+        };
+        // Re-quantisation of 32 columns of h: 16 code bytes; the scale byte (MXFP4) or the two
+        // E4M3 bytes of the two 16-column blocks, low byte first (NVFP4)
+        auto requant32 = [&](const float (&h)[32], uint4& cd) -> uint32_t {
+            if constexpr (kNv) {
+                uint2 c0, c1;
+                const uint32_t s0 = nv_quant16(h, q_g, q_r, c0);
+                const uint32_t s1 = nv_quant16(h + 16, q_g, q_r, c1);
+                cd = make_uint4(c0.x, c0.y, c1.x, c1.y);
+                return s0 | (s1 << 8);
+            } else {
+                return mx_quant32(h, cd);
+            }
         };
         uint32_t tc = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x, ++tc) {
             const Tile t = get_tile(args, w / args.n_tiles);
             const int nt = w % args.n_tiles;
+            if (kNv) {
+                alpha_a = alpha_b = args.alpha;
+                if (args.w_global != nullptr) {
+                    alpha_a = __fmul_rn(args.alpha, args.w_global[kL1 ? 2 * t.expert : t.expert]);
+                    alpha_b = kL1 ? __fmul_rn(args.alpha, args.w_global[2 * t.expert + 1]) : alpha_a;
+                }
+            }
             if (!warp_wait(smem_u32(&ctl->tmem_full), tc & 1u, abort_flag, args.status, kErrWaitTmemFull)) break;
             tc_fence_after();
             // Warp (q, hf) owns rows 32 q..32 q + 31 and half hf of the tile's columns. L1: kHB
@@ -538,12 +576,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int b = 0; b < kHB; ++b) {
                     float h[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float g = round_bf16(__uint_as_float(v[b][i]));
-                        const float u = round_bf16(__uint_as_float(v[2 + b][i]));
-                        h[i] = round_bf16(silu_f32(g) * u);
-                    }
-                    es[b] = mx_quant32(h, cds[b]);
+                    for (int i = 0; i < 32; ++i) h[i] = h_value(v[b][i], v[2 + b][i]);
+                    es[b] = requant32(h, cds[b]);
                 }
                 if (lane == 0) bulk_wait_read();   // the previous store has read the block
                 __syncwarp();
@@ -556,7 +590,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tma_store_2d(&tmY, staging_s, (int32_t)(col0 / 2), (int32_t)(t.row0 + 32 * q));
                     bulk_commit();
                 }
-                if (kHB == 2)
+                if (kNv)      // four E4M3 bytes: 64 columns of h, 16 per byte
+                    *reinterpret_cast<uint32_t*>(args.hs + grow * args.ld_hs + col0 / 16) =
+                        es[0] | (es[kHB - 1] << 16);
+                else if (kHB == 2)
                     *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col0 / 32) =
                         (uint16_t)(es[0] | (es[kHB - 1] << 8));
                 else
@@ -570,16 +607,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int b = 0; b < kHB; ++b) {
                     float h[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float g = round_bf16(__uint_as_float(v[b][i]));
-                        const float u = round_bf16(__uint_as_float(v[2 + b][i]));
-                        h[i] = round_bf16(silu_f32(g) * u);
-                    }
+                    for (int i = 0; i < 32; ++i) h[i] = h_value(v[b][i], v[2 + b][i]);
                     uint4 codes;
-                    const uint32_t E = mx_quant32(h, codes);
+                    const uint32_t E = requant32(h, codes);
                     const int64_t col = (int64_t)nt * (kN / 2) + (kN / 4) * hf + 32 * b;   // column of h
                     *reinterpret_cast<uint4*>(args.hq + grow * args.ld_hq + col / 2) = codes;
-                    args.hs[grow * args.ld_hs + col / 32] = (uint8_t)E;
+                    if (kNv)
+                        *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col / 16) = (uint16_t)E;
+                    else
+                        args.hs[grow * args.ld_hs + col / 32] = (uint8_t)E;
                 }
             } else {
 #pragma unroll
@@ -657,6 +693,11 @@ cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const C
 cudaError_t launch_gemm_nvfp4(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                               int grid, cudaStream_t s) {
     return launch<false, true, 256, true>(ta, tb, ty, a, grid, s);
+}
+
+cudaError_t launch_gemm_nvfp4_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
+                                 const GemmArgs& a, int grid, cudaStream_t s) {
+    return launch<true, true, 256, true>(ta, tb, ty, a, grid, s);
 }
 
 }  // namespace mx

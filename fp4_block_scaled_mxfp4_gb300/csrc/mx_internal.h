@@ -62,12 +62,18 @@ struct GemmArgs {
     int64_t n_valid;             // L1: I; L2: N (columns that exist)
     // outputs
     uint8_t* hq;                 // L1: requantised activation codes [rows, I/2]
-    uint8_t* hs;                 // L1: its scales [rows, I/32]
+    uint8_t* hs;                 // L1: its scales [rows, I/32] (NVFP4: [rows, I/16])
     int64_t ld_hq, ld_hs;
     uint16_t* y;                 // L2: BF16 output [rows, ld_y]
     int64_t ld_y;
     uint32_t* status;            // device status word
-    float alpha;                 // NVFP4: the product of the two global scales
+    // NVFP4 only. Without w_global the output is scaled by alpha (the product of the two
+    // operands' globals). With it, alpha is the activation's global and each expert's
+    // weight global(s) multiply it in the kernel: L1 w_global[2e] (gate), [2e + 1] (up);
+    // L2 w_global[e]. q_global is the global of L1's NVFP4 re-quantisation of h.
+    float alpha;
+    const float* w_global;
+    float q_global;
 };
 
 size_t gemm_smem_bytes();
@@ -81,11 +87,14 @@ cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const C
 cudaError_t launch_gemm_l2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                            int grid, bool b_tiled, int n_cols, cudaStream_t s);
 
-// NVFP4 one-group GEMM, BF16 out (times a.alpha): A codes with row-major E4M3 scales per 16
-// (a.sfa, ld_sf = K/16), B codes with E4M3 scales in the tile layout (a.sfb, kw = K/64);
-// tb in boxes of 256 rows; K % 256 == 0.
+// NVFP4 GEMMs (256-column tiles): A codes with row-major E4M3 scales per 16 (a.sfa,
+// ld_sf = K/16), B codes with E4M3 scales in the tile layout (a.sfb, kw = K/64); tb in
+// boxes of 256 rows (L1: the 4-D w13 view, 128 rows of each half); K % 128 == 0. L2: BF16
+// out; L1: SiLU(gate) * up re-quantised to NVFP4 with a.q_global (scales [rows, I/16]).
 cudaError_t launch_gemm_nvfp4(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
                               int grid, cudaStream_t s);
+cudaError_t launch_gemm_nvfp4_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
+                                 const GemmArgs& a, int grid, cudaStream_t s);
 
 // ---- element-wise kernels ----
 // Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][512 B] (kb % 4 == 0).
@@ -99,6 +108,9 @@ cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* ou
                                int64_t cols, int num_sms, cudaStream_t s);
 cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
                              int num_sms, cudaStream_t s);
+// NVFP4 activation quantisation with the float32 global (codes [M, K/2], E4M3 sf [M, K/16]).
+cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M,
+                                   int64_t K, int num_sms, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,
                            int64_t T, int64_t K, int64_t H, int num_sms, cudaStream_t s);
 
@@ -118,10 +130,10 @@ struct RouteBufs {
 };
 cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, const RouteBufs& rb,
                          cudaStream_t s);
-// Quantise each token row once and write it to the rows of all its routed pairs; also
-// writes row_of (needs launch_route first).
+// Quantise each token row once (MXFP4, or NVFP4 with the float32 global) and write it to the
+// rows of all its routed pairs; also writes row_of (needs launch_route first).
 cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,
                                 int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs,
-                                cudaStream_t s);
+                                cudaStream_t s, bool nvfp4 = false, float global_scale = 0.0f);
 
 }  // namespace mx

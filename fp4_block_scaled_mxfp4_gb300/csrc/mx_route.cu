@@ -10,6 +10,8 @@
 //      128-row M tiles (expert, first row, valid rows) that the grouped GEMMs walk;
 //   3. quant_gather: row_of[t, k] = offsets[e] + chunk_base[chunk, e] + rank, and the MX
 //      quantisation of each token row written once per routed pair into the grouped rows.
+#include <type_traits>
+
 #include "mx_device.cuh"
 #include "mx_internal.h"
 
@@ -106,12 +108,16 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
 
 constexpr int kGatherThreads = 256;
 
-// One thread per 32-element MX block of the token's row: four 16-byte loads, one
-// quantisation, then per routed copy of the row a 16-byte code store and a scale byte, so a
-// warp writes 512 contiguous code bytes and 32 contiguous scale bytes per destination row.
+// One thread per block of the token's row -- MXFP4: 32 elements, four 16-byte loads, a
+// 16-byte code store; NVFP4 (kNv, global g): 16 elements, two loads, an 8-byte store --
+// then per routed copy of the row the codes and a scale byte, so a warp writes 512 (256)
+// contiguous code bytes and 32 contiguous scale bytes per destination row.
+template <bool kNv>
 __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
     const uint4* __restrict__ x8, const int32_t* __restrict__ ids, int K, int E, int64_t blocks_per_row,
-    RouteBufs rb, uint4* __restrict__ xq16, uint8_t* __restrict__ xs) {
+    RouteBufs rb, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, float g) {
+    using Codes = typename std::conditional<kNv, uint2, uint4>::type;
+    constexpr int kLoads = kNv ? 2 : 4;
     __shared__ int32_t s_rows[kMaxTopK];
     pdl_wait();
     const int64_t t = blockIdx.x;
@@ -126,12 +132,14 @@ __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
         rb.row_of[p] = row;
     }
     __syncthreads();
-    const uint4* xrow = x8 + t * blocks_per_row * 4;
+    const uint4* xrow = x8 + t * blocks_per_row * kLoads;
+    Codes* xqc = reinterpret_cast<Codes*>(xq);
+    const float r = kNv ? __frcp_rn(__fmul_rn(6.0f, g)) : 0.0f;
     for (int64_t b = tid; b < blocks_per_row; b += kGatherThreads) {
-        float f[32];
+        float f[8 * kLoads];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 v = __ldg(xrow + 4 * b + i);
+        for (int i = 0; i < kLoads; ++i) {
+            const uint4 v = __ldg(xrow + kLoads * b + i);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -139,13 +147,17 @@ __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
                 f[8 * i + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
             }
         }
-        uint4 codes;
-        const uint32_t e8 = mx_quant32(f, codes);
+        Codes codes;
+        uint32_t sb;
+        if constexpr (kNv)
+            sb = nv_quant16(f, g, r, codes);
+        else
+            sb = mx_quant32(f, codes);
         for (int k = 0; k < K; ++k) {
-            const int32_t r = s_rows[k];
-            if (r < 0) continue;
-            xq16[(int64_t)r * blocks_per_row + b] = codes;
-            xs[(int64_t)r * blocks_per_row + b] = (uint8_t)e8;
+            const int32_t row = s_rows[k];
+            if (row < 0) continue;
+            xqc[(int64_t)row * blocks_per_row + b] = codes;
+            xs[(int64_t)row * blocks_per_row + b] = (uint8_t)sb;
         }
     }
     pdl_launch_dependents();
@@ -164,11 +176,15 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, co
 }
 
 cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,
-                                int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs, cudaStream_t s) {
+                                int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs, cudaStream_t s,
+                                bool nvfp4, float global_scale) {
     if (T == 0) return cudaSuccess;
-    return launch_pdl(quant_gather_kernel, dim3((unsigned)T), dim3(kGatherThreads), 0, s,
-                      reinterpret_cast<const uint4*>(x), ids, (int)K, (int)E, (int64_t)(H / 32), rb,
-                      reinterpret_cast<uint4*>(xq), xs);
+    if (nvfp4)
+        return launch_pdl(quant_gather_kernel<true>, dim3((unsigned)T), dim3(kGatherThreads), 0, s,
+                          reinterpret_cast<const uint4*>(x), ids, (int)K, (int)E, (int64_t)(H / 16), rb, xq, xs,
+                          global_scale);
+    return launch_pdl(quant_gather_kernel<false>, dim3((unsigned)T), dim3(kGatherThreads), 0, s,
+                      reinterpret_cast<const uint4*>(x), ids, (int)K, (int)E, (int64_t)(H / 32), rb, xq, xs, 0.0f);
 }
 
 }  // namespace mx

@@ -14,6 +14,9 @@
  *          cudagraph-safe with pre-allocated buffers).
  *   [BF16] same page -- "Phase 3: Clean up" (BF16 only for the SiLU activation and the
  *          final scatter).
+ *   [GS]   same page -- "Phase 1: CuTeDSL Shared Expert Kernel" (warm-up-based activation
+ *          global scale "gs") and "Phase 2: CuTeDSL Attention Kernel" (a per-tensor weight
+ *          global scale; the MoE's gate and up carry different ones).
  *
  * Conventions for every call below:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library allocates no
@@ -114,7 +117,7 @@ int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t
  *   The tensor cores read the scale bytes as unsigned E4M3: every scale byte of A and B
  *   must lie in 0x00..0x7E (sign bit clear, not NaN). The library cannot check device
  *   data; a byte outside that range gives a result other than the signed-E4M3 reading.
- *   K must be a positive multiple of 256, N a positive multiple of 16; M >= 0.
+ *   K must be a positive multiple of 128, N a positive multiple of 16; M >= 0.
  */
 int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b,
                     const uint8_t* sb_tiled, float b_global, void* d_bf16, int64_t M, int64_t N,
@@ -140,6 +143,22 @@ int fp8_block_dequant_128x128(const uint8_t* q_e4m3, const uint8_t* sf, void* ou
  *   K must be a positive multiple of 32.
  */
 int act_quant_mxfp4(const void* x_bf16, uint8_t* codes, uint8_t* sf,
+                    int64_t M, int64_t K, mx_stream_t stream);
+
+/*
+ * act_quant_nvfp4 -- BF16 -> NVFP4 activation quantisation against a float32 global scale g
+ * fixed by the caller (calibrated at warm-up, [GS]); the published NVFP4 encoder, which the
+ * pages name but do not print. Per row and 16-column block, each step one float32 operation
+ * rounded to nearest even:
+ *   r = 1 / (6 g); S = the E4M3 byte nearest min(amax * r, 448) (ties to even);
+ *   code = E2M1 nearest x * (1 / (e4m3(S) * g)), saturating at +-6, sign kept.
+ *   S = 0 gives the codes +-0; a block holding NaN/Inf gets S = 0x7F and codes sign|7.
+ *   x uint16 [M, K] (16-byte aligned), codes uint8 [M, K/2] (8-byte aligned), sf uint8
+ *   [M, K/16]. The dequantised value is LUT[code] * e4m3(S) * g (nvfp4_dequant).
+ *   K must be a positive multiple of 16; g must lie in [2^-117, 2^100] (MX_ERR_INVALID_ARG
+ *   otherwise), which keeps every intermediate a normal float.
+ */
+int act_quant_nvfp4(const void* x_bf16, float global_scale, uint8_t* codes, uint8_t* sf,
                     int64_t M, int64_t K, mx_stream_t stream);
 
 /*
@@ -254,6 +273,50 @@ int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float*
 int moe_mxfp4_route(const int32_t* topk_ids, int64_t T, int64_t K, int64_t E,
                     int32_t* counts, int32_t* offsets, int32_t* row_of,
                     void* workspace, size_t ws_bytes, mx_stream_t stream);
+
+/*
+ * moe_nvfp4_forward -- the MoE expert FFN of moe_mxfp4_forward with NVFP4 weights and
+ * activations (kind::mxf4nvf4 tensor-core MMAs, E4M3 scales per 16 elements):
+ *   xq = act_quant_nvfp4(x, x_global);
+ *   for each routed pair (t, k) with e = topk_ids[t, k] in [0, E):
+ *     g = bf16( (xq[t] . w13[e][0:I]^T) * x_global * g13[e][0] )    (gate global)
+ *     u = bf16( (xq[t] . w13[e][I:2I]^T) * x_global * g13[e][1] )   (up global, [GS])
+ *     h = bf16( silu(g) * u ),  hq = act_quant_nvfp4(h, h_global)    (fused epilogue)
+ *     y = bf16( (hq . w2[e]^T) * h_global * g2[e] )
+ *   out[t] = bf16( sum_k topk_w[t, k] * y(t, k) )   (float32, slot order)
+ *   Dot products use the codes times their E4M3 scales (globals excluded), accumulate in
+ *   float32 and are scaled once by the float32 product of the two globals.
+ *   Routing, shared-expert mode (topk_ids == topk_w == NULL, E == 1), sizes and workspace
+ *   rules as moe_mxfp4_forward, with the workspace of moe_nvfp4_workspace_size.
+ *   w13 uint8 [E, 2I, H/2] with s13_tiled = nvfp4_scales_to_tiled of its E4M3 scales viewed
+ *   as [E*2I, H/16]; w2 uint8 [E, H, I/2] with s2_tiled from [E*H, I/16]; g13 float32
+ *   [E, 2] (gate, up) and g2 float32 [E], device arrays; x_global, h_global as for
+ *   act_quant_nvfp4 (MX_ERR_INVALID_ARG outside [2^-117, 2^100]). Weight scale bytes must
+ *   lie in 0x00..0x7E (nvfp4_gemm_bf16); the library does not read device data to check.
+ */
+int moe_nvfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_w,
+                      const uint8_t* w13, const uint8_t* s13_tiled, const float* g13,
+                      const uint8_t* w2, const uint8_t* s2_tiled, const float* g2,
+                      float x_global, float h_global, void* out, int64_t T, int64_t H,
+                      int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                      mx_stream_t stream);
+
+/* moe_nvfp4_forward recording the six phase events of moe_mxfp4_forward_timed. */
+int moe_nvfp4_forward_timed(const void* x, const int32_t* topk_ids, const float* topk_w,
+                            const uint8_t* w13, const uint8_t* s13_tiled, const float* g13,
+                            const uint8_t* w2, const uint8_t* s2_tiled, const float* g2,
+                            float x_global, float h_global, void* out, int64_t T, int64_t H,
+                            int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                            mx_stream_t stream, void* const* events);
+
+/*
+ * moe_nvfp4_workspace_size / moe_nvfp4_workspace_layout -- as the moe_mxfp4_ pair, for
+ * moe_nvfp4_forward: xs [R, H/16] and hs [R, I/16] hold E4M3 scales (one per 16 columns).
+ */
+size_t moe_nvfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K,
+                                int routed);
+int moe_nvfp4_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed,
+                               int64_t* out);
 
 /* Bytes of the static device scratch area moe_mxfp4_forward_noalloc runs on (per device). */
 #define MXFP4MOE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

@@ -1,4 +1,4 @@
-"""Step-by-step parity of a moe_mxfp4_forward run against the oracle.
+"""Step-by-step parity of a moe_mxfp4_forward (or moe_nvfp4_forward) run against the oracle.
 
 The forward leaves its intermediates in the workspace (moe_mxfp4_workspace_layout), so
 every step is checked where it happens:
@@ -149,6 +149,136 @@ def check_moe_run(mx, d, tokens=None) -> dict:
         stats = assert_moe_close(out_gpu, oracle.bf16_bits_from_f64(y_cond[:, 0]),
                                  "out vs oracle on the GPU's re-quant decisions")
     ref = oracle.moe_forward(inp.x, inp.topk_ids, inp.topk_w, inp.w13, inp.s13, inp.w2, inp.s2, I, tokens=tok)
+    cos = cosine(bits_to_f64(out_gpu), bits_to_f64(ref))
+    assert cos >= MOE_COS, f"cosine vs the unconditioned oracle {cos:.6f} < {MOE_COS}"
+    err = np.abs(bits_to_f64(out_gpu) - bits_to_f64(ref))
+    stats.update(requant_blocks=blocks, requant_blocks_differing=differ, e2e_cos=cos,
+                 e2e_max_err=float(err.max()), e2e_bound=float(2e-2 * np.abs(bits_to_f64(ref)).max() + 1e-3))
+    return stats
+
+
+# ----------------------------------------------------------------------------- NVFP4 forward
+
+def _nv_scale_bytes(amax, global_scale):
+    """The E4M3 scale byte the NVFP4 quantiser picks for a block maximum (its float32 steps)."""
+    f32 = np.float32
+    r = f32(1.0) / (f32(6.0) * f32(global_scale))
+    with np.errstate(over="ignore"):
+        t = np.minimum(np.asarray(amax).astype(np.float32) * r, f32(448.0))
+    return oracle.e4m3_round_code(t.astype(np.float64)).astype(np.int64)
+
+
+def check_nv_requant_decisions(g, u, absg, absu, hq_gpu, hs_gpu, h_global):
+    """Step 2 for NVFP4: every GPU block (E4M3 scale + 16 codes) must be the NVFP4
+    quantisation of some h' in the interval the float32 accumulation and SiLU allow around
+    the oracle's h. g, u, absg, absu already carry the global scales. Returns (blocks,
+    blocks differing from the oracle's own decision)."""
+    n, I = g.shape
+    to = oracle.bf16_bits_to_f64
+    fr = oracle.bf16_bits_from_f64
+    eg, eu = absg * ACC_ALLOW, absu * ACC_ALLOW
+    gs = [to(fr(g - eg)), to(fr(g + eg))]
+    us = [to(fr(u - eu)), to(fr(u + eu))]
+    with np.errstate(over="ignore"):
+        corners = np.stack([gg / (1.0 + np.exp(-gg)) * uu for gg in gs for uu in us])
+    lo = corners.min(0)
+    hi = corners.max(0)
+    lo = lo - np.abs(lo) * SILU_ALLOW
+    hi = hi + np.abs(hi) * SILU_ALLOW
+    h_lo, h_hi = to(fr(lo)), to(fr(hi))
+    mag_lo = np.where((h_lo <= 0) & (h_hi >= 0), 0.0, np.minimum(np.abs(h_lo), np.abs(h_hi)))
+    mag_hi = np.maximum(np.abs(h_lo), np.abs(h_hi))
+    nb = I // 16
+    S_lo = _nv_scale_bytes(mag_lo.reshape(n, nb, 16).max(-1), h_global)
+    S_hi = _nv_scale_bytes(mag_hi.reshape(n, nb, 16).max(-1), h_global)
+    hs = hs_gpu.astype(np.int64)
+    bad_scale = (hs < S_lo) | (hs > S_hi) | (hs >= 0x7F)
+    assert not bad_scale.any(), (f"NVFP4 re-quant scale outside the admissible range at "
+                                 f"{np.argwhere(bad_scale)[0].tolist()}")
+    f32 = np.float32
+    d = oracle.e4m3fn_decode(hs).astype(np.float32) * f32(h_global)
+    with np.errstate(divide="ignore"):
+        rd = np.repeat(f32(1.0) / d, 16, axis=1)
+    zero = np.repeat(hs == 0, 16, axis=1)
+    nib = oracle.unpack_nibbles(hq_gpu)
+    v_gpu = _signed_code_value(nib & 7, (nib >> 3).astype(bool))
+
+    def qv(h):
+        with np.errstate(over="ignore", invalid="ignore"):
+            s = h.astype(np.float32) * np.where(zero, f32(0.0), rd)
+        s = s.astype(np.float64)
+        return _signed_code_value(_e2m1_round_magnitude(np.minimum(np.abs(s), 6.0)), np.signbit(s))
+
+    v_lo, v_hi = qv(h_lo), qv(h_hi)
+    bad = (v_gpu < np.minimum(v_lo, v_hi)) | (v_gpu > np.maximum(v_lo, v_hi)) | (zero & (v_gpu != 0))
+    assert not bad.any(), (f"NVFP4 re-quant code outside the admissible range at {np.argwhere(bad)[0].tolist()}: "
+                           f"gpu {v_gpu[bad][0]}, admissible [{v_lo[bad][0]}, {v_hi[bad][0]}]")
+    ref_q, ref_s = oracle.nvfp4_quantize(oracle.swiglu_bf16(g, u), h_global)
+    differ = (ref_s != hs_gpu) | (oracle.unpack_nibbles(ref_q).reshape(n, nb, 16) !=
+                                  nib.reshape(n, nb, 16)).any(-1)
+    return n * nb, int(differ.sum())
+
+
+def check_nvfp4_moe_run(mx, d, tokens=None) -> dict:
+    """check_moe_run for a finished moe_nvfp4_forward (d holds an NvMoEInputs)."""
+    inp = d.inp
+    T, H, I, E, K = inp.T, inp.H, inp.I, inp.E, inp.K
+    routed = inp.topk_ids is not None
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    L = mx.moe_nvfp4_workspace_layout(T, H, I, E, K, routed)
+    R = T * K if routed else T
+    out_gpu = bf16_host(d.out)[tok]
+    ids = inp.topk_ids[tok].astype(np.int64) if routed else np.zeros((tok.size, 1), np.int64)
+    row_of = _ws_view(d.ws, L["row_of"], T, K, "i32")[tok] if routed else tok[:, None]
+    gx, gh = float(np.float32(inp.x_global)), float(np.float32(inp.h_global))
+
+    # 1. first quantisation, bit-exact
+    xq_ref, xs_ref = oracle.nvfp4_quantize(inp.x[tok], inp.x_global)
+    xq_all = _ws_view(d.ws, L["xq"], R, H // 2)
+    xs_all = _ws_view(d.ws, L["xs"], R, H // 16)
+    hq_all = _ws_view(d.ws, L["hq"], R, I // 2)
+    hs_all = _ws_view(d.ws, L["hs"], R, I // 16)
+    y_all = _ws_view(d.ws, L["y"], R, H, "bf16") if routed else None
+    for j in range(ids.shape[1]):
+        live = (ids[:, j] >= 0) & (ids[:, j] < E)
+        rows = row_of[live, j]
+        np.testing.assert_array_equal(xq_all[rows], xq_ref[live], err_msg="xq")
+        np.testing.assert_array_equal(xs_all[rows], xs_ref[live], err_msg="xs")
+    xv = oracle.nvfp4_values(xq_ref, xs_ref, 1.0)
+
+    blocks = differ = 0
+    y_cond = np.zeros((tok.size, ids.shape[1], H))
+    for e in range(E):
+        sel = np.argwhere(ids == e)
+        if sel.size == 0:
+            continue
+        i_s, k_s = sel[:, 0], sel[:, 1]
+        rows = row_of[i_s, k_s]
+        W13 = oracle.nvfp4_values(inp.w13[e], inp.s13[e], 1.0)
+        gu = xv[i_s] @ W13.T
+        agu = np.abs(xv[i_s]) @ np.abs(W13).T
+        del W13
+        ag, au = gx * float(inp.g13[e, 0]), gx * float(inp.g13[e, 1])
+        b, dff = check_nv_requant_decisions(gu[:, :I] * ag, gu[:, I:] * au, agu[:, :I] * abs(ag),
+                                            agu[:, I:] * abs(au), hq_all[rows], hs_all[rows], gh)
+        blocks += b
+        differ += dff
+        # 3. L2 on the GPU's own decisions
+        W2 = oracle.nvfp4_values(inp.w2[e], inp.s2[e], 1.0)
+        hv = oracle.nvfp4_values(hq_all[rows], hs_all[rows], 1.0)
+        a2 = gh * float(inp.g2[e])
+        exact = (hv @ W2.T) * a2
+        if routed:
+            assert_gemm_close(y_all[rows], exact, (np.abs(hv) @ np.abs(W2).T) * abs(a2), f"L2 expert {e}")
+        y_cond[i_s, k_s] = oracle.bf16_bits_to_f64(oracle.bf16_bits_from_f64(exact))
+    # 4. output against the oracle on the same decisions, and against the plain oracle
+    if routed:
+        ref_cond = oracle.moe_combine(y_cond, ids, inp.topk_w[tok], E)
+    else:
+        ref_cond = oracle.bf16_bits_from_f64(y_cond[:, 0])
+    stats = assert_moe_close(out_gpu, ref_cond, "out vs oracle on the GPU's re-quant decisions")
+    ref = oracle.moe_nvfp4_forward(inp.x, inp.topk_ids, inp.topk_w, inp.w13, inp.s13, inp.g13, inp.w2, inp.s2,
+                                   inp.g2, inp.x_global, inp.h_global, I, tokens=tok)
     cos = cosine(bits_to_f64(out_gpu), bits_to_f64(ref))
     assert cos >= MOE_COS, f"cosine vs the unconditioned oracle {cos:.6f} < {MOE_COS}"
     err = np.abs(bits_to_f64(out_gpu) - bits_to_f64(ref))

@@ -90,7 +90,7 @@ def test_gemm_validation(lib):
     assert lib.mxfp4_gemm_bf16(FAKE, FAKE, None, FAKE, FAKE, 4, 256, 256, None) == MX_ERR_INVALID_ARG
     assert lib.mxfp4_gemm_bf16(FAKE, ODD, FAKE, FAKE, FAKE, 4, 256, 256, None) == MX_ERR_MISALIGNED
     # NVFP4: every call below is rejected (or has M == 0) before anything launches
-    assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, 4, 256, 128, None) == MX_ERR_UNSUPPORTED  # K % 256
+    assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, 4, 256, 192, None) == MX_ERR_UNSUPPORTED  # K % 128
     assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, 4, 250, 256, None) == MX_ERR_UNSUPPORTED
     assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, 0, 256, 256, None) == MX_OK
     assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, None, FAKE, 1.0, FAKE, 4, 256, 256, None) == MX_ERR_INVALID_ARG
@@ -152,3 +152,40 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _native.lib()
+
+
+def test_nvfp4_quant_and_forward_validation(lib):
+    """Every call is rejected (or has nothing to do) before anything launches."""
+    assert lib.act_quant_nvfp4(FAKE, 1.0, FAKE, FAKE, 4, 40, None) == MX_ERR_UNSUPPORTED       # K % 16
+    assert lib.act_quant_nvfp4(FAKE, 0.0, FAKE, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG       # global 0
+    assert lib.act_quant_nvfp4(FAKE, float("nan"), FAKE, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
+    assert lib.act_quant_nvfp4(FAKE, 2.0 ** -120, FAKE, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
+    assert lib.act_quant_nvfp4(FAKE, 2.0 ** 101, FAKE, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
+    assert lib.act_quant_nvfp4(FAKE, 1.0, None, FAKE, 4, 64, None) == MX_ERR_INVALID_ARG
+    assert lib.act_quant_nvfp4(FAKE, 1.0, FAKE + 4, FAKE, 4, 64, None) == MX_ERR_MISALIGNED   # codes 8-byte
+    assert lib.act_quant_nvfp4(FAKE, 1.0, FAKE, FAKE, 0, 64, None) == MX_OK
+
+    def fwd(ids=FAKE, w=FAKE, g13=FAKE, g2=FAKE, gx=0.01, gh=0.25, T=16, H=256, I=128, E=4, K=2, ws=FAKE,
+            ws_bytes=None):
+        if ws_bytes is None:
+            ws_bytes = lib.moe_nvfp4_workspace_size(T, H, I, E, K, 1 if ids else 0)
+        return lib.moe_nvfp4_forward(FAKE, ids, w, FAKE, FAKE, g13, FAKE, FAKE, g2, gx, gh, FAKE, T, H, I, E, K,
+                                     ws, ws_bytes, None)
+
+    assert fwd(H=200) == MX_ERR_UNSUPPORTED
+    assert fwd(gx=0.0) == MX_ERR_INVALID_ARG
+    assert fwd(gh=float("inf")) == MX_ERR_INVALID_ARG
+    assert fwd(g13=None) == MX_ERR_INVALID_ARG
+    assert fwd(g2=None) == MX_ERR_INVALID_ARG
+    assert fwd(w=None) == MX_ERR_INVALID_ARG
+    assert fwd(ids=None, w=None, E=2) == MX_ERR_INVALID_ARG
+    assert fwd(T=0) == MX_OK
+    need = lib.moe_nvfp4_workspace_size(16, 256, 128, 4, 2, 1)
+    assert need > 0 and need < lib.moe_mxfp4_workspace_size(16, 256, 128, 4, 2, 1) + 4096
+    assert fwd(ws_bytes=need - 1) == MX_ERR_WORKSPACE
+    assert fwd(ws=FAKE + 128) == MX_ERR_MISALIGNED
+    # the scale regions hold one byte per 16 columns
+    buf = (ctypes.c_int64 * 8)()
+    assert lib.moe_nvfp4_workspace_layout(16, 256, 128, 4, 2, 1, ctypes.addressof(buf)) == MX_OK
+    xs, hq = buf[1], buf[2]
+    assert hq - xs >= 32 * (256 // 16)

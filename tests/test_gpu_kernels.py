@@ -258,7 +258,8 @@ def test_nvfp4_scales_to_tiled_bit_exact(mx):
 
 # NVFP4 scales are read as unsigned E4M3 by the tensor core: the inputs keep the sign bit clear.
 @pytest.mark.parametrize("M,N,K,ga,gb", [(128, 256, 256, 1.0, 1.0), (77, 272, 512, 0.0123, 2.5),
-                                         (300, 512, 1024, 3.0e-3, -0.7), (1000, 1024, 7168, 0.05, 0.02)])
+                                         (300, 512, 1024, 3.0e-3, -0.7), (1000, 1024, 7168, 0.05, 0.02),
+                                         (200, 512, 384, 0.01, 0.5), (64, 256, 128, 1.0, 1.0)])
 def test_nvfp4_gemm_random(mx, M, N, K, ga, gb):
     import torch
     rng = np.random.default_rng(M + N + K)
