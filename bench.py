@@ -542,6 +542,8 @@ def measure_nvfp4_forward(mx, torch, dev, stream, timeit):
     ws = torch.empty(mx.moe_nvfp4_workspace_size(c["T"], c["H"], c["I"], c["E"], c["K"], True), dtype=torch.uint8,
                      device=dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record(stream)              # create the underlying CUDA events
 
     def fwd(events=None):
         mx.moe_nvfp4_forward(x, ids, w, w13, s13t, g13, w2, s2t, g2, inp.x_global, inp.h_global, out, ws,
