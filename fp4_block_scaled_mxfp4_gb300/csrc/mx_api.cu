@@ -322,7 +322,7 @@ int mxfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t
 
 size_t nvfp4_tiled_scales_bytes(int64_t rows, int64_t cols) {
     if (rows < 0 || cols <= 0 || cols % 64) return 0;
-    return 4 * tiled_bytes(rows, cols / 16);          // every block four times (four lane quarters)
+    return tiled_bytes(rows, cols / 16);
 }
 
 int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t cols, mx_stream_t stream) {
@@ -332,7 +332,7 @@ int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t
     if (!sf || !out) return MX_ERR_INVALID_ARG;
     if (!aligned16(sf) || !aligned16(out)) return MX_ERR_MISALIGNED;
     if ((cols / 64 + 31) / 32 > 65535) return MX_ERR_UNSUPPORTED;
-    return cuda_status(launch_sf_tile(sf, out, rows, cols / 16, static_cast<cudaStream_t>(stream), 4));
+    return cuda_status(launch_sf_tile(sf, out, rows, cols / 16, static_cast<cudaStream_t>(stream)));
 }
 
 int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b, const uint8_t* sb_tiled,

@@ -406,12 +406,6 @@ __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-// Copy 128 rows x 128 bits (a plain [128][16 B] image, desc_sf) from shared memory into 128
-// lanes x 4 columns of tensor memory; no replication.
-__device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Copy 128 rows x 256 bits from shared memory into 128 lanes x 8 columns of tensor memory
 // (row r -> lane r, its eight 32-bit words -> eight columns); no replication.
 __device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {

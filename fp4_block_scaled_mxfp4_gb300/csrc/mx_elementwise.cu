@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restri
 constexpr int kTileThreads = 128;
 __global__ void __launch_bounds__(kTileThreads) sf_tile_kernel(const uint8_t* __restrict__ sf,
                                                                uint8_t* __restrict__ out, int64_t rows,
-                                                               int64_t kb, int rep) {
+                                                               int64_t kb) {
     __shared__ uint32_t s_rows[128][33];             // 128 rows x 32 words (+1 against conflicts)
     const int64_t g = blockIdx.x;                    // row group
     const int64_t wc = (int64_t)blockIdx.y * 32;     // first K-word of this chunk
@@ -356,21 +356,19 @@ __global__ void __launch_bounds__(kTileThreads) sf_tile_kernel(const uint8_t* __
     const uint32_t* src = reinterpret_cast<const uint32_t*>(sf + row * kb) + wc;
     for (int w = 0; w < nw; ++w) s_rows[t][w] = row < rows ? __ldg(src + w) : 0u;
     __syncthreads();
-    // block w holds rep copies of its 32 lanes x 16 bytes
-    uint4* o = reinterpret_cast<uint4*>(out + ((g * kw) + wc) * 512 * rep);
+    uint4* o = reinterpret_cast<uint4*>(out + ((g * kw) + wc) * 512);
     for (int u = t; u < nw * 32; u += kTileThreads) {
         const int w = u >> 5, l = u & 31;
-        const uint4 v = make_uint4(s_rows[l][w], s_rows[l + 32][w], s_rows[l + 64][w], s_rows[l + 96][w]);
-        for (int q = 0; q < rep; ++q) o[(w * rep + q) * 32 + l] = v;
+        o[u] = make_uint4(s_rows[l][w], s_rows[l + 32][w], s_rows[l + 64][w], s_rows[l + 96][w]);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s, int rep) {
+cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
     const dim3 grid((unsigned)((rows + 127) / 128), (unsigned)((kb / 4 + 31) / 32));
-    sf_tile_kernel<<<grid, kTileThreads, 0, s>>>(sf, out, rows, kb, rep);
+    sf_tile_kernel<<<grid, kTileThreads, 0, s>>>(sf, out, rows, kb);
     return cudaGetLastError();
 }
 

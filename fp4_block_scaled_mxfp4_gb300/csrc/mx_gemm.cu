@@ -81,11 +81,8 @@ constexpr int kMaxStages = 5;
 // CTAs, and fits a fifth stage.
 //
 // kNv: NVFP4 operands (E4M3 scales per 16 elements of K, idesc scale format E4M3): four
-// scale words per row and stage instead of two, so two A images, twice the TMEM columns per
-// slot, and three stages. Eight replicating copies of B's words would cost the tensor pipe
-// more than the stage's MMAs, so NVFP4 weight scales are stored with each 512-byte block
-// repeated for the four lane quarters (a 2 KB, 128-lane image) and reach tensor memory by
-// non-replicating 128x128b copies. The accumulator is scaled by
+// scale words per row and stage instead of two, so two A images, twice B's blocks and
+// copies, twice the TMEM columns per slot, and three stages. The accumulator is scaled by
 // the operands' global scales in the epilogue (L1: per expert, gate and up separately), and
 // L1 re-quantises h to NVFP4 (E4M3 per 16 against h's global).
 template <int kN, bool kNv = false>
@@ -95,8 +92,7 @@ struct Cfg {
     static constexpr int kWords = kNv ? 4 : 2;                      // scale words per row and stage
     static constexpr int kWordsHalf = kWords / 2;                   // ... at a K tail of 128
     static constexpr int kSfaBytes = (kWords / 2) * 4096;           // wide images of two words each
-    static constexpr int kSfbBlock = kNv ? 2048 : 512;             // one K-word of 128 rows
-    static constexpr int kSfbBytes = (kN / 128) * kWords * kSfbBlock;
+    static constexpr int kSfbBytes = (kN / 128) * kWords * 512;     // per 128 rows: kWords x 512 B
     static constexpr int kSfCols = kNv ? 48 : kSfColsPerStage;      // A: 4 per word; B: 8 per word
     static constexpr uint32_t kIdesc = kNv ? (idesc_mxf4(kBM, kN) & ~(1u << 23)) : idesc_mxf4(kBM, kN);
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
@@ -141,8 +137,6 @@ template <int kN, bool kNv = false>
 constexpr size_t smem_bytes() {
     return (size_t)Cfg<kN, kNv>::kStagingOff + 8 * kStagingBytes + sizeof(Ctl) + 1024;
 }
-static_assert(smem_bytes<256, true>() <= 232448 && smem_bytes<256>() <= 232448 && smem_bytes<128>() <= 232448,
-              "dynamic shared memory above the 227 KB a CTA may use");
 
 struct Tile {
     int32_t expert;
@@ -358,7 +352,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // B scales: the stage's kWords K-words of each 128-row group (half of them at
                     // the K tail); each 128-row half of the tile is one whole group of the tile
                     // layout
-                    const uint32_t sf_bytes = (uint32_t)((half ? C::kWordsHalf : C::kWords) * C::kSfbBlock);
+                    const uint32_t sf_bytes = (uint32_t)((half ? C::kWordsHalf : C::kWords) * 512);
                     const uint32_t bar = smem_u32(&ctl->sf_full[s]);
                     int64_t grp[2];
                     uint32_t tx = 0;
@@ -369,8 +363,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive_expect_tx(bar, tx);
                     for (int h = 0; h < 2; ++h)
                         if (grp[h] < args.b_groups)
-                            bulk_load(st + kABytes + kBBytes + kSfaBytes + h * (C::kWords * C::kSfbBlock),
-                                      args.sfb + (grp[h] * args.kw + C::kWords * kt) * C::kSfbBlock, sf_bytes, bar);
+                            bulk_load(st + kABytes + kBBytes + kSfaBytes + h * (C::kWords * 512),
+                                      args.sfb + (grp[h] * args.kw + C::kWords * kt) * 512, sf_bytes, bar);
                 }
                 if (kBTiled && kN == 128) {
                     // B scales in tile layout for a 128-row tile of two 64-row pieces (L1) that
@@ -459,11 +453,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int i = 0; i < C::kWords / 2; ++i)                                   // A, two K-words each
                         tc_cp_128x256b(sfa_t + 8 * i, desc_sf_wide(sfa_s + 4096 * i));
                     for (int wd = 0; wd < nwords; ++wd) {
-                        if constexpr (kNv) {                                                    // images
-                            tc_cp_128x128b(sfb_t + 8 * wd, desc_sf(sfb_s + wd * C::kSfbBlock));
-                            tc_cp_128x128b(sfb_t + 8 * wd + 4, desc_sf(sfb_s + (C::kWords + wd) * C::kSfbBlock));
-                            continue;
-                        }
                         tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 512));          // B rows 0-127
                         if (kN == 256)                                                          // 128-255
                             tc_cp_32x128b_x4(sfb_t + 8 * wd + 4, desc_sf(sfb_s + C::kWords * 512 + wd * 512));

@@ -41,8 +41,7 @@ constexpr int kMaxTopK = 64;
 struct GemmArgs {
     const uint8_t* sfa;          // A scales [a_rows, K/32]
     const uint8_t* sfb;          // B scales: row-major [b_rows, K/32], or tile layout
-                                 // [b_rows/128][K/128][512 B] (b_tiled launches; NVFP4:
-                                 // [b_rows/128][K/64][4 x 512 B])
+                                 // [b_rows/128][K/128][512 B] (b_tiled launches)
     int64_t ld_sf;               // K/32: scale bytes per row (A and B share K)
     int64_t a_rows;              // rows of A (bound for scale loads; TMA zero-fills beyond)
     int64_t b_rows;              // rows of the stacked B tensor
@@ -98,10 +97,8 @@ cudaError_t launch_gemm_nvfp4_l1(const CUtensorMap& ta, const CUtensorMap& tb, c
                                  const GemmArgs& a, int grid, cudaStream_t s);
 
 // ---- element-wise kernels ----
-// Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][rep][512 B] (kb % 4 == 0):
-// rep = 1 for MXFP4; NVFP4 weights keep rep = 4 copies of each block, the 128-lane image a
-// non-replicating tcgen05.cp reads.
-cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s, int rep = 1);
+// Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][512 B] (kb % 4 == 0).
+cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s);
 cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* sf, uint16_t* out, int64_t rows,
                                  int64_t cols, int num_sms, cudaStream_t s);
 // NVFP4 codes [rows, cols/2] + E4M3 scales [rows, cols/16] + float32 global -> BF16.

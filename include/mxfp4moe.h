@@ -99,9 +99,7 @@ int nvfp4_dequant(const uint8_t* codes, const uint8_t* sf_e4m3, float global_sca
 /*
  * nvfp4_tiled_scales_bytes / nvfp4_scales_to_tiled -- the tile layout above for an NVFP4
  * scale tensor sf uint8 [rows, cols/16] (E4M3 bytes, one per 16 columns): its 4-byte
- * words (four scales, 64 columns) take the place of the MXFP4 K-words, and each 512-byte
- * block is stored four times in a row (2 KB per block: the 128-lane image the GEMM copies
- * into tensor memory without replicating it). cols % 64 == 0.
+ * words (four scales, 64 columns) take the place of the MXFP4 K-words. cols % 64 == 0.
  */
 size_t nvfp4_tiled_scales_bytes(int64_t rows, int64_t cols);
 int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t cols,

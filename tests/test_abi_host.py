@@ -95,7 +95,7 @@ def test_gemm_validation(lib):
     assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, 0, 256, 256, None) == MX_OK
     assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, None, FAKE, 1.0, FAKE, 4, 256, 256, None) == MX_ERR_INVALID_ARG
     assert lib.nvfp4_gemm_bf16(FAKE, FAKE, 1.0, FAKE, ODD, 1.0, FAKE, 4, 256, 256, None) == MX_ERR_MISALIGNED
-    assert lib.nvfp4_tiled_scales_bytes(300, 7168) == 3 * 112 * 4 * 512      # four copies of each block
+    assert lib.nvfp4_tiled_scales_bytes(300, 7168) == 3 * 112 * 512
     assert lib.nvfp4_tiled_scales_bytes(300, 7200) == 0
     assert lib.nvfp4_scales_to_tiled(FAKE, FAKE, 4, 96, None) == MX_ERR_UNSUPPORTED
     assert lib.nvfp4_scales_to_tiled(ODD, FAKE, 4, 128, None) == MX_ERR_MISALIGNED
