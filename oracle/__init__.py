@@ -29,6 +29,7 @@ from .mxfp4_oracle import (  # noqa: F401
     nvfp4_dequant,
     nvfp4_gemm_bf16,
     nvfp4_gemm_f64,
+    nvfp4_gemm_segments_bf16,
     nvfp4_quantize,
     nvfp4_values,
     unpack_nibbles,

@@ -80,6 +80,9 @@ R16 The NVFP4 MoE forward is the MXFP4 one (R1, R3-R5) with NVFP4 in every quant
     w2 one; L1's g = bf16(sum * g_x * g_gate) and u = bf16(sum * g_x * g_up), L2's
     y = bf16(sum * g_h * g_w2), each product of two float32 globals exact in float64 and
     applied once to the exact sum (R14).
+R17 A fused projection (the pages' q_a + kv weights stacked along N, each with its own
+    weight_scale_2, [GS]) is one NVFP4 GEMM over the stacked B whose output columns of
+    segment s are scaled by a_global * b_global[s] (R14 per segment).
 
 Parity status: every function below is pinned by the ``-m "not gpu"`` tests (tables from
 the OCP MX definitions and torch's float8 conversions, one-hot nibble/scale tests, the
@@ -96,7 +99,7 @@ __all__ = [
     "unpack_nibbles", "mxfp4_values", "mxfp4_dequant", "fp8_block_dequant_128x128",
     "act_quant_mxfp4", "mxfp4_gemm_bf16", "mxfp4_gemm_blockint", "moe_route", "moe_forward",
     "nvfp4_values", "nvfp4_dequant", "nvfp4_gemm_f64", "nvfp4_gemm_bf16",
-    "e4m3_round_code", "nvfp4_quantize", "moe_nvfp4_forward",
+    "e4m3_round_code", "nvfp4_quantize", "moe_nvfp4_forward", "nvfp4_gemm_segments_bf16",
     "moe_flops_per_pair", "moe_l1_exact", "swiglu_bf16", "moe_l2_bf16", "moe_combine",
 ]
 
@@ -411,6 +414,19 @@ def nvfp4_gemm_bf16(a_codes, a_sf, a_global, b_codes, b_sf, b_global) -> np.ndar
     (the NVFP4 GEMM the pages plan for their attention projections, "Phase 2: CuTeDSL
     Attention Kernel", with one global scale per operand)."""
     return bf16_bits_from_f64(nvfp4_gemm_f64(a_codes, a_sf, a_global, b_codes, b_sf, b_global))
+
+
+def nvfp4_gemm_segments_bf16(a_codes, a_sf, a_global, b_codes, b_sf, b_globals, seg_rows) -> np.ndarray:
+    """Fused projection (R17): B [N, K] is several weight matrices stacked along N, segment s
+    holding seg_rows[s] rows with float32 global b_globals[s]; column n of segment s is
+    bf16(a_global * b_globals[s] * sum_k A[m, k] B[n, k]), the sum exact (R14)."""
+    seg_rows = [int(r) for r in seg_rows]
+    if sum(seg_rows) != np.asarray(b_codes).shape[0] or len(seg_rows) != len(b_globals):
+        raise ValueError("segments must cover B's rows, one global each")
+    S = nvfp4_values(a_codes, a_sf, 1.0) @ nvfp4_values(b_codes, b_sf, 1.0).T
+    g = np.repeat([float(np.float32(a_global)) * float(np.float32(gb)) for gb in b_globals], seg_rows)
+    with np.errstate(invalid="ignore", over="ignore"):
+        return bf16_bits_from_f64(S * g[None, :])
 
 
 def moe_flops_per_pair(H: int, I: int) -> int:

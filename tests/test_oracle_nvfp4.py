@@ -337,3 +337,40 @@ def test_moe_nvfp4_shared_equals_single_expert_routing():
     shared = _nv_forward(inp)
     routed = _nv_forward(inp, ids=np.zeros((5, 1), np.int32), w=np.ones((5, 1), np.float32))
     np.testing.assert_array_equal(shared, routed)
+
+
+# ----------------------------------------------------------------------------- fused projection (R17)
+
+def test_gemm_segments_brute_force_exact_rationals():
+    """Two stacked weight matrices with their own globals (q_a and kv of the pages' fused
+    projection): every output is the exact rational sum times a_global * b_global[segment],
+    rounded once; a segment boundary inside a 16-column block is allowed."""
+    from fractions import Fraction
+    rng = np.random.default_rng(27)
+    M, K = 3, 32
+    seg = [5, 3, 8]
+    N = sum(seg)
+    a = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x20, 0x50, size=(M, K // 16), dtype=np.uint8)
+    sb = rng.integers(0x20, 0x50, size=(N, K // 16), dtype=np.uint8)
+    ga, gbs = np.float32(0.0371), [np.float32(1.5e-3), np.float32(-2.0 ** -9), np.float32(7.25)]
+    got = oracle.bf16_bits_to_f64(oracle.nvfp4_gemm_segments_bf16(a, sa, ga, b, sb, gbs, seg))
+    bounds = np.cumsum([0] + seg)
+    for i in range(M):
+        for j in range(N):
+            s_idx = int(np.searchsorted(bounds, j, side="right")) - 1
+            exact = sum(_nv_exact(a, sa, i, k) * _nv_exact(b, sb, j, k) for k in range(K))
+            exact *= Fraction(float(ga)) * Fraction(float(gbs[s_idx]))
+            want = oracle.bf16_bits_to_f64(oracle.bf16_bits_from_f64(np.array([float(exact)])))[0]
+            assert got[i, j] == want, (i, j)
+
+
+def test_gemm_segments_single_segment_is_the_gemm():
+    rng = np.random.default_rng(28)
+    a = rng.integers(0, 256, size=(4, 64), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(32, 64), dtype=np.uint8)
+    sa = rng.integers(0x20, 0x50, size=(4, 8), dtype=np.uint8)
+    sb = rng.integers(0x20, 0x50, size=(32, 8), dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.nvfp4_gemm_segments_bf16(a, sa, 0.5, b, sb, [0.25], [32]),
+                                  oracle.nvfp4_gemm_bf16(a, sa, 0.5, b, sb, 0.25))
