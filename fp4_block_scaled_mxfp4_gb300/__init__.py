@@ -1,9 +1,9 @@
 """GB300 (sm_103a) MXFP4 mixture-of-experts expert FFN.
 
 The compute path is the C-ABI library ``libmxfp4moe.so`` (hand-written CUDA: tcgen05
-block-scaled grouped GEMM (MXFP4 and NVFP4), routing, MX / NVFP4 quantisers, combine, MXFP4 / NVFP4 / FP8 dequant
-kernels); this package only builds it (``build.build()``) and marshals torch tensors into
-its calls.
+block-scaled grouped GEMM in MXFP4 and NVFP4, routing, MX and NVFP4 quantisers, combine,
+MXFP4 / NVFP4 / FP8 dequant kernels); this package only builds it (``build.build()``)
+and marshals torch tensors into its calls.
 """
 from ._native import (  # noqa: F401
     MXError,
@@ -26,6 +26,7 @@ from ._native import (  # noqa: F401
     mxfp4_tiled_scales_bytes,
     nvfp4_dequant,
     nvfp4_gemm_bf16,
+    nvfp4_gemm_bf16_multi,
     nvfp4_scales_to_tiled,
     nvfp4_tiled_scales_bytes,
     status_string,

@@ -29,6 +29,8 @@ _SIGNATURES = {
     "nvfp4_scales_to_tiled": (ctypes.c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "nvfp4_gemm_bf16": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_ptr, ctypes.c_float, _c_ptr,
                                        _c_i64, _c_i64, _c_i64, _c_ptr]),
+    "nvfp4_gemm_bf16_multi": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                             ctypes.c_int, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "act_quant_mxfp4": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "act_quant_nvfp4": (ctypes.c_int, [_c_ptr, ctypes.c_float, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "moe_nvfp4_workspace_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
@@ -184,6 +186,32 @@ def nvfp4_gemm_bf16(a, sa, a_global, b, sb_tiled, b_global, d, stream=None) -> N
     _need(d, d.dtype, (M, N), "d")
     _check(lib().nvfp4_gemm_bf16(_ptr(a), _ptr(sa), float(a_global), _ptr(b), _ptr(sb_tiled), float(b_global),
                                  _ptr(d), M, N, K, _stream(stream)), "nvfp4_gemm_bf16")
+
+
+def nvfp4_gemm_bf16_multi(a, sa, a_global, b, sb_tiled, b_globals, seg_rows, d, stream=None) -> None:
+    """Fused NVFP4 projection: B stacks len(seg_rows) weight matrices along N (segment s has
+    seg_rows[s] rows and global b_globals[s]); d[:, segment s] = bf16(a_global * b_globals[s]
+    * A . B_s^T). b_globals / seg_rows are host sequences."""
+    import torch
+    M, half = a.shape
+    N = b.shape[0]
+    K = 2 * half
+    if sum(int(r) for r in seg_rows) != N or len(seg_rows) != len(b_globals):
+        raise ValueError("seg_rows must cover B's rows, with one global per segment")
+    _need(a, torch.uint8, (M, half), "a")
+    _need(sa, torch.uint8, (M, K // 16), "sa")
+    _need(b, torch.uint8, (N, half), "b")
+    if sb_tiled.dtype != torch.uint8 or sb_tiled.numel() < nvfp4_tiled_scales_bytes(N, K) or not sb_tiled.is_cuda:
+        raise ValueError("sb_tiled: uint8 CUDA buffer of nvfp4_tiled_scales_bytes(N, K) bytes")
+    if not _bf16_like(d):
+        raise ValueError("d must be bfloat16 (or its 16-bit bit pattern)")
+    _need(d, d.dtype, (M, N), "d")
+    n = len(seg_rows)
+    gl = (ctypes.c_float * n)(*[float(x) for x in b_globals])
+    rows = (ctypes.c_int64 * n)(*[int(x) for x in seg_rows])
+    _check(lib().nvfp4_gemm_bf16_multi(_ptr(a), _ptr(sa), float(a_global), _ptr(b), _ptr(sb_tiled),
+                                       ctypes.addressof(gl), ctypes.addressof(rows), n, _ptr(d), M, K,
+                                       _stream(stream)), "nvfp4_gemm_bf16_multi")
 
 
 def fp8_block_dequant_128x128(q, sf, out, stream=None) -> None:

@@ -337,8 +337,23 @@ int nvfp4_scales_to_tiled(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t
 
 int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b, const uint8_t* sb_tiled,
                     float b_global, void* d_bf16, int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
-    if (M < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
-    if (K % 128 || N % 16) return MX_ERR_UNSUPPORTED;
+    return nvfp4_gemm_bf16_multi(a, sa, a_global, b, sb_tiled, &b_global, &N, 1, d_bf16, M, K, stream);
+}
+
+int nvfp4_gemm_bf16_multi(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b,
+                          const uint8_t* sb_tiled, const float* b_globals, const int64_t* seg_rows, int nseg,
+                          void* d_bf16, int64_t M, int64_t K, mx_stream_t stream) {
+    if (!b_globals || !seg_rows || nseg < 1) return MX_ERR_INVALID_ARG;
+    if (nseg > kMaxSegments) return MX_ERR_UNSUPPORTED;
+    int64_t N = 0;
+    for (int i = 0; i < nseg; ++i) {
+        if (seg_rows[i] <= 0) return MX_ERR_INVALID_ARG;
+        if (seg_rows[i] % 16) return MX_ERR_UNSUPPORTED;
+        if (seg_rows[i] >= ((int64_t)1 << 31)) return MX_ERR_UNSUPPORTED;
+        N += seg_rows[i];
+    }
+    if (M < 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (K % 128) return MX_ERR_UNSUPPORTED;
     if (M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 24)) return MX_ERR_UNSUPPORTED;
     if (M == 0) return MX_OK;
     if (!a || !sa || !b || !sb_tiled || !d_bf16) return MX_ERR_INVALID_ARG;
@@ -352,7 +367,16 @@ int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const u
     GemmArgs g = base_args(sa, sb_tiled, K, M, N, d->status);
     g.ld_sf = K / 16;                  // one E4M3 scale per 16 elements
     g.kw = K / 64;                     // scale words (4 scales) per row
-    g.alpha = a_global * b_global;
+    g.alpha = a_global * b_globals[0];
+    if (nseg > 1) {                    // a fused projection: one scale per segment of columns
+        int64_t end = 0;
+        g.nseg = nseg;
+        for (int i = 0; i < nseg; ++i) {
+            end += seg_rows[i];
+            g.seg_end[i] = (int32_t)end;
+            g.seg_alpha[i] = a_global * b_globals[i];
+        }
+    }
     g.num_mtiles_host = (int32_t)((M + kBM - 1) / kBM);
     g.m_total = M;
     g.n_tiles = (int32_t)((N + kBN - 1) / kBN);

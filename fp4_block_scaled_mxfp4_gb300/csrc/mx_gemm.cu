@@ -480,9 +480,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float alpha_a = 1.0f, alpha_b = 1.0f;
         const float q_g = kNv ? args.q_global : 0.0f;
         const float q_r = kNv && kL1 ? __frcp_rn(__fmul_rn(6.0f, q_g)) : 0.0f;
-        // L2's output value of an accumulator word
-        auto out_value = [&](uint32_t acc) {
-            return kNv ? __fmul_rn(__uint_as_float(acc), alpha_a) : __uint_as_float(acc);
+        // L2's output value of an accumulator word, with the scale of its 16-column block
+        auto out_value = [&](uint32_t acc, float alpha) {
+            return kNv ? __fmul_rn(__uint_as_float(acc), alpha) : __uint_as_float(acc);
+        };
+        // NVFP4 L2: the scale of the 16 output columns starting at col (its segment's, in a
+        // fused projection)
+        auto col_alpha = [&](int64_t col) {
+            float a = alpha_a;
+            if (kNv && !kL1 && args.nseg > 0) {
+                a = args.seg_alpha[args.nseg - 1];
+                for (int s = args.nseg - 2; s >= 0; --s)
+                    if (col < args.seg_end[s]) a = args.seg_alpha[s];
+            }
+            return a;
         };
         // L1's h = bf16(silu(bf16(g)) * bf16(u)) from the gate and up accumulator words
         auto h_value = [&](uint32_t acc_g, uint32_t acc_u) {
@@ -543,10 +554,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int i = 0; i < kPieces; ++i) {
                     const int64_t col = (int64_t)nt * kN + (kN / 2) * hf + 32 * i;
                     if (col >= args.n_valid) break;
+                    const float al[2] = {col_alpha(col), col_alpha(col + 16)};
                     uint32_t p[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        p[j] = pack_bf16x2(out_value(v[i][2 * j]), out_value(v[i][2 * j + 1]));
+                        p[j] = pack_bf16x2(out_value(v[i][2 * j], al[j >> 3]), out_value(v[i][2 * j + 1], al[j >> 3]));
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {       // 16 columns (32 bytes) per row and store
                         if (col + 16 * c >= args.n_valid) break;
@@ -621,10 +633,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kPieces; ++i) {
                     const int64_t col = (int64_t)nt * kN + (kN / 2) * hf + 32 * i;
+                    const float al[2] = {col_alpha(col), col_alpha(col + 16)};
                     uint32_t p[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        p[j] = pack_bf16x2(out_value(v[i][2 * j]), out_value(v[i][2 * j + 1]));
+                        p[j] = pack_bf16x2(out_value(v[i][2 * j], al[j >> 3]), out_value(v[i][2 * j + 1], al[j >> 3]));
                     uint16_t* dst = args.y + grow * args.ld_y + col;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {

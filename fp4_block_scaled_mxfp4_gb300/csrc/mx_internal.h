@@ -36,6 +36,8 @@ constexpr int kGemmThreads = 384;  // 4 control warps + 8 epilogue warps
 constexpr int kRouteChunk = 2048;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 64;
+// Stacked weight matrices of one fused NVFP4 projection.
+constexpr int kMaxSegments = 8;
 
 // Arguments of the expert GEMM kernels (plain data, copied into the kernel parameters).
 struct GemmArgs {
@@ -74,6 +76,12 @@ struct GemmArgs {
     float alpha;
     const float* w_global;
     float q_global;
+    // NVFP4 L2 with nseg > 0: B is nseg weight matrices stacked along N (a fused projection);
+    // output columns below seg_end[s] (and at or above seg_end[s - 1]) are scaled by
+    // seg_alpha[s] instead of alpha. Boundaries are multiples of 16.
+    int32_t nseg;
+    int32_t seg_end[kMaxSegments];
+    float seg_alpha[kMaxSegments];
 };
 
 size_t gemm_smem_bytes();

@@ -124,6 +124,22 @@ int nvfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, float a_global, const u
                     int64_t K, mx_stream_t stream);
 
 /*
+ * nvfp4_gemm_bf16_multi -- a fused NVFP4 projection: B is nseg weight matrices stacked along
+ * N, each with its own global scale ([GS]: the fused q_a + kv projection carries two
+ * weight_scale_2 values). Output columns of segment s are
+ *   D[:, seg s] = bf16(a_global * b_globals[s] * A . B_s^T),
+ * i.e. nvfp4_gemm_bf16 of each segment, computed as one GEMM over the stacked B.
+ *   b_globals float32 [nseg] and seg_rows int64 [nseg] are HOST arrays, read during the
+ *   call; seg_rows[s] > 0 rows of B each, a multiple of 16; N = sum(seg_rows);
+ *   1 <= nseg <= 8 (MX_ERR_UNSUPPORTED above). B's scales: nvfp4_scales_to_tiled of the
+ *   stacked [N, K/16] E4M3 scales. Other arguments, layouts and rules as nvfp4_gemm_bf16;
+ *   D uint16 [M, N].
+ */
+int nvfp4_gemm_bf16_multi(const uint8_t* a, const uint8_t* sa, float a_global, const uint8_t* b,
+                          const uint8_t* sb_tiled, const float* b_globals, const int64_t* seg_rows,
+                          int nseg, void* d_bf16, int64_t M, int64_t K, mx_stream_t stream);
+
+/*
  * fp8_block_dequant_128x128 -- FP8 E4M3 x E8M0 128x128 block scale -> BF16 ([DQ] item 1).
  *   out[i, j] = bf16( e4m3(q[i, j]) * 2^(sf[i/128, j/128] - 127) )
  *   q uint8 [rows, cols] (E4M3 "fn" bytes), sf uint8 [ceil(rows/128), ceil(cols/128)],

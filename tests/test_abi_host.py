@@ -189,3 +189,21 @@ def test_nvfp4_quant_and_forward_validation(lib):
     assert lib.moe_nvfp4_workspace_layout(16, 256, 128, 4, 2, 1, ctypes.addressof(buf)) == MX_OK
     xs, hq = buf[1], buf[2]
     assert hq - xs >= 32 * (256 // 16)
+
+
+def test_nvfp4_fused_projection_validation(lib):
+    """Every call is rejected (or has M == 0) before anything launches."""
+    def call(rows, globals_=None, M=4, K=256, b=FAKE):
+        n = len(rows)
+        gl = (ctypes.c_float * max(n, 1))(*([0.5] * n if globals_ is None else globals_))
+        rr = (ctypes.c_int64 * max(n, 1))(*rows)
+        return lib.nvfp4_gemm_bf16_multi(FAKE, FAKE, 1.0, b, FAKE, ctypes.addressof(gl), ctypes.addressof(rr), n,
+                                         FAKE, M, K, None)
+    assert call([1536, 520]) == MX_ERR_UNSUPPORTED                 # a segment not a multiple of 16
+    assert call([1536, 0]) == MX_ERR_INVALID_ARG
+    assert call([]) == MX_ERR_INVALID_ARG
+    assert call([16] * 9) == MX_ERR_UNSUPPORTED                    # more than 8 segments
+    assert call([1536, 576], K=192) == MX_ERR_UNSUPPORTED           # K % 128
+    assert call([1536, 576], M=0) == MX_OK
+    assert call([1536, 576], b=None) == MX_ERR_INVALID_ARG
+    assert call([1536, 576], b=ODD) == MX_ERR_MISALIGNED

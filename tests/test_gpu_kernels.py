@@ -310,3 +310,29 @@ def test_route_bit_exact(mx, T, K, E):
     np.testing.assert_array_equal(counts.cpu().numpy(), rc)
     np.testing.assert_array_equal(offsets.cpu().numpy(), ro)
     np.testing.assert_array_equal(row_of.cpu().numpy(), rr)
+
+
+@pytest.mark.parametrize("M,K,seg", [(300, 7168, [1536, 576]), (130, 512, [48, 208, 16, 272]),
+                                     (64, 384, [256]), (200, 256, [16] * 8)])
+def test_nvfp4_fused_projection(mx, M, K, seg):
+    """Weights stacked along N with one global per segment (the fused q_a + kv projection):
+    segment boundaries inside 256-column tiles and inside 32-column pieces, up to eight
+    segments, against the oracle within the GEMM bound."""
+    import torch
+    rng = np.random.default_rng(M + K + len(seg))
+    N = sum(seg)
+    a = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x20, 0x50, size=(M, K // 16), dtype=np.uint8)
+    sb = rng.integers(0x28, 0x48, size=(N, K // 16), dtype=np.uint8)
+    ga = 0.0173
+    gbs = [float(np.float32(v)) for v in rng.uniform(1e-4, 4.0, size=len(seg)) * rng.choice([-1, 1], len(seg))]
+    d = _empty((M, N), torch.bfloat16)
+    mx.nvfp4_gemm_bf16_multi(dev(a), dev(sa), ga, dev(b), _nv_tiled(mx, sb), gbs, seg, d)
+    g = np.repeat([float(np.float32(ga)) * v for v in gbs], seg)
+    S = oracle.nvfp4_values(a, sa, 1.0) @ oracle.nvfp4_values(b, sb, 1.0).T
+    absdot = np.abs(oracle.nvfp4_values(a, sa, 1.0)) @ np.abs(oracle.nvfp4_values(b, sb, 1.0)).T
+    got = bf16_host(d)
+    assert_gemm_close(got, S * g[None, :], absdot * np.abs(g)[None, :], f"fused projection {seg}")
+    ref = oracle.nvfp4_gemm_segments_bf16(a, sa, ga, b, sb, gbs, seg)
+    assert (got == ref).mean() > 0.98
