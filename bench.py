@@ -471,7 +471,19 @@ def measure_extra(mx, torch, dev, stream):
         ms = timeit(fn, reps=20)
         tflops = 2.0 * M * N * K / ms / 1e9
         res[name] = {"shape": [M, N, K], "ms": ms, "TFLOP/s": tflops, "frac_fp4_peak": tflops / fp4_peak}
-    del g, d
+    # the fused q_a + kv projection: two weight matrices stacked along N, one global each
+    seg = [1536, 576]
+    Nf = sum(seg)
+    df = torch.empty((M, Nf), dtype=torch.bfloat16, device=dev)
+    bf = g["b"][:Nf]
+    sbf = torch.empty(mx.nvfp4_tiled_scales_bytes(Nf, K), dtype=torch.uint8, device=dev)
+    mx.nvfp4_scales_to_tiled(torch.from_numpy(np.ascontiguousarray(nv_sb[:Nf])).to(dev), sbf)
+    ms = timeit(lambda: mx.nvfp4_gemm_bf16_multi(g["a"], g["nv_sa"], ga, bf, sbf, [gb, 0.5 * gb], seg, df,
+                                                 stream=stream), reps=20)
+    tflops = 2.0 * M * Nf * K / ms / 1e9
+    res["gemm_nvfp4_fused_projection"] = {"shape": [M, Nf, K], "segments": seg, "ms": ms, "TFLOP/s": tflops,
+                                          "frac_fp4_peak": tflops / fp4_peak}
+    del g, d, df, sbf
     torch.cuda.empty_cache()
     for name in ("decode", "shared"):
         inp = make_config_inputs(name)
