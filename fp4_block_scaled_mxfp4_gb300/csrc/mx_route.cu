@@ -8,8 +8,9 @@
 //      the earlier pairs of its expert inside the chunk (warp match + a per-warp scan);
 //   2. route_scan (one CTA): per-expert prefix over chunks, expert offsets, and the list of
 //      128-row M tiles (expert, first row, valid rows) that the grouped GEMMs walk;
-//   3. quant_gather: row_of[t, k] = offsets[e] + chunk_base[chunk, e] + rank, and the MX
-//      quantisation of each token row written once per routed pair into the grouped rows.
+//   3. quant_gather: row_of[t, k] = offsets[e] + chunk_base[chunk, e] + rank, and the
+//      quantisation of each token row (MXFP4, or NVFP4 against the activation's global scale)
+//      written once per routed pair into the grouped rows.
 #include <type_traits>
 
 #include "mx_device.cuh"

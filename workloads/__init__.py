@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the MXFP4 MoE expert FFN.
+"""Seeded synthetic inputs for the MoE expert FFN (MXFP4 and NVFP4) and its kernels.
 
 This module is shared by the CUDA-path tests, ``bench.py`` and the oracle tests. It
 holds none of the method's arithmetic: it draws random bytes, normals and routing
