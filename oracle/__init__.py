@@ -7,6 +7,7 @@ C-ABI library and its Python binding) never imports it, and it never imports the
 """
 from .mxfp4_oracle import (  # noqa: F401
     act_quant_mxfp4,
+    act_quant_mxfp8,
     bf16_bits_from_f64,
     bf16_bits_to_f64,
     e2m1_decode,
@@ -18,8 +19,10 @@ from .mxfp4_oracle import (  # noqa: F401
     mxfp4_gemm_blockint,
     mxfp4_gemm_bf16,
     mxfp4_values,
+    mxfp8_values,
     moe_combine,
     moe_forward,
+    moe_mxfp8_forward,
     moe_nvfp4_forward,
     moe_l1_exact,
     moe_l2_bf16,

@@ -83,6 +83,13 @@ R16 The NVFP4 MoE forward is the MXFP4 one (R1, R3-R5) with NVFP4 in every quant
 R17 A fused projection (the pages' q_a + kv weights stacked along N, each with its own
     weight_scale_2, [GS]) is one NVFP4 GEMM over the stacked B whose output columns of
     segment s are scaled by a_global * b_global[s] (R14 per segment).
+R18 MXFP8 activations (E4M3 elements, one E8M0 scale per 32; the pages do not name this
+    variant, it is the FP8 reading of "re-quant"): the OCP MX rule with E4M3's largest
+    exponent 8 in place of E2M1's 2 -- scale byte E = clamp(floor(log2 amax) - 8 + 127,
+    0, 254) (0 for amax = 0); element = E4M3 nearest x * 2^(127 - E), ties to even,
+    saturating at +-448, sign kept (-0 -> 0x80); a block holding a NaN or an infinity gets
+    E = 255 and elements sign|0x7F. The MXFP8 MoE forward is R1, R3-R5 with MXFP8 in both
+    activation quantisations and the MXFP4 weights unchanged.
 
 Parity status: every function below is pinned by the ``-m "not gpu"`` tests (tables from
 the OCP MX definitions and torch's float8 conversions, one-hot nibble/scale tests, the
@@ -100,6 +107,7 @@ __all__ = [
     "act_quant_mxfp4", "mxfp4_gemm_bf16", "mxfp4_gemm_blockint", "moe_route", "moe_forward",
     "nvfp4_values", "nvfp4_dequant", "nvfp4_gemm_f64", "nvfp4_gemm_bf16",
     "e4m3_round_code", "nvfp4_quantize", "moe_nvfp4_forward", "nvfp4_gemm_segments_bf16",
+    "act_quant_mxfp8", "mxfp8_values", "moe_mxfp8_forward",
     "moe_flops_per_pair", "moe_l1_exact", "swiglu_bf16", "moe_l2_bf16", "moe_combine",
 ]
 
@@ -576,6 +584,71 @@ def moe_nvfp4_forward(x_bits, topk_ids, topk_w, w13, s13, g13, w2, s2, g2, x_glo
         u = gu[:, I:] * (gx * float(g13[e, 1]))
         hq, hs = nvfp4_quantize(swiglu_bf16(g, u), h_global)
         y = (nvfp4_values(hq, hs, 1.0) @ nvfp4_values(w2[e], s2[e], 1.0).T) * (gh * float(g2[e]))
+        return bf16_bits_to_f64(bf16_bits_from_f64(y))
+
+    if topk_ids is None:
+        if E != 1:
+            raise ValueError("the unrouted (shared expert) mode needs exactly one expert")
+        return bf16_bits_from_f64(ffn(np.arange(tok.size), 0))
+    ids = np.asarray(topk_ids, dtype=np.int64)[tok]
+    n, K = ids.shape
+    Y = np.zeros((n, K, H), dtype=np.float64)
+    for e in range(E):
+        sel = np.argwhere(ids == e)
+        if sel.size == 0:
+            continue
+        Y[sel[:, 0], sel[:, 1]] = ffn(sel[:, 0], e)
+    return moe_combine(Y, ids, np.asarray(topk_w, dtype=np.float32)[tok], E)
+
+
+# --------------------------------------------------------------------------------------
+# MXFP8 activations (reading R18)
+# --------------------------------------------------------------------------------------
+
+
+def act_quant_mxfp8(x_bits):
+    """BF16 [M, K] -> (E4M3 codes uint8 [M, K], E8M0 scales uint8 [M, K/32]) by reading R18."""
+    xb = np.asarray(x_bits, dtype=np.uint16)
+    M, K = xb.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    x = bf16_bits_to_f64(xb).reshape(M, K // 32, 32)
+    finite = np.isfinite(x).all(axis=-1)
+    amax = np.abs(np.where(np.isfinite(x), x, 0.0)).max(axis=-1)
+    _, e = np.frexp(amax)                          # amax = f * 2^e -> floor(log2) = e - 1
+    E = np.where(amax > 0, np.clip(e - 1 - 8 + 127, 0, 254), 0).astype(np.int64)
+    v = np.abs(np.where(np.isfinite(x), x, 0.0)) * np.ldexp(1.0, 127 - E)[..., None]   # exact
+    mag = e4m3_round_code(np.minimum(v, 448.0))
+    sign = (np.signbit(x).astype(np.uint8) << 7)
+    code = np.where(finite[..., None], sign | mag, sign | 0x7F).astype(np.uint8)
+    sf = np.where(finite, E, 255).astype(np.uint8)
+    return code.reshape(M, K), sf
+
+
+def mxfp8_values(codes, sf) -> np.ndarray:
+    """Exact float64 value of an MXFP8 tensor: e4m3(code) * 2^(sf[r, c // 32] - 127)."""
+    q = np.asarray(codes, dtype=np.uint8)
+    sf = np.asarray(sf, dtype=np.uint8)
+    if sf.shape[-1] * 32 != q.shape[-1]:
+        raise ValueError("need one scale per 32 columns")
+    with np.errstate(invalid="ignore"):
+        return e4m3fn_decode(np.arange(256))[q] * np.repeat(e8m0_decode(sf), 32, axis=-1)
+
+
+def moe_mxfp8_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, I: int, tokens=None):
+    """MoE expert FFN with MXFP8 activations and the MXFP4 weights (R18); arguments and
+    result as moe_forward."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    T, H = x_bits.shape
+    E = w13.shape[0]
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    xq, xs = act_quant_mxfp8(x_bits[tok])
+    xv = mxfp8_values(xq, xs)
+
+    def ffn(rows, e):
+        g, u = moe_l1_exact(xv[rows], w13[e], s13[e], I)                   # exact sums
+        hq, hs = act_quant_mxfp8(swiglu_bf16(g, u))
+        y = mxfp8_values(hq, hs) @ mxfp4_values(w2[e], s2[e]).T
         return bf16_bits_to_f64(bf16_bits_from_f64(y))
 
     if topk_ids is None:
