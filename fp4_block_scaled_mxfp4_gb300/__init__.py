@@ -29,5 +29,6 @@ from ._native import (  # noqa: F401
     nvfp4_gemm_bf16_multi,
     nvfp4_scales_to_tiled,
     nvfp4_tiled_scales_bytes,
+    selftest_wait_timeout,
     status_string,
 )

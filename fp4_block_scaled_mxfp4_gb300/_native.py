@@ -22,6 +22,7 @@ _SIGNATURES = {
     "mx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mx_version": (ctypes.c_int, []),
     "mx_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "mx_selftest_wait_timeout": (ctypes.c_int, [_c_ptr]),
     "mxfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "fp8_block_dequant_128x128": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "nvfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_i64, _c_i64, _c_ptr]),
@@ -395,6 +396,12 @@ def moe_mxfp4_route(topk_ids, E: int, counts, offsets, row_of, workspace, stream
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().moe_mxfp4_route(_ptr(topk_ids), T, K, E, _ptr(counts), _ptr(offsets), _ptr(row_of),
                                  _ptr(workspace), ws_bytes, _stream(stream)), "moe_mxfp4_route")
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launch the failure-path self-test: a bounded wait (about 2 s) on a barrier nothing
+    arrives at, which records a timeout in the device status word (see device_status)."""
+    _check(lib().mx_selftest_wait_timeout(_stream(stream)), "mx_selftest_wait_timeout")
 
 
 def device_status(clear: bool = True) -> int:

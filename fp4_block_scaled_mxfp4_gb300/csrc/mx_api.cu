@@ -229,6 +229,12 @@ const char* mx_status_string(int s) {
 
 int mx_version(void) { return 100; }
 
+int mx_selftest_wait_timeout(mx_stream_t stream) {
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_wait_probe(d->status, static_cast<cudaStream_t>(stream)));
+}
+
 int mx_device_status(int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return MX_ERR_CUDA;
     uint32_t v = 0;

@@ -275,6 +275,20 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __rest
     pdl_launch_dependents();
 }
 
+// Self-test of the failure path: one thread waits, with the bounded wait every pipeline of
+// the GEMMs uses, on a freshly initialised mbarrier that nothing arrives at. The wait runs
+// out after its limit, records kErrWaitFull in the status word and the kernel returns, so
+// the context stays usable. No asynchronous copy or MMA references the barrier.
+__global__ void __launch_bounds__(32) wait_probe_kernel(uint32_t* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, status, kErrWaitFull);
+}
+
 // NVFP4 activation quantisation (nv_quant16): one thread per 16-element block, two 16-byte
 // loads, 8 bytes of codes and one E4M3 scale byte out.
 __global__ void __launch_bounds__(kThreads) act_quant_nv_kernel(const uint4* __restrict__ x8,
@@ -405,6 +419,11 @@ cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int
     if (blocks == 0) return cudaSuccess;
     return launch_pdl(act_quant_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
                       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks);
+}
+
+cudaError_t launch_wait_probe(uint32_t* status, cudaStream_t s) {
+    wait_probe_kernel<<<1, 32, 0, s>>>(status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M,

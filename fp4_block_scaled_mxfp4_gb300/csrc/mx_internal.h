@@ -119,6 +119,8 @@ cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int
 // NVFP4 activation quantisation with the float32 global (codes [M, K/2], E4M3 sf [M, K/16]).
 cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M,
                                    int64_t K, int num_sms, cudaStream_t s);
+// Failure-path self-test: a bounded wait on a barrier nothing arrives at (see mx_elementwise.cu).
+cudaError_t launch_wait_probe(uint32_t* status, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,
                            int64_t T, int64_t K, int64_t H, int num_sms, cudaStream_t s);
 

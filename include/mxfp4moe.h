@@ -70,6 +70,16 @@ int mx_version(void);
 int mx_device_status(int clear);
 
 /*
+ * mx_selftest_wait_timeout -- exercises the failure path of the bounded device waits: launches
+ * a one-thread kernel on `stream` that waits, with the same bounded wait the GEMM pipelines use
+ * (about 2 s), on a barrier nothing arrives at. When the wait runs out the kernel records a
+ * timeout in the device status word and returns; nothing traps and the context stays usable.
+ * mx_device_status() then reports MX_ERR_DEVICE_TIMEOUT. For tests only. Returns MX_OK once
+ * launched, MX_ERR_CUDA if the launch fails.
+ */
+int mx_selftest_wait_timeout(mx_stream_t stream);
+
+/*
  * mxfp4_dequant -- MXFP4 -> BF16 ([DQ] item 2, [FMT]).
  *   out[r, c] = bf16( E2M1(nibble(codes[r, c/2], c%2)) * 2^(sf[r, c/32] - 127) )
  *   codes uint8 [rows, cols/2], sf uint8 [rows, cols/32], out uint16 [rows, cols].
