@@ -25,11 +25,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// ---- GEMM tile geometry (tcgen05 kind::mxf4, one CTA per tile, M = 128, N = 256) ----
+// ---- GEMM tile geometry (tcgen05 block-scaled MMA; persistent CTAs walk 128-row x kBN tiles;
+// each configuration's stage count is in mx_gemm.cu) ----
 constexpr int kBM = 128;           // rows of A per tile (TMEM lanes)
 constexpr int kBN = 256;           // columns of the accumulator (L1: 128 gate + 128 up); 128 for small M
 constexpr int kBK = 256;           // E2M1 elements of K per pipeline stage (128 bytes)
-constexpr int kStages = 4;
 constexpr int kGemmThreads = 384;  // 4 control warps + 8 epilogue warps
 
 // Routing: pairs per counting block.
