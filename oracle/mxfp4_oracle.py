@@ -32,7 +32,7 @@ Element formats follow the OCP Microscaling (MX) v1.0 definitions of E2M1, E8M0 
 E4M3 ("fn": no infinities, S.1111.111 is NaN) encoding; the pages name the formats but
 print no bit layout.
 
-Readings where the pages are silent (each is listed with the same wording in the design doc):
+Readings where the pages are silent:
 
 R1  The first activation quantisation uses the same MXFP4 rule as the re-quant: "re-quant"
     in [PIPE] presupposes an earlier quantisation of x, and both GEMM operands are E2M1.
