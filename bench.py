@@ -355,7 +355,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         extra["forward_row_major_scales_ms"] = p0.elapsed_time(p1) / 10
     if rank == 0 and not args.no_extra:
-        extra = measure_extra(mx, torch, dev, stream)
+        extra.update(measure_extra(mx, torch, dev, stream))
 
     if rank != 0:
         if world > 1:
