@@ -19,6 +19,7 @@ from .mxfp4_oracle import (  # noqa: F401
     mxfp4_gemm_blockint,
     mxfp4_gemm_bf16,
     mxfp4_values,
+    mxfp8_mxfp4_gemm_bf16,
     mxfp8_values,
     moe_combine,
     moe_forward,

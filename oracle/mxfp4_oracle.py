@@ -107,7 +107,7 @@ __all__ = [
     "act_quant_mxfp4", "mxfp4_gemm_bf16", "mxfp4_gemm_blockint", "moe_route", "moe_forward",
     "nvfp4_values", "nvfp4_dequant", "nvfp4_gemm_f64", "nvfp4_gemm_bf16",
     "e4m3_round_code", "nvfp4_quantize", "moe_nvfp4_forward", "nvfp4_gemm_segments_bf16",
-    "act_quant_mxfp8", "mxfp8_values", "moe_mxfp8_forward",
+    "act_quant_mxfp8", "mxfp8_values", "moe_mxfp8_forward", "mxfp8_mxfp4_gemm_bf16",
     "moe_flops_per_pair", "moe_l1_exact", "swiglu_bf16", "moe_l2_bf16", "moe_combine",
 ]
 
@@ -633,6 +633,13 @@ def mxfp8_values(codes, sf) -> np.ndarray:
         raise ValueError("need one scale per 32 columns")
     with np.errstate(invalid="ignore"):
         return e4m3fn_decode(np.arange(256))[q] * np.repeat(e8m0_decode(sf), 32, axis=-1)
+
+
+def mxfp8_mxfp4_gemm_bf16(a_codes, a_sf, b_codes, b_sf) -> np.ndarray:
+    """y = bf16(A . B^T) with MXFP8 A [M, K] (E4M3 codes [M, K], E8M0 [M, K/32]) and MXFP4 B
+    [N, K] (codes [N, K/2], E8M0 [N, K/32]): the GEMM of the MXFP8-activation path (R18);
+    the float64 sum is exact for these inputs and rounded once."""
+    return bf16_bits_from_f64(mxfp8_values(a_codes, a_sf) @ mxfp4_values(b_codes, b_sf).T)
 
 
 def moe_mxfp8_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, I: int, tokens=None):

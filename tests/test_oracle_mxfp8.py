@@ -200,3 +200,22 @@ def test_mxfp8_is_closer_to_bf16_than_mxfp4():
     def cos(a, b):
         return float(a.ravel() @ b.ravel() / (np.linalg.norm(a) * np.linalg.norm(b)))
     assert cos(ref, exact) > cos(four, exact)
+
+
+def test_mxfp8_mxfp4_gemm_brute_force():
+    """The mixed GEMM against exact rationals from the bit fields of both formats."""
+    rng = np.random.default_rng(88)
+    M, N, K = 3, 4, 64
+    a = rng.integers(0, 256, size=(M, K), dtype=np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0x10                                     # no NaN codes
+    sa = rng.integers(115, 135, size=(M, K // 32), dtype=np.uint8)
+    b = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sb = rng.integers(118, 125, size=(N, K // 32), dtype=np.uint8)
+    grid = _e4m3_grid()
+    got = oracle.bf16_bits_to_f64(oracle.mxfp8_mxfp4_gemm_bf16(a, sa, b, sb))
+    for i in range(M):
+        av = [(-1 if a[i, k] >> 7 else 1) * grid[int(a[i, k]) & 0x7F] * Fraction(2) ** (int(sa[i, k // 32]) - 127)
+              for k in range(K)]
+        for j in range(N):
+            bv = _mx4_row(b[j], sb[j])
+            assert got[i, j] == float(_bf16(sum(x * y for x, y in zip(av, bv)))), (i, j)
