@@ -1,4 +1,4 @@
-"""CPU oracle for the MXFP4 MoE expert FFN (test infrastructure).
+"""CPU oracle for the MoE expert FFN: MXFP4, NVFP4 and MXFP8 variants (test infrastructure).
 
 This package is the plain, slow, float64 CPU statement of what the hot path computes.
 It is test infrastructure: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU

@@ -1,4 +1,5 @@
-"""Plain CPU oracle (numpy, float64) for the MXFP4 mixture-of-experts expert FFN.
+"""Plain CPU oracle (numpy, float64) for the mixture-of-experts expert FFN over FP4 weights
+(MXFP4, and the NVFP4 and MXFP8-activation variants).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s
 CPU-baseline / reference leg may import or run this module. It shares no code with the
