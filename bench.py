@@ -16,19 +16,24 @@ every input resident in HBM and the weight scales in the GEMM's tile layout (con
 once, at weight load, like the weights themselves); `e2e` is the same metric through the C ABI with the step's
 inputs copied from pinned host memory and the output copied back inside the timed region.
 `roofline` reports the L1 GEMM, timed live with CUDA events recorded by the library at
-its phase boundaries. `cpu_baseline` times the CPU oracle on a small token sample.
+its phase boundaries, against the measured burst BF16 tensor rate times the nominal
+FP4:BF16 ratio (and, beside it, against the FP4 MMA issue rate at the sampled SM clock).
+`cpu_baseline` times the CPU oracle on a bounded token sample: one process per host core
+(spawned, each single-threaded), with the single-core figure beside it.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import multiprocessing as mp
 import os
 import subprocess
 import sys
 import time
 
-# The oracle is timed on one host core: pin BLAS before numpy loads.
+# Every oracle process runs on one host core: pin BLAS before numpy loads (spawned oracle
+# workers inherit this).
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -44,6 +49,9 @@ METRIC = "MoE fwd TFLOP/s (MXFP4 grouped GEMM) & dequant GB/s, % of roofline, 1 
 WORKLOAD = ("routed MoE prefill forward: T=8192 tokens, hidden 7168, intermediate 3072, 48 experts, "
             "top-8, Zipf(1.0) expert skew, MXFP4 (E2M1 + E8M0/32) weights")
 FP4_OVER_BF16 = 13.5 / 2.25       # nominal dense FP4 : BF16 tensor-core ratio on GB300
+# FP4 MMA issue rate measured on every SM of a GB300: one 128 x 256 x 64 kind::mxf4 MMA
+# (2 * 128 * 256 * 64 FLOP) per 128 cycles, i.e. 32,768 FLOP per cycle per SM.
+MMA_FLOP_PER_CYCLE_SM = 2 * 128 * 256 * 64 / 128
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "l1_gemm_prefill_traffic.json")
 GEMM_SRC = os.path.join(ROOT, "fp4_block_scaled_mxfp4_gb300", "csrc", "mx_gemm.cu")
 
@@ -81,6 +89,17 @@ def measured_peaks():
             d = json.load(f)
         return d, "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def fp4_peak_tflops(peaks):
+    """The FP4 roofline denominator: the measured burst BF16 tensor rate (the GEMMs here are
+    timed in sub-second regions) times the nominal FP4:BF16 ratio."""
+    return peaks["bf16_tflops"] * FP4_OVER_BF16
+
+
+def mma_rate_tflops(num_sms, sm_mhz):
+    """FP4 MMA issue rate of all SMs at the given SM clock (TFLOP/s)."""
+    return MMA_FLOP_PER_CYCLE_SM * num_sms * sm_mhz * 1e6 / 1e12
 
 
 def l1_traffic_per_launch():
@@ -162,31 +181,93 @@ def time_oracle_sample(inp, tokens):
     return dt, pairs
 
 
+# ---- the oracle on every host core: one spawned, single-threaded process per core, each
+# holding its own copy of the seeded prefill inputs and computing whole tokens ----
+_ORACLE_INP = None
+
+
+def _oracle_worker_init():
+    global _ORACLE_INP
+    _ORACLE_INP = make_config_inputs("prefill")
+
+
+def _oracle_worker_token(t):
+    dt, pairs = time_oracle_sample(_ORACLE_INP, [int(t)])
+    return pairs
+
+
+def oracle_processes():
+    """Host cores to use, limited so each process's copy of the inputs (~1.8 GB) and its
+    per-expert float64 temporaries (~1.2 GB) fit in the available memory."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    avail = None
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    avail = int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    if avail is not None:
+        cores = min(cores, max(1, int(avail // (4 << 30))))
+    return max(1, cores)
+
+
+class OraclePool:
+    """A spawn-started pool of single-threaded oracle processes (spawn: the parent may
+    already hold a CUDA context, which a forked child must not inherit)."""
+
+    def __init__(self, procs):
+        self.procs = procs
+        self.pool = mp.get_context("spawn").Pool(procs, initializer=_oracle_worker_init)
+        # every worker has built its inputs before anything is timed
+        self.pool.map(_oracle_worker_token, [0] * procs, chunksize=1)
+
+    def run(self, tokens):
+        """Wall time and routed pairs of the oracle over `tokens`, spread over the processes."""
+        t0 = time.perf_counter()
+        pairs = sum(self.pool.map(_oracle_worker_token, list(tokens), chunksize=1))
+        return time.perf_counter() - t0, pairs
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
 def run_reference(args):
-    """The reference arm: the CPU oracle, one token of the workload per step."""
+    """The reference arm: the CPU oracle on every host core, one prefill token per core and
+    step."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     c = CONFIGS["prefill"]
-    inp = make_config_inputs("prefill")
     fpp = flops_per_pair(c["H"], c["I"])
+    procs = oracle_processes()
+    pool = OraclePool(procs)
     rng = np.random.default_rng(1234)
-    for _ in range(args.warmup):
-        time_oracle_sample(inp, [int(rng.integers(inp.T))])
-    total_t, total_pairs = 0.0, 0
-    for _ in range(args.steps):
-        dt, pairs = time_oracle_sample(inp, [int(rng.integers(inp.T))])
-        total_t += dt
-        total_pairs += pairs
+    try:
+        for _ in range(args.warmup):
+            pool.run(rng.integers(c["T"], size=procs))
+        total_t, total_pairs = 0.0, 0
+        for _ in range(args.steps):
+            dt, pairs = pool.run(rng.integers(c["T"], size=procs))
+            total_t += dt
+            total_pairs += pairs
+    finally:
+        pool.close()
     value = total_pairs * fpp / total_t / 1e12
+    sample = (f"{procs} prefill tokens per step (one per process, {procs * 8} routed pairs), numpy float64, "
+              f"{procs} single-threaded processes")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": "one token (its 8 routed pairs) per step"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                         "sample": "one prefill token (8 routed pairs) per step, numpy float64, 1 thread"},
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": procs, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -363,18 +444,16 @@ def run_ours(args):
         return
 
     peaks, peak_kind = measured_peaks()
-    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    fp4_peak = fp4_peak_tflops(peaks)
     l1_tflops = flop_l1 / (phase_ms["l1_gemm"] * 1e-3) / 1e12
     traffic = l1_traffic_per_launch()
+    clk = clocks.summary()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mma_peak = mma_rate_tflops(num_sms, clk["sm_mhz"] or peaks.get("sm_max_mhz", 2070.0))
 
     cpu = None
-    if not args.no_cpu_baseline:
-        rng = np.random.default_rng(7)
-        tokens = sorted(rng.choice(T, size=2, replace=False).tolist())
-        dt, p = time_oracle_sample(inp, tokens)
-        cpu = {"value": p * flops_per_pair(H, I) / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-               "sample": f"{len(tokens)} prefill tokens ({p} routed pairs), numpy float64, 1 thread, "
-                         f"{dt:.1f} s"}
+    if not args.no_cpu_baseline and not args.tokens:
+        cpu = cpu_baseline(inp, H, I)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -387,18 +466,41 @@ def run_ours(args):
         "roofline": {"kernel": "L1 grouped GEMM (gate/up, fused SiLU + MX re-quant)", "bound": "tensor",
                      "achieved": l1_tflops, "peak": fp4_peak, "unit": "TFLOP/s", "frac": l1_tflops / fp4_peak,
                      "traffic": traffic,
-                     "peak_source": f"{peak_kind} bf16_tflops_sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
+                     "peak_source": f"{peak_kind} bf16_tflops (burst) x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
+                     "mma_rate_peak": mma_peak, "frac_mma_rate": l1_tflops / mma_peak,
+                     "mma_rate_source": f"one 128x256x64 kind::mxf4 MMA per 128 cycles per SM, {num_sms} SMs, "
+                                        f"median sampled SM clock"},
         "phases_ms": phase_ms,
         "cpu_baseline": cpu,
         "e2e": {"value": job_tflops(world, flop_step, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 6 * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clk,
         "extra": extra,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def cpu_baseline(inp, H, I):
+    """The oracle on a bounded sample of the step's tokens: on every host core (one
+    single-threaded process per core, two tokens each), and on one core (two tokens)."""
+    fpp = flops_per_pair(H, I)
+    rng = np.random.default_rng(7)
+    dt1, p1 = time_oracle_sample(inp, sorted(rng.choice(inp.T, size=2, replace=False).tolist()))
+    single = {"value": p1 * fpp / dt1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+              "sample": f"2 prefill tokens ({p1} routed pairs), {dt1:.1f} s"}
+    procs = oracle_processes()
+    pool = OraclePool(procs)
+    try:
+        dt, p = pool.run(rng.integers(inp.T, size=2 * procs))
+    finally:
+        pool.close()
+    return {"value": p * fpp / dt / 1e12, "unit": "TFLOP/s", "cores": procs, "kind": "oracle",
+            "sample": f"{2 * procs} prefill tokens ({p} routed pairs) over {procs} single-threaded processes, "
+                      f"numpy float64, {dt:.1f} s",
+            "single_core": single}
 
 
 def measure_extra(mx, torch, dev, stream):
@@ -473,7 +575,7 @@ def measure_extra(mx, torch, dev, stream):
     g["nv_sbt"] = torch.empty(mx.nvfp4_tiled_scales_bytes(N, K), dtype=torch.uint8, device=dev)
     mx.nvfp4_scales_to_tiled(torch.from_numpy(nv_sb).to(dev), g["nv_sbt"])
     d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    fp4_peak = peaks["bf16_tflops_sustained"] * 6.0
+    fp4_peak = fp4_peak_tflops(peaks)
     for name, fn in (("gemm_mxfp4", lambda: mx.mxfp4_gemm_bf16(g["a"], g["mx_sa"], g["b"], g["mx_sbt"], d,
                                                                stream=stream)),
                      ("gemm_nvfp4", lambda: mx.nvfp4_gemm_bf16(g["a"], g["nv_sa"], ga, g["b"], g["nv_sbt"], gb, d,
@@ -579,7 +681,7 @@ def measure_nvfp4_forward(mx, torch, dev, stream, timeit):
     flop = pairs * flops_per_pair(c["H"], c["I"])
     l1_ms = ev[2].elapsed_time(ev[3])
     l1_tflops = pairs * 2 * c["H"] * 2 * c["I"] / l1_ms / 1e9
-    fp4_peak = measured_peaks()[0]["bf16_tflops_sustained"] * 6.0
+    fp4_peak = fp4_peak_tflops(measured_peaks()[0])
     r = {"nvfp4_forward": {"workload": "routed prefill T=8192, H=7168, I=3072, 48 experts, top-8, NVFP4",
                            "ms": ms, "TFLOP/s": flop / ms / 1e9,
                            "phases_ms": {k: ev[i].elapsed_time(ev[i + 1]) for i, k in

@@ -9,6 +9,7 @@ from ._native import (  # noqa: F401
     MXError,
     act_quant_mxfp4,
     act_quant_nvfp4,
+    check_workspace,
     device_status,
     fp8_block_dequant_128x128,
     lib,

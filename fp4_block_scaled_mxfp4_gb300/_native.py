@@ -23,6 +23,8 @@ _SIGNATURES = {
     "mx_version": (ctypes.c_int, []),
     "mx_device_status": (ctypes.c_int, [ctypes.c_int]),
     "mx_selftest_wait_timeout": (ctypes.c_int, [_c_ptr]),
+    "mx_selftest_wait_timeout_ws": (ctypes.c_int, [_c_ptr, _c_ptr]),
+    "mx_check_workspace": (ctypes.c_int, [_c_ptr, ctypes.c_int, _c_ptr]),
     "mxfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "fp8_block_dequant_128x128": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "nvfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_i64, _c_i64, _c_ptr]),
@@ -398,10 +400,23 @@ def moe_mxfp4_route(topk_ids, E: int, counts, offsets, row_of, workspace, stream
                                  _ptr(workspace), ws_bytes, _stream(stream)), "moe_mxfp4_route")
 
 
-def selftest_wait_timeout(stream=None) -> None:
+def selftest_wait_timeout(stream=None, workspace=None) -> None:
     """Launch the failure-path self-test: a bounded wait (about 2 s) on a barrier nothing
-    arrives at, which records a timeout in the device status word (see device_status)."""
-    _check(lib().mx_selftest_wait_timeout(_stream(stream)), "mx_selftest_wait_timeout")
+    arrives at, which records a timeout in the device status word (see device_status) and,
+    given a workspace, in that workspace's word (see check_workspace)."""
+    if workspace is None:
+        _check(lib().mx_selftest_wait_timeout(_stream(stream)), "mx_selftest_wait_timeout")
+    else:
+        _check(lib().mx_selftest_wait_timeout_ws(_ptr(workspace), _stream(stream)), "mx_selftest_wait_timeout_ws")
+
+
+def check_workspace(workspace, stream=None, clear: bool = True) -> int:
+    """Wait for `stream` only and return the status of the last forward launched on it with
+    this workspace (0 = MX_OK, 6 = MX_ERR_DEVICE_TIMEOUT)."""
+    st = int(lib().mx_check_workspace(_ptr(workspace), 1 if clear else 0, _stream(stream)))
+    if st not in (MX_OK, 6):
+        raise MXError(st, "mx_check_workspace")
+    return st
 
 
 def device_status(clear: bool = True) -> int:

@@ -106,10 +106,11 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t tiled_bytes(int64_t rows, int64_t kb) { return (size_t)((rows + 127) / 128) * (size_t)(kb / 4) * 512; }
 
 // Workspace layout shared by moe_mxfp4_forward, moe_nvfp4_forward (sf_div 16: one scale
-// per 16 columns) and moe_mxfp4_route.
+// per 16 columns) and moe_mxfp4_route. The status word comes first, at offset 0, where
+// mx_check_workspace finds it.
 struct WsLayout {
     int64_t R = 0, nchunks = 0, max_mtiles = 0;
-    size_t num_mtiles = 0, counts = 0, offsets = 0, chunk_counts = 0, chunk_base = 0, local_rank = 0,
+    size_t status = 0, num_mtiles = 0, counts = 0, offsets = 0, chunk_counts = 0, chunk_base = 0, local_rank = 0,
            row_of = 0, tile_expert = 0, tile_row0 = 0, tile_rows = 0, xq = 0, xs = 0, hq = 0, hs = 0, y = 0,
            total = 0;
 };
@@ -125,6 +126,7 @@ WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool r
         off = align256(off + bytes);
         return at;
     };
+    L.status = take(16);
     L.num_mtiles = take(16);
     if (routed) {
         L.counts = take(4 * (size_t)E);
@@ -180,9 +182,10 @@ int check_moe_dims(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool r
     return MX_OK;
 }
 
-// Fill the GEMM arguments shared by L1 and L2.
+// Fill the GEMM arguments shared by L1 and L2; waits that run out report to the device-wide
+// word (a forward adds its workspace word).
 GemmArgs base_args(const uint8_t* sfa, const uint8_t* sfb, int64_t K, int64_t a_rows, int64_t b_rows,
-                   uint32_t* status) {
+                   uint32_t* dev_status) {
     GemmArgs g;
     std::memset(&g, 0, sizeof(g));
     g.sfa = sfa;
@@ -194,7 +197,7 @@ GemmArgs base_args(const uint8_t* sfa, const uint8_t* sfb, int64_t K, int64_t a_
     g.kw = K / 128;
     g.k_tiles = (int32_t)((K + kBK - 1) / kBK);
     g.k_tail_half = (K % kBK) != 0 ? 1 : 0;
-    g.status = status;
+    g.status = StatusWords{nullptr, dev_status};
     return g;
 }
 
@@ -232,7 +235,30 @@ int mx_version(void) { return 100; }
 int mx_selftest_wait_timeout(mx_stream_t stream) {
     DeviceInfo* d;
     if (int e = device_info(&d)) return e;
-    return cuda_status(launch_wait_probe(d->status, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_wait_probe(StatusWords{nullptr, d->status}, static_cast<cudaStream_t>(stream)));
+}
+
+int mx_selftest_wait_timeout_ws(void* workspace, mx_stream_t stream) {
+    if (!workspace) return MX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_wait_probe(StatusWords{static_cast<uint32_t*>(workspace), d->status},
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int mx_check_workspace(const void* workspace, int clear, mx_stream_t stream) {
+    if (!workspace) return MX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    // ordered after the stream's work; the wait covers this stream only
+    if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MX_ERR_CUDA;
+    if (clear && v != 0 && cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(v), s) != cudaSuccess)
+        return MX_ERR_CUDA;
+    return v ? MX_ERR_DEVICE_TIMEOUT : MX_OK;
 }
 
 int mx_device_status(int clear) {
@@ -512,10 +538,13 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     uint8_t* xs = at<uint8_t>(workspace, L.xs);
     uint8_t* hq = at<uint8_t>(workspace, L.hq);
     uint8_t* hs = at<uint8_t>(workspace, L.hs);
+    // The forward's status word: its first kernel clears it, its GEMMs' waits set it.
+    uint32_t* ws_status = at<uint32_t>(workspace, L.status);
     const int64_t R = L.R;
 
     GemmArgs g1 = base_args(xs, s13, H, R, E * 2 * I, d->status);
     GemmArgs g2 = base_args(hs, s2, I, R, E * H, d->status);
+    g1.status.ws = g2.status.ws = ws_status;
     if (nv) {
         // one E4M3 scale per 16 elements: four per 4-byte word
         g1.ld_sf = H / 16;
@@ -532,7 +561,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     if (!mark(0)) return MX_ERR_CUDA;
     if (routed) {
         rb = route_bufs(workspace, L);
-        if (launch_route(topk_ids, T, K, E, rb, s) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
+        if (launch_route(topk_ids, T, K, E, rb, s, ws_status) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
         if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s, nv != nullptr,
                                 nv ? nv->x_global : 0.0f) != cudaSuccess)
             return MX_ERR_CUDA;
@@ -545,8 +574,9 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     } else {
         if (!mark(1)) return MX_ERR_CUDA;
         const cudaError_t qe =
-            nv ? launch_act_quant_nvfp4(static_cast<const uint16_t*>(x), nv->x_global, xq, xs, T, H, d->num_sms, s)
-               : launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s);
+            nv ? launch_act_quant_nvfp4(static_cast<const uint16_t*>(x), nv->x_global, xq, xs, T, H, d->num_sms, s,
+                                        ws_status)
+               : launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s, ws_status);
         if (qe != cudaSuccess) return MX_ERR_CUDA;
         for (GemmArgs* g : {&g1, &g2}) {
             g->num_mtiles_host = (int32_t)((T + kBM - 1) / kBM);

@@ -7,11 +7,14 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "mx_internal.h"
+
 namespace mx {
 
 // ------------------------------------------------------------------------------------
-// Device status word (one per device, owned by the API layer and passed to each kernel).
-// Bounded waits OR a code into it and give up.
+// Status words. A bounded wait that runs out ORs a code into the caller's workspace word
+// (the forward's own, which its first kernel clears and mx_check_workspace reads) and into
+// the device-wide word (read by mx_device_status), then gives up.
 // ------------------------------------------------------------------------------------
 enum : uint32_t {
     kErrWaitFull = 1u << 0,
@@ -31,8 +34,9 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
-__device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {
-    if (status != nullptr) atomicOr(status, code);
+__device__ __forceinline__ void set_status(const StatusWords& st, uint32_t code) {
+    if (st.ws != nullptr) atomicOr(st.ws, code);
+    if (st.dev != nullptr) atomicOr(st.dev, code);
 }
 
 // ------------------------------------------------------------------------------------
@@ -225,7 +229,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity. Returns false when the CTA-wide abort
 // flag is raised or the time limit passes (then it raises the flag and sets `code`).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status, uint32_t code) {
+                                          const StatusWords& status, uint32_t code) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = 0;
     for (uint32_t i = 1;; ++i) {

@@ -253,8 +253,10 @@ __global__ void __launch_bounds__(kThreads) fp8_dequant_kernel(const uint8_t* __
 // store and a scale byte (consecutive threads write consecutive codes and scales).
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __restrict__ x8,
                                                              uint4* __restrict__ codes16,
-                                                             uint8_t* __restrict__ sf, int64_t blocks) {
+                                                             uint8_t* __restrict__ sf, int64_t blocks,
+                                                             uint32_t* clear_word) {
     pdl_wait();
+    if (clear_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *clear_word = 0u;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < blocks; b += stride) {
         float f[32];
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __rest
 // the GEMMs uses, on a freshly initialised mbarrier that nothing arrives at. The wait runs
 // out after its limit, records kErrWaitFull in the status word and the kernel returns, so
 // the context stays usable. No asynchronous copy or MMA references the barrier.
-__global__ void __launch_bounds__(32) wait_probe_kernel(uint32_t* status) {
+__global__ void __launch_bounds__(32) wait_probe_kernel(StatusWords status) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x != 0) return;
@@ -294,8 +296,9 @@ __global__ void __launch_bounds__(32) wait_probe_kernel(uint32_t* status) {
 __global__ void __launch_bounds__(kThreads) act_quant_nv_kernel(const uint4* __restrict__ x8,
                                                                 uint2* __restrict__ codes8,
                                                                 uint8_t* __restrict__ sf, int64_t blocks,
-                                                                float g) {
+                                                                float g, uint32_t* clear_word) {
     pdl_wait();
+    if (clear_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *clear_word = 0u;
     const float r = __frcp_rn(__fmul_rn(6.0f, g));
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < blocks; b += stride) {
@@ -414,24 +417,25 @@ cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* ou
 }
 
 cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
-                             int num_sms, cudaStream_t s) {
+                             int num_sms, cudaStream_t s, uint32_t* clear_word) {
     const int64_t blocks = M * (K / 32);
     if (blocks == 0) return cudaSuccess;
     return launch_pdl(act_quant_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
-                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks);
+                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks, clear_word);
 }
 
-cudaError_t launch_wait_probe(uint32_t* status, cudaStream_t s) {
+cudaError_t launch_wait_probe(StatusWords status, cudaStream_t s) {
     wait_probe_kernel<<<1, 32, 0, s>>>(status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M,
-                                   int64_t K, int num_sms, cudaStream_t s) {
+                                   int64_t K, int num_sms, cudaStream_t s, uint32_t* clear_word) {
     const int64_t blocks = M * (K / 16);
     if (blocks == 0) return cudaSuccess;
     return launch_pdl(act_quant_nv_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
-                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(codes), sf, blocks, global_scale);
+                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(codes), sf, blocks, global_scale,
+                      clear_word);
 }
 
 cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,

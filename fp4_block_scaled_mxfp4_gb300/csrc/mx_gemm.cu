@@ -178,7 +178,7 @@ __device__ __forceinline__ int64_t b_tile_row(const GemmArgs& a, int expert, int
 // Every lane polls; the warp proceeds only if all lanes saw the phase complete, so an
 // abort never splits a warp between two code paths.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status, uint32_t code) {
+                                          const StatusWords& status, uint32_t code) {
     return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, status, code)) != 0;
 }
 

@@ -7,6 +7,14 @@
 
 namespace mx {
 
+// Where a bounded device wait that runs out reports (either may be null): the caller's
+// workspace word, which the forward's first kernel clears and mx_check_workspace reads,
+// and the device-wide word that mx_device_status reads.
+struct StatusWords {
+    uint32_t* ws;
+    uint32_t* dev;
+};
+
 // Launch a kernel of the forward with programmatic stream serialisation (see pdl_wait in
 // mx_device.cuh): it may be scheduled before the previous kernel in the stream completes and
 // waits for it on the device.
@@ -68,7 +76,7 @@ struct GemmArgs {
     int64_t ld_hq, ld_hs;
     uint16_t* y;                 // L2: BF16 output [rows, ld_y]
     int64_t ld_y;
-    uint32_t* status;            // device status word
+    StatusWords status;          // where a wait that runs out reports
     // NVFP4 only. Without w_global the output is scaled by alpha (the product of the two
     // operands' globals). With it, alpha is the activation's global and each expert's
     // weight global(s) multiply it in the kernel: L1 w_global[2e] (gate), [2e + 1] (up);
@@ -114,13 +122,15 @@ cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* sf, float 
                                  int64_t rows, int64_t cols, int num_sms, cudaStream_t s);
 cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* out, int64_t rows,
                                int64_t cols, int num_sms, cudaStream_t s);
+// The activation quantisers; clear_word (optional): a forward's workspace status word, set
+// to zero once this kernel may touch global memory (the forward's first kernel does this).
 cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
-                             int num_sms, cudaStream_t s);
+                             int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr);
 // NVFP4 activation quantisation with the float32 global (codes [M, K/2], E4M3 sf [M, K/16]).
 cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M,
-                                   int64_t K, int num_sms, cudaStream_t s);
+                                   int64_t K, int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr);
 // Failure-path self-test: a bounded wait on a barrier nothing arrives at (see mx_elementwise.cu).
-cudaError_t launch_wait_probe(uint32_t* status, cudaStream_t s);
+cudaError_t launch_wait_probe(StatusWords status, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,
                            int64_t T, int64_t K, int64_t H, int num_sms, cudaStream_t s);
 
@@ -138,8 +148,9 @@ struct RouteBufs {
     int32_t* num_mtiles;     // [1]
     int64_t nchunks;
 };
+// clear_word: as for launch_act_quant.
 cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, const RouteBufs& rb,
-                         cudaStream_t s);
+                         cudaStream_t s, uint32_t* clear_word = nullptr);
 // Quantise each token row once (MXFP4, or NVFP4 with the float32 global) and write it to the
 // rows of all its routed pairs; also writes row_of (needs launch_route first).
 cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,

@@ -44,8 +44,11 @@ extern "C" int moe_mxfp4_forward_noalloc(const void* x, const int32_t* topk_ids,
                                          const uint8_t* s2, void* out, int64_t T, int64_t H, int64_t I,
                                          int64_t E, int64_t K, mx_stream_t stream) {
     const int routed = topk_ids != nullptr ? 1 : 0;
+    // argument rules first, in moe_mxfp4_forward's order and with no CUDA call, so both
+    // entry points return the same status: routing ids and weights come together, then
+    // the size rules, then the scratch limit
+    if ((topk_ids != nullptr) != (topk_w != nullptr)) return MX_ERR_INVALID_ARG;
     int64_t layout[8];
-    // size rules first, with no CUDA call: the same status moe_mxfp4_forward would return
     if (int st = moe_mxfp4_workspace_layout(T, H, I, E, K, routed, layout)) return st;
     if (moe_mxfp4_workspace_size(T, H, I, E, K, routed) > MXFP4MOE_NOALLOC_SCRATCH_BYTES) return MX_ERR_WORKSPACE;
     if (T == 0) return MX_OK;

@@ -26,10 +26,13 @@ constexpr int kCountWarps = kCountThreads / 32;
 __global__ void __launch_bounds__(kCountThreads) route_count_kernel(const int32_t* __restrict__ ids,
                                                                     int64_t n_pairs, int E,
                                                                     int32_t* __restrict__ chunk_counts,
-                                                                    int32_t* __restrict__ local_rank) {
+                                                                    int32_t* __restrict__ local_rank,
+                                                                    uint32_t* clear_word) {
     __shared__ int32_t s_run[kMaxExperts];
     __shared__ int32_t s_warp[kCountWarps][kMaxExperts];
     pdl_wait();
+    // the forward's first kernel: its workspace status word starts at zero
+    if (clear_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *clear_word = 0u;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < E; e += kCountThreads) s_run[e] = 0;
     const int64_t base = (int64_t)blockIdx.x * kRouteChunk;
@@ -167,11 +170,11 @@ __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
 }  // namespace
 
 cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, const RouteBufs& rb,
-                         cudaStream_t s) {
+                         cudaStream_t s, uint32_t* clear_word) {
     const int64_t n = T * K;
     if (n == 0) return cudaSuccess;
     const cudaError_t err = launch_pdl(route_count_kernel, dim3((unsigned)rb.nchunks), dim3(kCountThreads), 0, s, ids,
-                                       n, (int)E, rb.chunk_counts, rb.local_rank);
+                                       n, (int)E, rb.chunk_counts, rb.local_rank, clear_word);
     if (err != cudaSuccess) return err;
     return launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, rb.chunk_counts, rb.nchunks, (int)E, rb);
 }

@@ -31,9 +31,11 @@
  *   - Base pointers must be 16-byte aligned (MX_ERR_MISALIGNED otherwise).
  *   - Arguments are validated before anything is launched; on any error nothing is launched.
  *     A CUDA launch error maps to MX_ERR_CUDA.
- *   - Kernels never trap. Every device-side wait is bounded; a wait that runs out sets a
- *     device status word and the kernel returns early. mx_device_status() reads (and
- *     optionally clears) that word.
+ *   - Kernels never trap. Every device-side wait is bounded; a wait that runs out records a
+ *     code and the kernel returns early. A call with a workspace records it in the
+ *     workspace's status word (its first 16 bytes; the call's first kernel clears it), read
+ *     for one stream by mx_check_workspace(); every call also records it in a device-wide
+ *     word that mx_device_status() reads (and optionally clears).
  *   - NaN results are written as 0x7FC0 with the element's sign bit.
  */
 #ifndef MXFP4MOE_H
@@ -70,6 +72,19 @@ int mx_version(void);
 int mx_device_status(int clear);
 
 /*
+ * mx_check_workspace -- the device status of the last forward (moe_mxfp4_forward and its
+ * variants, moe_nvfp4_forward) launched on `stream` with this workspace ("Current Bug: vLLM
+ * produces empty/garbage output", "Phase 1: CuTeDSL Shared Expert Kernel": the experts
+ * runner owns pre-allocated buffers; this is their error channel). Waits for `stream` only
+ * (other streams keep running), then returns MX_OK, or MX_ERR_DEVICE_TIMEOUT when one of
+ * that forward's bounded waits ran out (its output is then incomplete). `clear` != 0 zeroes
+ * the word afterwards (the next forward on the workspace zeroes it too, so check before
+ * reusing the workspace). Returns MX_ERR_INVALID_ARG for a null workspace,
+ * MX_ERR_MISALIGNED unless it is 256-byte aligned, MX_ERR_CUDA if a CUDA call fails.
+ */
+int mx_check_workspace(const void* workspace, int clear, mx_stream_t stream);
+
+/*
  * mx_selftest_wait_timeout -- exercises the failure path of the bounded device waits: launches
  * a one-thread kernel on `stream` that waits, with the same bounded wait the GEMM pipelines use
  * (about 2 s), on a barrier nothing arrives at. When the wait runs out the kernel records a
@@ -78,6 +93,14 @@ int mx_device_status(int clear);
  * launched, MX_ERR_CUDA if the launch fails.
  */
 int mx_selftest_wait_timeout(mx_stream_t stream);
+
+/*
+ * mx_selftest_wait_timeout_ws -- mx_selftest_wait_timeout whose timeout is also recorded in
+ * the status word of `workspace` (256-byte aligned device memory of at least 16 bytes), as a
+ * forward's would be: mx_check_workspace(workspace, ., stream) then reports
+ * MX_ERR_DEVICE_TIMEOUT. For tests only.
+ */
+int mx_selftest_wait_timeout_ws(void* workspace, mx_stream_t stream);
 
 /*
  * mxfp4_dequant -- MXFP4 -> BF16 ([DQ] item 2, [FMT]).
@@ -253,6 +276,8 @@ int moe_mxfp4_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64
  *   1 <= K <= 64; T >= 0 (T == 0 launches nothing). workspace: device memory of at least
  *   moe_mxfp4_workspace_size(T, H, I, E, K, topk_ids != NULL) bytes, 256-byte aligned, not
  *   used by another call that runs at the same time.
+ *   Weight scales given here row-major are gathered per GEMM stage; the faster route is to
+ *   convert them once at load time and call moe_mxfp4_forward_tiled.
  */
 int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_w,
                       const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
@@ -265,7 +290,12 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
  * layout (s13_tiled = mxfp4_scales_to_tiled of s13 viewed as [E*2I, H/32]; s2_tiled of s2
  * viewed as [E*H, I/32]). A weight-format transform done once when the weights are loaded;
  * the GEMMs then fetch each stage's weight scales with two bulk copies instead of one small
- * copy per row. Same arguments, results and errors otherwise.
+ * copy per row. Same arguments, results (bit for bit) and errors otherwise.
+ *   This is the fast path: convert the weight scales once at load time and call this entry
+ * point. With the checkpoint's row-major scales (moe_mxfp4_forward) each GEMM stage
+ * gathers its weight scales as 4-byte copies, which makes the routed prefill forward
+ * (T = 8192, H = 7168, I = 3072, 48 experts, top-8) about 25 % slower on a GB300
+ * (2.48 ms against 1.98 ms).
  */
 int moe_mxfp4_forward_tiled(const void* x, const int32_t* topk_ids, const float* topk_w,
                             const uint8_t* w13, const uint8_t* s13_tiled, const uint8_t* w2,
@@ -363,11 +393,15 @@ int moe_nvfp4_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64
  * (for H = 7168, I = 3072, top-8 that is about 200 routed tokens; use moe_mxfp4_forward
  * with a caller workspace for larger batches).
  *   The first call on each device looks up the scratch area's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture. All calls on a device share the one scratch area and it keeps the last call's
- * contents (no result depends on them): calls that may overlap on the GPU (different
- * streams, or different host threads without ordering) race on it and must be serialised
- * by the caller.
+ * (cudaGetSymbolAddress) with that device current. Under CUDA's lazy module loading (the
+ * default) that lookup is also what loads the library's device code and creates the
+ * 32 MiB array on that device, so the first call may itself take device memory and
+ * synchronise: make it once per device at initialisation (a call with T = 1 will do),
+ * before other allocators reserve the device's memory and before any stream capture.
+ * Later calls allocate nothing. All calls on a device share the one scratch area and it
+ * keeps the last call's contents (no result depends on them): calls that may overlap on
+ * the GPU (different streams, or different host threads without ordering) race on it and
+ * must be serialised by the caller.
  */
 int moe_mxfp4_forward_noalloc(const void* x, const int32_t* topk_ids, const float* topk_w,
                               const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,

@@ -11,6 +11,13 @@ MOE_COS = 0.9999
 
 _built = False
 
+# Canary guard bands (the stand-in for an out-of-bounds checker, which this pool does not
+# offer): a guarded tensor sits inside a larger device buffer whose bytes before and after
+# it hold CANARY; check_canaries() asserts that no kernel wrote into them.
+CANARY = 0xA5
+GUARD_BYTES = 4096                 # a multiple of 256: the tensor keeps the workspace alignment
+_guarded: list = []
+
 
 def native():
     """Build (once per process) and return the binding module."""
@@ -21,6 +28,32 @@ def native():
         build.build()
         _built = True
     return m
+
+
+def guarded_empty(shape, dtype, guard: int = GUARD_BYTES):
+    """An uninitialised device tensor with canary-filled guard bands on both sides."""
+    import torch
+    shape = tuple(int(v) for v in (shape if isinstance(shape, (tuple, list)) else (shape,)))
+    nbytes = int(np.prod(shape, dtype=np.int64)) * torch.empty((), dtype=dtype).element_size()
+    raw = torch.full((guard + nbytes + guard,), CANARY, dtype=torch.uint8, device="cuda")
+    t = raw[guard: guard + nbytes].view(dtype).view(shape)
+    _guarded.append((raw, guard, nbytes))
+    return t
+
+
+def check_canaries() -> int:
+    """Assert every guard band registered since the last call is intact; returns how many
+    buffers were checked."""
+    bufs = list(_guarded)
+    _guarded.clear()
+    for raw, guard, nbytes in bufs:
+        before = raw[:guard].cpu().numpy()            # only the bands come back to the host
+        after = raw[guard + nbytes:].cpu().numpy()
+        for name, band in (("before", before), ("after", after)):
+            bad = np.nonzero(band != CANARY)[0]
+            assert bad.size == 0, (f"a kernel wrote {bad.size} byte(s) into the guard band {name} a buffer of "
+                                   f"{nbytes} bytes (first at offset {int(bad[0])} of the band)")
+    return len(bufs)
 
 
 def dev(a: np.ndarray, dtype=None):

@@ -9,12 +9,17 @@ every step is checked where it happens:
    boundary may legitimately land on either side. Each GPU block (scale + 32 codes) must be
    the MX quantisation of some h' whose elements lie in the interval that the float32
    accumulation allowance and float32 SiLU allow around the oracle's h (decisions that
-   the oracle pins uniquely must match exactly);
+   the oracle pins uniquely must match exactly). The number of blocks whose decision
+   differs from the oracle's own is bounded too: at most FLIP_FRAC of all blocks (never
+   less than FLIP_MIN), so a systematic drift that stays inside every block's window
+   (a biased SiLU, a lossy accumulation) still fails;
 3. y (L2, BF16): within one BF16 rounding plus the float32 accumulation allowance of the
    exact product of the GPU's own hq with w2;
 4. out: per element |err| <= 2e-2 * max|ref| + 1e-3 and cosine >= 0.9999 against the
-   oracle run on the same decisions (the GPU's hq), and cosine >= 0.9999 against the
-   unconditioned oracle.
+   oracle run on the same decisions (the GPU's hq); against the unconditioned oracle,
+   cosine >= 0.9999 over the sample and the same per-element bound on every token whose
+   re-quant decisions all equal the oracle's (a token with a flipped block legitimately
+   differs by a whole E2M1 step of h times a column of w2).
 """
 from __future__ import annotations
 
@@ -22,10 +27,45 @@ import numpy as np
 
 import oracle
 from oracle.mxfp4_oracle import _e2m1_round_magnitude
-from gpu_util import MOE_COS, assert_gemm_close, assert_moe_close, bf16_host, bits_to_f64, cosine
+from gpu_util import (MOE_ABS, MOE_COS, MOE_REL, assert_gemm_close, assert_moe_close, bf16_host, bits_to_f64,
+                      cosine)
 
 ACC_ALLOW = 2.0 ** -14      # float32 accumulation allowance, relative to sum |a||b|
 SILU_ALLOW = 2.0 ** -20     # float32 SiLU / product allowance, relative
+# Re-quant blocks allowed to differ from the oracle's decision (step 2). A block differs
+# only where the float32 accumulation or SiLU moves one of its BF16 or E2M1 decisions
+# across a boundary; measured on the full-size shared, decode and prefill configs in both
+# formats that is 1.6e-4 to 6e-4 of the blocks. The cap is 2^-9 (about 2e-3), three to
+# twelve times that, with a floor of 4 blocks for small samples.
+FLIP_FRAC = 2.0 ** -9
+FLIP_MIN = 4
+
+
+def flip_cap(blocks: int) -> int:
+    return max(FLIP_MIN, int(FLIP_FRAC * blocks))
+
+
+def tile_edge_tokens(topk_ids, E: int, tail_tiles: int = 2, per_tail: int = 4, tile_rows: int = 128):
+    """A token sample for the large routed configs chosen where grouped-GEMM indexing bugs
+    would show: for every expert, the tokens of its first row, of the first row of its last
+    128-row M tile and of its last row (the ragged end), plus per_tail tokens spread over each
+    of the last tail_tiles M tiles of the grouped order (the work units the persistent GEMM
+    grid takes last). The routing comes from the oracle's permutation, which the routing
+    tests pin bit-exactly to the GPU's."""
+    counts, offsets, _, tok_of = oracle.moe_route(topk_ids, E)
+    pick = set()
+    tiles = []
+    for e in range(E):
+        n = int(counts[e])
+        if n == 0:
+            continue
+        o = int(offsets[e])
+        last_tile0 = o + ((n - 1) // tile_rows) * tile_rows
+        pick.update(int(tok_of[r]) for r in (o, last_tile0, o + n - 1))
+        tiles += [(o + m * tile_rows, min(tile_rows, n - m * tile_rows)) for m in range((n + tile_rows - 1) // tile_rows)]
+    for r0, n in tiles[-tail_tiles:]:
+        pick.update(int(tok_of[r]) for r in np.linspace(r0, r0 + n - 1, per_tail).astype(np.int64))
+    return np.array(sorted(pick), dtype=np.int64)
 
 
 def _ws_view(ws, off, rows, cols, dtype=None):
@@ -43,7 +83,8 @@ def _signed_code_value(mag_code, neg):
 
 
 def check_requant_decisions(g, u, absg, absu, hq_gpu, hs_gpu):
-    """Step 2. Returns (blocks, blocks differing from the oracle's own decision)."""
+    """Step 2. Returns (differ [n, I/32]: the block's decision differs from the oracle's own,
+    at_risk: blocks whose admissible window holds more than one outcome)."""
     n, I = g.shape
     to = oracle.bf16_bits_to_f64
     fr = oracle.bf16_bits_from_f64
@@ -87,7 +128,8 @@ def check_requant_decisions(g, u, absg, absu, hq_gpu, hs_gpu):
     ref_q, ref_s = oracle.act_quant_mxfp4(oracle.swiglu_bf16(g, u))
     differ = (ref_s != hs_gpu) | (oracle.unpack_nibbles(ref_q).reshape(n, nb, 32) !=
                                   nib.reshape(n, nb, 32)).any(-1)
-    return n * nb, int(differ.sum())
+    at_risk = (E_lo != E_hi) | (v_lo != v_hi).reshape(n, nb, 32).any(-1)
+    return differ, int(at_risk.sum())
 
 
 def check_moe_run(mx, d, tokens=None) -> dict:
@@ -119,7 +161,7 @@ def check_moe_run(mx, d, tokens=None) -> dict:
         np.testing.assert_array_equal(xs_all[rows], xs_ref[live], err_msg="xs")
     xv = oracle.mxfp4_values(xq_ref, xs_ref)
 
-    blocks = differ = 0
+    flips = _Flips(tok.size, ids.shape[1])
     y_cond = np.zeros((tok.size, ids.shape[1], H))
     for e in range(E):
         sel = np.argwhere((ids == e))
@@ -131,9 +173,8 @@ def check_moe_run(mx, d, tokens=None) -> dict:
         gu = xv[i_s] @ W13.T
         agu = np.abs(xv[i_s]) @ np.abs(W13).T
         del W13
-        b, dff = check_requant_decisions(gu[:, :I], gu[:, I:], agu[:, :I], agu[:, I:], hq_all[rows], hs_all[rows])
-        blocks += b
-        differ += dff
+        flips.add(i_s, k_s, *check_requant_decisions(gu[:, :I], gu[:, I:], agu[:, :I], agu[:, I:], hq_all[rows],
+                                                      hs_all[rows]))
         # 3. L2 on the GPU's own decisions
         W2 = oracle.mxfp4_values(inp.w2[e], inp.s2[e])
         hv = oracle.mxfp4_values(hq_all[rows], hs_all[rows])
@@ -149,11 +190,47 @@ def check_moe_run(mx, d, tokens=None) -> dict:
         stats = assert_moe_close(out_gpu, oracle.bf16_bits_from_f64(y_cond[:, 0]),
                                  "out vs oracle on the GPU's re-quant decisions")
     ref = oracle.moe_forward(inp.x, inp.topk_ids, inp.topk_w, inp.w13, inp.s13, inp.w2, inp.s2, I, tokens=tok)
-    cos = cosine(bits_to_f64(out_gpu), bits_to_f64(ref))
+    return _unconditioned(stats, flips, out_gpu, ref)
+
+
+class _Flips:
+    """Step 2's tally: blocks checked, blocks whose decision differs from the oracle's, blocks
+    at risk, and which (token, slot) rows hold a differing block."""
+
+    def __init__(self, n, K):
+        self.blocks = self.differ = self.at_risk = 0
+        self.row = np.zeros((n, K), dtype=bool)
+
+    def add(self, i_s, k_s, differ, at_risk):
+        self.blocks += differ.size
+        self.differ += int(differ.sum())
+        self.at_risk += at_risk
+        self.row[i_s, k_s] |= differ.any(-1)
+
+    def check(self):
+        cap = flip_cap(self.blocks)
+        assert self.differ <= cap, (f"{self.differ} of {self.blocks} re-quant blocks differ from the oracle's "
+                                    f"decision (cap {cap}; {self.at_risk} at risk)")
+        return cap
+
+
+def _unconditioned(stats, flips, out_gpu, ref):
+    """Step 4 against the plain oracle: cosine over the sample, the per-element bound on
+    every token whose re-quant decisions all equal the oracle's."""
+    cap = flips.check()
+    g, r = bits_to_f64(out_gpu), bits_to_f64(ref)
+    cos = cosine(g, r)
     assert cos >= MOE_COS, f"cosine vs the unconditioned oracle {cos:.6f} < {MOE_COS}"
-    err = np.abs(bits_to_f64(out_gpu) - bits_to_f64(ref))
-    stats.update(requant_blocks=blocks, requant_blocks_differing=differ, e2e_cos=cos,
-                 e2e_max_err=float(err.max()), e2e_bound=float(2e-2 * np.abs(bits_to_f64(ref)).max() + 1e-3))
+    err = np.abs(g - r)
+    bound = MOE_REL * np.abs(r).max() + MOE_ABS
+    clean = ~flips.row.any(-1)
+    err_clean = float(err[clean].max()) if clean.any() else 0.0
+    assert err_clean <= bound, (f"unconditioned max |err| {err_clean:.4g} > {bound:.4g} on tokens whose re-quant "
+                                f"decisions all equal the oracle's")
+    stats.update(requant_blocks=flips.blocks, requant_blocks_differing=flips.differ,
+                 requant_blocks_at_risk=flips.at_risk, requant_flip_cap=cap, e2e_cos=cos,
+                 e2e_max_err=float(err.max()), e2e_max_err_clean_tokens=err_clean, e2e_bound=float(bound),
+                 clean_tokens=int(clean.sum()), tokens=int(clean.size))
     return stats
 
 
@@ -171,8 +248,8 @@ def _nv_scale_bytes(amax, global_scale):
 def check_nv_requant_decisions(g, u, absg, absu, hq_gpu, hs_gpu, h_global):
     """Step 2 for NVFP4: every GPU block (E4M3 scale + 16 codes) must be the NVFP4
     quantisation of some h' in the interval the float32 accumulation and SiLU allow around
-    the oracle's h. g, u, absg, absu already carry the global scales. Returns (blocks,
-    blocks differing from the oracle's own decision)."""
+    the oracle's h. g, u, absg, absu already carry the global scales. Returns (differ
+    [n, I/16], at_risk) as check_requant_decisions."""
     n, I = g.shape
     to = oracle.bf16_bits_to_f64
     fr = oracle.bf16_bits_from_f64
@@ -216,7 +293,8 @@ def check_nv_requant_decisions(g, u, absg, absu, hq_gpu, hs_gpu, h_global):
     ref_q, ref_s = oracle.nvfp4_quantize(oracle.swiglu_bf16(g, u), h_global)
     differ = (ref_s != hs_gpu) | (oracle.unpack_nibbles(ref_q).reshape(n, nb, 16) !=
                                   nib.reshape(n, nb, 16)).any(-1)
-    return n * nb, int(differ.sum())
+    at_risk = (S_lo != S_hi) | (v_lo != v_hi).reshape(n, nb, 16).any(-1)
+    return differ, int(at_risk.sum())
 
 
 def check_nvfp4_moe_run(mx, d, tokens=None) -> dict:
@@ -246,7 +324,7 @@ def check_nvfp4_moe_run(mx, d, tokens=None) -> dict:
         np.testing.assert_array_equal(xs_all[rows], xs_ref[live], err_msg="xs")
     xv = oracle.nvfp4_values(xq_ref, xs_ref, 1.0)
 
-    blocks = differ = 0
+    flips = _Flips(tok.size, ids.shape[1])
     y_cond = np.zeros((tok.size, ids.shape[1], H))
     for e in range(E):
         sel = np.argwhere(ids == e)
@@ -259,10 +337,8 @@ def check_nvfp4_moe_run(mx, d, tokens=None) -> dict:
         agu = np.abs(xv[i_s]) @ np.abs(W13).T
         del W13
         ag, au = gx * float(inp.g13[e, 0]), gx * float(inp.g13[e, 1])
-        b, dff = check_nv_requant_decisions(gu[:, :I] * ag, gu[:, I:] * au, agu[:, :I] * abs(ag),
-                                            agu[:, I:] * abs(au), hq_all[rows], hs_all[rows], gh)
-        blocks += b
-        differ += dff
+        flips.add(i_s, k_s, *check_nv_requant_decisions(gu[:, :I] * ag, gu[:, I:] * au, agu[:, :I] * abs(ag),
+                                                         agu[:, I:] * abs(au), hq_all[rows], hs_all[rows], gh))
         # 3. L2 on the GPU's own decisions
         W2 = oracle.nvfp4_values(inp.w2[e], inp.s2[e], 1.0)
         hv = oracle.nvfp4_values(hq_all[rows], hs_all[rows], 1.0)
@@ -279,9 +355,4 @@ def check_nvfp4_moe_run(mx, d, tokens=None) -> dict:
     stats = assert_moe_close(out_gpu, ref_cond, "out vs oracle on the GPU's re-quant decisions")
     ref = oracle.moe_nvfp4_forward(inp.x, inp.topk_ids, inp.topk_w, inp.w13, inp.s13, inp.g13, inp.w2, inp.s2,
                                    inp.g2, inp.x_global, inp.h_global, I, tokens=tok)
-    cos = cosine(bits_to_f64(out_gpu), bits_to_f64(ref))
-    assert cos >= MOE_COS, f"cosine vs the unconditioned oracle {cos:.6f} < {MOE_COS}"
-    err = np.abs(bits_to_f64(out_gpu) - bits_to_f64(ref))
-    stats.update(requant_blocks=blocks, requant_blocks_differing=differ, e2e_cos=cos,
-                 e2e_max_err=float(err.max()), e2e_bound=float(2e-2 * np.abs(bits_to_f64(ref)).max() + 1e-3))
-    return stats
+    return _unconditioned(stats, flips, out_gpu, ref)

@@ -45,6 +45,13 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_check_workspace_validation(lib):
+    assert lib.mx_check_workspace(None, 1, None) == MX_ERR_INVALID_ARG
+    assert lib.mx_check_workspace(FAKE + 16, 1, None) == MX_ERR_MISALIGNED
+    assert lib.mx_selftest_wait_timeout_ws(None, None) == MX_ERR_INVALID_ARG
+    assert lib.mx_selftest_wait_timeout_ws(FAKE + 16, None) == MX_ERR_MISALIGNED
+
+
 def test_status_strings(lib):
     assert lib.mx_status_string(0) == b"MX_OK"
     assert lib.mx_status_string(4) == b"MX_ERR_WORKSPACE"

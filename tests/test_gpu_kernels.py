@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import assert_gemm_close, bf16_host, dev, native
+from gpu_util import assert_gemm_close, bf16_host, dev, guarded_empty, native
 from workloads import f32_to_bf16_bits, make_dequant_inputs, make_nvfp4_scales
 
 pytestmark = pytest.mark.gpu
@@ -28,8 +28,8 @@ def mx():
 
 
 def _empty(shape, dtype):
-    import torch
-    return torch.empty(shape, dtype=dtype, device="cuda")
+    """An output buffer with canary guard bands, checked after the test."""
+    return guarded_empty(shape, dtype)
 
 
 # ----------------------------------------------------------------------------- dequant
@@ -153,7 +153,7 @@ def test_act_quant_bit_exact(mx, M, K):
 def _tiled(mx, sb):
     import torch
     rows, kb = sb.shape
-    out = torch.empty(mx.mxfp4_tiled_scales_bytes(rows, 32 * kb), dtype=torch.uint8, device="cuda")
+    out = _empty(mx.mxfp4_tiled_scales_bytes(rows, 32 * kb), torch.uint8)
     mx.mxfp4_scales_to_tiled(dev(sb), out)
     return out
 
@@ -245,7 +245,7 @@ def test_gemm_random(mx, M, N, K):
 def _nv_tiled(mx, sf):
     import torch
     rows, kb = sf.shape
-    out = torch.empty(mx.nvfp4_tiled_scales_bytes(rows, 16 * kb), dtype=torch.uint8, device="cuda")
+    out = _empty(mx.nvfp4_tiled_scales_bytes(rows, 16 * kb), torch.uint8)
     mx.nvfp4_scales_to_tiled(dev(sf), out)
     return out
 
@@ -301,7 +301,7 @@ def test_route_bit_exact(mx, T, K, E):
     ids = rng.integers(-1, E + 1, size=(T, K)).astype(np.int32)      # includes dropped ids
     if T >= 100:
         ids[: T // 2, 0] = 0                                          # one expert with many tiles
-    ws = torch.empty(mx.moe_mxfp4_workspace_size(T, 128, 128, E, K, True), dtype=torch.uint8, device="cuda")
+    ws = _empty(mx.moe_mxfp4_workspace_size(T, 128, 128, E, K, True), torch.uint8)
     counts = _empty((E,), torch.int32)
     offsets = _empty((E + 1,), torch.int32)
     row_of = _empty((T, K), torch.int32)

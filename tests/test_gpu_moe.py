@@ -10,8 +10,8 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import assert_moe_close, bf16_host, dev, native
-from moe_check import check_moe_run
+from gpu_util import assert_moe_close, bf16_host, dev, guarded_empty, native
+from moe_check import check_moe_run, tile_edge_tokens
 from workloads import make_config_inputs, make_moe_inputs
 
 pytestmark = pytest.mark.gpu
@@ -38,9 +38,9 @@ class Dev:
         self.ids = dev(inp.topk_ids) if inp.topk_ids is not None else None
         self.w = dev(inp.topk_w) if inp.topk_w is not None else None
         self.w13, self.s13, self.w2, self.s2 = (dev(a) for a in (inp.w13, inp.s13, inp.w2, inp.s2))
-        self.out = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
+        self.out = guarded_empty((inp.T, inp.H), torch.bfloat16)
         n = mx.moe_mxfp4_workspace_size(inp.T, inp.H, inp.I, inp.E, inp.K, self.ids is not None)
-        self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
+        self.ws = guarded_empty(max(n, 256), torch.uint8)
 
     def run(self, mx, stream=None, tiled=False):
         if tiled:
@@ -58,6 +58,7 @@ class Dev:
         else:
             mx.moe_mxfp4_forward(self.x, self.ids, self.w, self.w13, self.s13, self.w2, self.s2, self.out,
                                  self.ws, stream=stream)
+        assert mx.check_workspace(self.ws, stream=stream) == 0, "a bounded device wait ran out"
         return bf16_host(self.out)
 
 
@@ -158,20 +159,23 @@ def test_shared_config_full(mx):
     np.testing.assert_array_equal(d.run(mx, tiled=True), plain)
 
 
-def test_decode_config_sampled(mx):
+def test_decode_config_full(mx):
     inp = make_config_inputs("decode")
     d = Dev(mx, inp)
     plain = d.run(mx)
-    print("decode", check_moe_run(mx, d, tokens=[0, 17, 42, 63]))
+    print("decode", check_moe_run(mx, d))                       # all 64 tokens
     np.testing.assert_array_equal(d.run(mx, tiled=True), plain)
 
 
 def test_prefill_config_sampled(mx):
+    """The prefill forward on every expert's first and last (ragged) M tile and on the tiles
+    the persistent grid takes last: the sample the bench's workload is checked on, in the
+    launch configuration the bench times (tile-layout weight scales)."""
     inp = make_config_inputs("prefill")
     d = Dev(mx, inp)
-    got = d.run(mx)
+    got = d.run(mx, tiled=True)
     assert np.isfinite((got.astype(np.uint32) << 16).view(np.float32)).all()
-    rng = np.random.default_rng(5)
-    tokens = np.sort(rng.choice(inp.T, size=6, replace=False))
+    tokens = tile_edge_tokens(inp.topk_ids, inp.E)
+    assert tokens.size >= 64
     print("prefill", check_moe_run(mx, d, tokens=tokens))
-    np.testing.assert_array_equal(d.run(mx, tiled=True), got)
+    np.testing.assert_array_equal(d.run(mx), got)

@@ -12,8 +12,8 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import bf16_host, dev, native
-from moe_check import check_nvfp4_moe_run
+from gpu_util import bf16_host, dev, guarded_empty, native
+from moe_check import check_nvfp4_moe_run, tile_edge_tokens
 from workloads import f32_to_bf16_bits, make_nvfp4_config_inputs, make_nvfp4_moe_inputs
 
 pytestmark = pytest.mark.gpu
@@ -91,9 +91,9 @@ class NvDev:
         self.s2t = torch.empty(mx.nvfp4_tiled_scales_bytes(inp.E * inp.H, inp.I), dtype=torch.uint8, device="cuda")
         mx.nvfp4_scales_to_tiled(dev(inp.s13.reshape(-1, inp.H // 16)), self.s13t)
         mx.nvfp4_scales_to_tiled(dev(inp.s2.reshape(-1, inp.I // 16)), self.s2t)
-        self.out = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
+        self.out = guarded_empty((inp.T, inp.H), torch.bfloat16)
         n = mx.moe_nvfp4_workspace_size(inp.T, inp.H, inp.I, inp.E, inp.K, self.ids is not None)
-        self.ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
+        self.ws = guarded_empty(max(n, 256), torch.uint8)
 
     def launch(self, mx, stream=None):
         inp = self.inp
@@ -102,6 +102,7 @@ class NvDev:
 
     def run(self, mx, stream=None):
         self.launch(mx, stream)
+        assert mx.check_workspace(self.ws, stream=stream) == 0, "a bounded device wait ran out"
         return bf16_host(self.out)
 
 
@@ -139,10 +140,22 @@ def test_nvfp4_shared_config_full(mx):
     print("nvfp4 shared T=256", check_nvfp4_moe_run(mx, d))
 
 
-def test_nvfp4_decode_config_sampled(mx):
+def test_nvfp4_decode_config_full(mx):
     d = NvDev(mx, make_nvfp4_config_inputs("decode"))
     d.run(mx)
-    print("nvfp4 decode", check_nvfp4_moe_run(mx, d, tokens=[0, 21, 50, 63]))
+    print("nvfp4 decode", check_nvfp4_moe_run(mx, d))           # all 64 tokens
+
+
+def test_nvfp4_prefill_config_sampled(mx):
+    """The NVFP4 routed prefill forward the bench reports (T = 8192, 48 experts, top-8, Zipf
+    routing), on every expert's first and last M tile and the tiles scheduled last."""
+    inp = make_nvfp4_config_inputs("prefill")
+    d = NvDev(mx, inp)
+    got = d.run(mx)
+    assert np.isfinite((got.astype(np.uint32) << 16).view(np.float32)).all()
+    tokens = tile_edge_tokens(inp.topk_ids, inp.E)
+    assert tokens.size >= 64
+    print("nvfp4 prefill", check_nvfp4_moe_run(mx, d, tokens=tokens))
 
 
 def test_nvfp4_graph_capture_replays_bit_identical(mx):
