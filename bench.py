@@ -616,18 +616,22 @@ def measure_extra(mx, torch, dev, stream):
                          dtype=torch.uint8, device=dev)
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-        def fwd():
+        def fwd(fused=False):
             flush.zero_()          # keep the weights out of L2 between repetitions
-            mx.moe_mxfp4_forward(x, ids, w, *W, out, ws, stream=stream, scales_tiled=True)
+            mx.moe_mxfp4_forward(x, ids, w, *W, out, ws, stream=stream, scales_tiled=True, fused=fused)
+
+        def fwd_fused():
+            fwd(True)
 
         def only_flush():
             flush.zero_()
 
         ms = timeit(fwd, reps=20) - timeit(only_flush, reps=20)
-        # The same forward replayed as a CUDA graph (the API is capture-safe), which removes
-        # the host launch gaps between its few short kernels.
+        ms_fused = timeit(fwd_fused, reps=20) - timeit(only_flush, reps=20)
+        # The same forwards replayed as CUDA graphs (the API is capture-safe), which removes
+        # the host launch gaps between the multi-kernel forward's few short kernels.
         graphs = []
-        for body in (fwd, only_flush):
+        for body in (fwd, fwd_fused, only_flush):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(stream):
                 body()
@@ -635,14 +639,19 @@ def measure_extra(mx, torch, dev, stream):
             with torch.cuda.graph(g, stream=stream):
                 body()
             graphs.append(g)
-        ms_graph = timeit(graphs[0].replay, reps=20) - timeit(graphs[1].replay, reps=20)
+        t_flush = timeit(graphs[2].replay, reps=20)
+        ms_graph = timeit(graphs[0].replay, reps=20) - t_flush
+        ms_fused_graph = timeit(graphs[1].replay, reps=20) - t_flush
         pairs = int(((inp.topk_ids >= 0) & (inp.topk_ids < c["E"])).sum()) if routed else c["T"]
         touched = np.unique(inp.topk_ids).size if routed else 1
         wbytes = touched * (inp.w13[0].nbytes + inp.s13[0].nbytes + inp.w2[0].nbytes + inp.s2[0].nbytes)
         nbytes = wbytes + inp.x.nbytes * 2
         res[name] = {"ms": ms, "TFLOP/s": pairs * flops_per_pair(c["H"], c["I"]) / ms / 1e9,
                      "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm, "algorithmic_bytes": nbytes,
-                     "graph_ms": ms_graph, "graph_frac_hbm": nbytes / ms_graph / 1e6 / hbm}
+                     "graph_ms": ms_graph, "graph_frac_hbm": nbytes / ms_graph / 1e6 / hbm,
+                     "single_launch_ms": ms_fused, "single_launch_frac_hbm": nbytes / ms_fused / 1e6 / hbm,
+                     "single_launch_graph_ms": ms_fused_graph,
+                     "single_launch_graph_frac_hbm": nbytes / ms_fused_graph / 1e6 / hbm}
         del graphs
         del x, ids, w, W, out, ws, flush
         torch.cuda.empty_cache()

@@ -25,11 +25,13 @@ from ._native import (  # noqa: F401
     mxfp4_gemm_bf16,
     mxfp4_scales_to_tiled,
     mxfp4_tiled_scales_bytes,
+    nvfp4_calibrate_global,
     nvfp4_dequant,
     nvfp4_gemm_bf16,
     nvfp4_gemm_bf16_multi,
     nvfp4_scales_to_tiled,
     nvfp4_tiled_scales_bytes,
+    selftest_grid_barrier_timeout,
     selftest_wait_timeout,
     status_string,
 )

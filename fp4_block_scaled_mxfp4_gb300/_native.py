@@ -25,6 +25,7 @@ _SIGNATURES = {
     "mx_selftest_wait_timeout": (ctypes.c_int, [_c_ptr]),
     "mx_selftest_wait_timeout_ws": (ctypes.c_int, [_c_ptr, _c_ptr]),
     "mx_check_workspace": (ctypes.c_int, [_c_ptr, ctypes.c_int, _c_ptr]),
+    "mx_selftest_grid_barrier_timeout": (ctypes.c_int, [_c_ptr, _c_ptr]),
     "mxfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "fp8_block_dequant_128x128": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "nvfp4_dequant": (ctypes.c_int, [_c_ptr, _c_ptr, ctypes.c_float, _c_ptr, _c_i64, _c_i64, _c_ptr]),
@@ -36,6 +37,7 @@ _SIGNATURES = {
                                              ctypes.c_int, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "act_quant_mxfp4": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "act_quant_nvfp4": (ctypes.c_int, [_c_ptr, ctypes.c_float, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "nvfp4_calibrate_global": (ctypes.c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr]),
     "moe_nvfp4_workspace_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
     "moe_nvfp4_workspace_layout": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int, _c_ptr]),
     "moe_nvfp4_forward": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
@@ -55,6 +57,9 @@ _SIGNATURES = {
                                                _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
                                                _c_ptr, _c_ptr, ctypes.c_int]),
     "moe_mxfp4_forward_tiled": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                               _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
+                                               _c_ptr]),
+    "moe_mxfp4_forward_fused": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
                                                _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
                                                _c_ptr]),
     "moe_mxfp4_forward_noalloc": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
@@ -252,6 +257,19 @@ def act_quant_nvfp4(x, global_scale, codes, sf, stream=None) -> None:
            "act_quant_nvfp4")
 
 
+def nvfp4_calibrate_global(x, amax, global_scale, stream=None) -> None:
+    """Warm-up calibration of an NVFP4 activation global on the GPU: folds the largest finite
+    |x| of the batch x (bf16 [M, K]) into the running maximum amax (float32 [1], device;
+    zero it before the first batch) and writes amax / (6 * 448) to global_scale (float32 [1])."""
+    import torch
+    M, K = x.shape
+    _need(x, x.dtype, (M, K), "x")
+    _need(amax, torch.float32, (1,), "amax")
+    _need(global_scale, torch.float32, (1,), "global_scale")
+    _check(lib().nvfp4_calibrate_global(_ptr(x), M, K, _ptr(amax), _ptr(global_scale), _stream(stream)),
+           "nvfp4_calibrate_global")
+
+
 def mxfp4_tiled_scales_bytes(rows: int, cols: int) -> int:
     return int(lib().mxfp4_tiled_scales_bytes(rows, cols))
 
@@ -299,14 +317,15 @@ def moe_mxfp4_workspace_layout(T: int, H: int, I: int, E: int, K: int, routed: b
 
 
 def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, stream=None, events=None,
-                      scales_tiled=False) -> None:
+                      scales_tiled=False, fused=False) -> None:
     """MoE expert FFN over MXFP4 weights; topk_ids/topk_w None selects the shared expert.
 
     s13 / s2: the row-major E8M0 scales ([E, 2I, H/32], [E, H, I/32]), or with
     scales_tiled=True their tile layout (mxfp4_scales_to_tiled; any uint8 buffer of that
     size). ``events``: optional sequence of 6 torch.cuda.Event (or None) recorded at the
     phase boundaries (before, after routing, after quantisation, after L1, after L2, after
-    combine).
+    combine). ``fused=True`` (tile-layout scales only) runs the whole forward as one
+    persistent kernel launch (moe_mxfp4_forward_fused).
     """
     import torch
     T, H = x.shape
@@ -330,7 +349,11 @@ def moe_mxfp4_forward(x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, str
     ws_bytes = workspace.numel() * workspace.element_size()
     args = (_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(out),
             T, H, I, E, K, _ptr(workspace), ws_bytes, _stream(stream))
-    if events is not None:
+    if fused:
+        if not scales_tiled or events is not None:
+            raise ValueError("the single-launch forward takes tile-layout scales and records no phase events")
+        _check(lib().moe_mxfp4_forward_fused(*args), "moe_mxfp4_forward_fused")
+    elif events is not None:
         evs = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else 0) for e in events])
         _check(lib().moe_mxfp4_forward_timed(*args, ctypes.addressof(evs), 1 if scales_tiled else 0),
                "moe_mxfp4_forward_timed")
@@ -408,6 +431,12 @@ def selftest_wait_timeout(stream=None, workspace=None) -> None:
         _check(lib().mx_selftest_wait_timeout(_stream(stream)), "mx_selftest_wait_timeout")
     else:
         _check(lib().mx_selftest_wait_timeout_ws(_ptr(workspace), _stream(stream)), "mx_selftest_wait_timeout_ws")
+
+
+def selftest_grid_barrier_timeout(workspace, stream=None) -> None:
+    """Launch the grid-barrier failure-path self-test on `workspace` (see the header)."""
+    _check(lib().mx_selftest_grid_barrier_timeout(_ptr(workspace), _stream(stream)),
+           "mx_selftest_grid_barrier_timeout")
 
 
 def check_workspace(workspace, stream=None, clear: bool = True) -> int:

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build", "mxfp4moe")
 LIB_PATH = os.path.join(PKG_DIR, "libmxfp4moe.so")
 SOURCES = ["mx_api.cu", "mx_gemm.cu", "mx_elementwise.cu", "mx_route.cu", "mx_noalloc.cu"]
-HEADERS = ["mx_device.cuh", "mx_internal.h"]
+HEADERS = ["mx_device.cuh", "mx_internal.h", "mx_phases.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

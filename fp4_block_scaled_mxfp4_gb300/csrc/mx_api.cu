@@ -105,12 +105,15 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Bytes of a scale tensor [rows, kb] in the tile layout (128-row groups x 4-byte K-words).
 size_t tiled_bytes(int64_t rows, int64_t kb) { return (size_t)((rows + 127) / 128) * (size_t)(kb / 4) * 512; }
 
-// Workspace layout shared by moe_mxfp4_forward, moe_nvfp4_forward (sf_div 16: one scale
-// per 16 columns) and moe_mxfp4_route. The status word comes first, at offset 0, where
-// mx_check_workspace finds it.
+// Workspace layout shared by moe_mxfp4_forward (and its persistent form), moe_nvfp4_forward
+// (sf_div 16: one scale per 16 columns) and moe_mxfp4_route. The status word comes first, at
+// offset 0, where mx_check_workspace finds it; the persistent forward's grid-barrier counter
+// follows at 256.
+constexpr size_t kWsStatusOff = 0;
+constexpr size_t kWsSyncOff = 256;
 struct WsLayout {
     int64_t R = 0, nchunks = 0, max_mtiles = 0;
-    size_t status = 0, num_mtiles = 0, counts = 0, offsets = 0, chunk_counts = 0, chunk_base = 0, local_rank = 0,
+    size_t status = 0, sync = 0, num_mtiles = 0, counts = 0, offsets = 0, chunk_counts = 0, chunk_base = 0, local_rank = 0,
            row_of = 0, tile_expert = 0, tile_row0 = 0, tile_rows = 0, xq = 0, xs = 0, hq = 0, hs = 0, y = 0,
            total = 0;
 };
@@ -127,6 +130,7 @@ WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool r
         return at;
     };
     L.status = take(16);
+    L.sync = take(16);
     L.num_mtiles = take(16);
     if (routed) {
         L.counts = take(4 * (size_t)E);
@@ -247,6 +251,18 @@ int mx_selftest_wait_timeout_ws(void* workspace, mx_stream_t stream) {
                                          static_cast<cudaStream_t>(stream)));
 }
 
+int mx_selftest_grid_barrier_timeout(void* workspace, mx_stream_t stream) {
+    if (!workspace) return MX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* counter = at<uint32_t>(workspace, kWsSyncOff);
+    if (cudaMemsetAsync(counter, 0, sizeof(uint32_t), s) != cudaSuccess) return MX_ERR_CUDA;
+    return cuda_status(
+        launch_grid_sync_probe(counter, StatusWords{at<uint32_t>(workspace, kWsStatusOff), d->status}, s));
+}
+
 int mx_check_workspace(const void* workspace, int clear, mx_stream_t stream) {
     if (!workspace) return MX_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
@@ -323,6 +339,20 @@ int act_quant_nvfp4(const void* x_bf16, float global_scale, uint8_t* codes, uint
     if (int e = device_info(&d)) return e;
     return cuda_status(launch_act_quant_nvfp4(static_cast<const uint16_t*>(x_bf16), global_scale, codes, sf, M, K,
                                               d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4_calibrate_global(const void* x_bf16, int64_t M, int64_t K, float* amax, float* global_scale,
+                           mx_stream_t stream) {
+    if (M < 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (!amax || !global_scale || (M > 0 && !x_bf16)) return MX_ERR_INVALID_ARG;
+    if ((M > 0 && !aligned16(x_bf16)) || (reinterpret_cast<uintptr_t>(amax) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(global_scale) & 3u) != 0)
+        return MX_ERR_MISALIGNED;
+    if (M > ((int64_t)1 << 40) / K) return MX_ERR_UNSUPPORTED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_nv_calibrate(static_cast<const uint16_t*>(x_bf16), M * K, amax, global_scale,
+                                           d->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 int act_quant_mxfp4(const void* x_bf16, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K, mx_stream_t stream) {
@@ -513,7 +543,7 @@ struct NvGlobals {
 int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
                  const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T, int64_t H,
                  int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream,
-                 void* const* events, bool scales_tiled, const NvGlobals* nv = nullptr) {
+                 void* const* events, bool scales_tiled, const NvGlobals* nv = nullptr, bool fused = false) {
     const bool routed = topk_ids != nullptr;
     if (routed != (topk_w != nullptr)) return MX_ERR_INVALID_ARG;
     if (int e = check_moe_dims(T, H, I, E, K, routed)) return e;
@@ -558,13 +588,8 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
         g2.w_global = nv->g2;
     }
     RouteBufs rb{};
-    if (!mark(0)) return MX_ERR_CUDA;
     if (routed) {
         rb = route_bufs(workspace, L);
-        if (launch_route(topk_ids, T, K, E, rb, s, ws_status) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
-        if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s, nv != nullptr,
-                                nv ? nv->x_global : 0.0f) != cudaSuccess)
-            return MX_ERR_CUDA;
         for (GemmArgs* g : {&g1, &g2}) {
             g->tile_expert = rb.tile_expert;
             g->tile_row0 = rb.tile_row0;
@@ -572,26 +597,20 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
             g->num_mtiles_dev = rb.num_mtiles;
         }
     } else {
-        if (!mark(1)) return MX_ERR_CUDA;
-        const cudaError_t qe =
-            nv ? launch_act_quant_nvfp4(static_cast<const uint16_t*>(x), nv->x_global, xq, xs, T, H, d->num_sms, s,
-                                        ws_status)
-               : launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s, ws_status);
-        if (qe != cudaSuccess) return MX_ERR_CUDA;
         for (GemmArgs* g : {&g1, &g2}) {
             g->num_mtiles_host = (int32_t)((T + kBM - 1) / kBM);
             g->m_total = T;
         }
     }
-    if (!mark(2)) return MX_ERR_CUDA;
     const int64_t max_mtiles = L.max_mtiles;
 
     // Tile widths: 256 columns, or 128 where 256-wide tiles would leave SMs idle. Only with
     // uniform tiling: the routed tile count is known on the device alone, and its bound
-    // max_mtiles counts an extra tile per expert.
-    // NVFP4 runs 256-column tiles only.
-    const int n1 = routed || nv ? kBN : tile_cols(max_mtiles * (I / 128), d->num_sms);
-    const int n2 = routed || nv ? kBN : tile_cols(max_mtiles * ((H + kBN - 1) / kBN), d->num_sms);
+    // max_mtiles counts an extra tile per expert. NVFP4 runs 256-column tiles only. The
+    // persistent forward runs both GEMMs through one pipeline, so one width for both.
+    int n1 = routed || nv ? kBN : tile_cols(max_mtiles * (I / 128), d->num_sms);
+    int n2 = routed || nv ? kBN : tile_cols(max_mtiles * ((H + kBN - 1) / kBN), d->num_sms);
+    if (fused && (n1 == 128 || n2 == 128)) n1 = n2 = 128;
 
     // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
     CUtensorMap ta1, tb1, ty1, ta2, tb2, ty2;
@@ -606,12 +625,6 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     g1.hs = hs;
     g1.ld_hq = I / 2;
     g1.ld_hs = I / sf_div;
-    const int grid1 = grid_for(max_mtiles * g1.n_tiles, d->num_sms);
-    if ((nv ? launch_gemm_nvfp4_l1(ta1, tb1, ty1, g1, grid1, s) : launch_gemm_l1(ta1, tb1, ty1, g1, grid1, scales_tiled,
-                                                                                  n1, s)) != cudaSuccess ||
-        !mark(3))
-        return MX_ERR_CUDA;
-
     // L2: [R, I] x [H, I]^T per expert, BF16 out (to `out` directly without routing).
     if (make_tmap(&ta2, hq, I / 2, R, 128) || make_tmap(&tb2, w2, I / 2, E * H, (uint32_t)n2)) return MX_ERR_CUDA;
     g2.n_tiles = (int32_t)((H + n2 - 1) / n2);
@@ -620,12 +633,56 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     g2.y = routed ? at<uint16_t>(workspace, L.y) : static_cast<uint16_t*>(out);
     g2.ld_y = H;
     if (make_tmap_out(&ty2, g2.y, H, R)) return MX_ERR_CUDA;
+
+    if (fused) {
+        FusedArgs fa;
+        std::memset(&fa, 0, sizeof(fa));
+        fa.g1 = g1;
+        fa.g2 = g2;
+        fa.x = static_cast<const uint16_t*>(x);
+        fa.ids = topk_ids;
+        fa.topk_w = topk_w;
+        fa.out = static_cast<uint16_t*>(out);
+        fa.y = g2.y;
+        fa.xq = xq;
+        fa.xs = xs;
+        fa.rb = rb;
+        fa.T = T;
+        fa.H = H;
+        fa.K = (int32_t)(routed ? K : 1);
+        fa.E = (int32_t)E;
+        fa.sync = at<uint32_t>(workspace, L.sync);
+        fa.clear_word = ws_status;
+        fa.status = g1.status;
+        if (cudaMemsetAsync(fa.sync, 0, sizeof(uint32_t), s) != cudaSuccess) return MX_ERR_CUDA;
+        return cuda_status(launch_moe_fused(ta1, tb1, ty1, ta2, tb2, ty2, fa, n1, d->num_sms, s));
+    }
+
+    if (!mark(0)) return MX_ERR_CUDA;
+    if (routed) {
+        if (launch_route(topk_ids, T, K, E, rb, s, ws_status) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
+        if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s, nv != nullptr,
+                                nv ? nv->x_global : 0.0f) != cudaSuccess)
+            return MX_ERR_CUDA;
+    } else {
+        if (!mark(1)) return MX_ERR_CUDA;
+        const cudaError_t qe =
+            nv ? launch_act_quant_nvfp4(static_cast<const uint16_t*>(x), nv->x_global, xq, xs, T, H, d->num_sms, s,
+                                        ws_status)
+               : launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s, ws_status);
+        if (qe != cudaSuccess) return MX_ERR_CUDA;
+    }
+    if (!mark(2)) return MX_ERR_CUDA;
+    const int grid1 = grid_for(max_mtiles * g1.n_tiles, d->num_sms);
+    if ((nv ? launch_gemm_nvfp4_l1(ta1, tb1, ty1, g1, grid1, s) : launch_gemm_l1(ta1, tb1, ty1, g1, grid1, scales_tiled,
+                                                                                  n1, s)) != cudaSuccess ||
+        !mark(3))
+        return MX_ERR_CUDA;
     const int grid2 = grid_for(max_mtiles * g2.n_tiles, d->num_sms);
     if ((nv ? launch_gemm_nvfp4(ta2, tb2, ty2, g2, grid2, s) : launch_gemm_l2(ta2, tb2, ty2, g2, grid2, scales_tiled,
                                                                               n2, s)) != cudaSuccess ||
         !mark(4))
         return MX_ERR_CUDA;
-
     if (routed) {
         if (launch_combine(at<uint16_t>(workspace, L.y), rb.row_of, topk_w, static_cast<uint16_t*>(out), T, K, H,
                            d->num_sms, s) != cudaSuccess)
@@ -659,6 +716,14 @@ int moe_mxfp4_forward_timed(const void* x, const int32_t* topk_ids, const float*
                             mx_stream_t stream, void* const* events, int scales_tiled) {
     return forward_impl(x, topk_ids, topk_w, w13, s13, w2, s2, out, T, H, I, E, K, workspace, ws_bytes, stream,
                         events, scales_tiled != 0);
+}
+
+int moe_mxfp4_forward_fused(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                            const uint8_t* s13_tiled, const uint8_t* w2, const uint8_t* s2_tiled, void* out,
+                            int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, void* workspace,
+                            size_t ws_bytes, mx_stream_t stream) {
+    return forward_impl(x, topk_ids, topk_w, w13, s13_tiled, w2, s2_tiled, out, T, H, I, E, K, workspace, ws_bytes,
+                        stream, nullptr, true, nullptr, true);
 }
 
 size_t moe_nvfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed) {

@@ -22,6 +22,7 @@ enum : uint32_t {
     kErrWaitTmemFull = 1u << 2,
     kErrWaitTmemEmpty = 1u << 3,
     kErrWaitDrain = 1u << 4,
+    kErrWaitGrid = 1u << 5,
 };
 
 // Upper bound on one wait, in globaltimer nanoseconds. Every legitimate wait in these
@@ -246,6 +247,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             }
         }
     }
+}
+
+// Grid-wide barrier of a cooperative launch (every CTA resident at once). Each CTA makes its
+// earlier global writes visible to the other CTAs, including to their TMA (async-proxy)
+// reads; thread 0 adds the CTA's arrival to `counter` and waits until it reaches `target`
+// (the barrier's cumulative arrival count: gridDim.x per barrier passed). The wait is
+// bounded like an mbarrier wait: past the limit it raises the CTA's abort flag, records
+// kErrWaitGrid and lets the CTA go on. Every thread of the CTA calls it.
+__device__ __forceinline__ void grid_sync(uint32_t* counter, uint32_t target, volatile int* abort_flag,
+                                          const StatusWords& status) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(counter, 1u);
+        uint64_t t0 = 0;
+        for (uint32_t i = 0;; ++i) {
+            uint32_t v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+            if (v >= target) break;
+            if ((i & 63u) == 63u) {
+                const uint64_t t = globaltimer();
+                if (t0 == 0) {
+                    t0 = t;
+                } else if (t - t0 > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    set_status(status, kErrWaitGrid);
+                    break;
+                }
+            }
+            __nanosleep(32);
+        }
+        __threadfence();
+    }
+    __syncthreads();
 }
 
 // ------------------------------------------------------------------------------------

@@ -6,8 +6,7 @@
 // byte, lower nibble first, LUT x E8M0 per row per 32 columns; item 1: FP8 x E8M0 per
 // 128x128 block). Combine per "Current Bug: vLLM produces empty/garbage output", "Phase 1"
 // (routing, top-k, scatter) and "Phase 3: Clean up" (the final scatter is BF16).
-#include "mx_device.cuh"
-#include "mx_internal.h"
+#include "mx_phases.cuh"
 
 namespace mx {
 
@@ -142,40 +141,61 @@ __device__ __forceinline__ uint4 nv_lookup8(uint32_t c, uint32_t hi0, uint32_t h
                       __byte_perm(eb, ob, 0x7632u));
 }
 
+// One 16-element block: 8 code bytes and its scale byte -> 32 bytes of BF16 at out[2b], out[2b + 1].
+__device__ __forceinline__ void nvfp4_block_to_bf16(uint2 c, uint32_t sbyte, float ga, uint32_t gneg, uint4* out) {
+    const float sa = (sbyte & 0x7Fu) == 0x7Fu ? __uint_as_float(0x7FC00000u) : fabsf(e4m3_value(sbyte));
+    // t[k]: BF16 magnitudes of codes 2k (low half) and 2k + 1 (high half)
+    uint32_t t[4];
+    const float m[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    if (isfinite(sa) && isfinite(ga)) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            t[k] = pack_bf16x2(__fmul_rn(__fmul_rn(m[2 * k], sa), ga), __fmul_rn(__fmul_rn(m[2 * k + 1], sa), ga));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t hh[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float v = __fmul_rn(__fmul_rn(m[2 * k + j], sa), ga);
+                hh[j] = v != v ? 0x7FC0u : f32_to_bf16(v);
+            }
+            t[k] = hh[0] | (hh[1] << 16);
+        }
+    }
+    const uint32_t hi0 = __byte_perm(t[0], t[1], 0x7531u), hi1 = __byte_perm(t[2], t[3], 0x7531u);
+    const uint32_t lo0 = __byte_perm(t[0], t[1], 0x6420u), lo1 = __byte_perm(t[2], t[3], 0x6420u);
+    const uint32_t sneg = (((sbyte >> 7) ^ gneg) & 1u) ? 0x80808080u : 0u;
+    out[0] = nv_lookup8(c.x, hi0, hi1, lo0, lo1, sneg);
+    out[1] = nv_lookup8(c.y, hi0, hi1, lo0, lo1, sneg);
+}
+
+// Each thread takes kNvBlocksPerThread blocks a whole grid apart per pass, loading all of
+// them before converting any, so that many loads are in flight per thread: one 8-byte load
+// each left the kernel latency-bound near 70 % of HBM.
+constexpr int kNvBlocksPerThread = 4;
 __global__ void __launch_bounds__(kThreads) nvfp4_dequant_kernel(const uint2* __restrict__ codes8,
                                                                  const uint8_t* __restrict__ sf, float g,
                                                                  uint4* __restrict__ out, int64_t blocks) {
     const uint32_t gneg = __float_as_uint(g) >> 31;
     const float ga = fabsf(g);
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < blocks; b += stride) {
-        const uint2 c = __ldg(codes8 + b);           // elements 16b .. 16b + 15
-        const uint32_t sbyte = __ldg(sf + b);
-        const float sa = (sbyte & 0x7Fu) == 0x7Fu ? __uint_as_float(0x7FC00000u) : fabsf(e4m3_value(sbyte));
-        // t[k]: BF16 magnitudes of codes 2k (low half) and 2k + 1 (high half)
-        uint32_t t[4];
-        const float m[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
-        if (isfinite(sa) && isfinite(ga)) {
+    const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+    for (int64_t b0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; b0 < blocks;
+         b0 += kNvBlocksPerThread * nthreads) {
+        uint2 c[kNvBlocksPerThread];
+        uint32_t sb[kNvBlocksPerThread];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                t[k] = pack_bf16x2(__fmul_rn(__fmul_rn(m[2 * k], sa), ga), __fmul_rn(__fmul_rn(m[2 * k + 1], sa), ga));
-        } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t hh[2];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float v = __fmul_rn(__fmul_rn(m[2 * k + j], sa), ga);
-                    hh[j] = v != v ? 0x7FC0u : f32_to_bf16(v);
-                }
-                t[k] = hh[0] | (hh[1] << 16);
-            }
+        for (int i = 0; i < kNvBlocksPerThread; ++i) {
+            const int64_t b = b0 + i * nthreads;
+            const bool ok = b < blocks;
+            c[i] = ok ? __ldg(codes8 + b) : make_uint2(0u, 0u);
+            sb[i] = ok ? (uint32_t)__ldg(sf + b) : 0u;
         }
-        const uint32_t hi0 = __byte_perm(t[0], t[1], 0x7531u), hi1 = __byte_perm(t[2], t[3], 0x7531u);
-        const uint32_t lo0 = __byte_perm(t[0], t[1], 0x6420u), lo1 = __byte_perm(t[2], t[3], 0x6420u);
-        const uint32_t sneg = (((sbyte >> 7) ^ gneg) & 1u) ? 0x80808080u : 0u;
-        out[2 * b] = nv_lookup8(c.x, hi0, hi1, lo0, lo1, sneg);
-        out[2 * b + 1] = nv_lookup8(c.y, hi0, hi1, lo0, lo1, sneg);
+#pragma unroll
+        for (int i = 0; i < kNvBlocksPerThread; ++i) {
+            const int64_t b = b0 + i * nthreads;
+            if (b < blocks) nvfp4_block_to_bf16(c[i], sb[i], ga, gneg, out + 2 * b);
+        }
     }
 }
 
@@ -249,31 +269,15 @@ __global__ void __launch_bounds__(kThreads) fp8_dequant_kernel(const uint8_t* __
     }
 }
 
-// One thread per 32-element block: four 16-byte loads, one quantisation, a 16-byte code
-// store and a scale byte (consecutive threads write consecutive codes and scales).
+// One thread per 32-element block (act_quant_blocks).
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __restrict__ x8,
                                                              uint4* __restrict__ codes16,
                                                              uint8_t* __restrict__ sf, int64_t blocks,
                                                              uint32_t* clear_word) {
     pdl_wait();
     if (clear_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *clear_word = 0u;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < blocks; b += stride) {
-        float f[32];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 v = __ldg(x8 + 4 * b + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                f[8 * i + 2 * j] = bf16_to_f32(w[j] & 0xFFFFu);
-                f[8 * i + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
-            }
-        }
-        uint4 codes;
-        sf[b] = (uint8_t)mx_quant32(f, codes);
-        codes16[b] = codes;
-    }
+    act_quant_blocks(x8, codes16, sf, blocks, (int64_t)blockIdx.x * kThreads + threadIdx.x,
+                     (int64_t)gridDim.x * kThreads);
     pdl_launch_dependents();
 }
 
@@ -320,37 +324,58 @@ __global__ void __launch_bounds__(kThreads) act_quant_nv_kernel(const uint4* __r
     pdl_launch_dependents();
 }
 
-// out[t, c] = bf16( sum_k w[t,k] * y[row_of[t,k], c] ), float32, slot order, no FMA.
+// NVFP4 activation-global calibration ("Current Bug: vLLM produces empty/garbage output",
+// "Phase 1: CuTeDSL Shared Expert Kernel": a warm-up-based gs). amax_kernel folds the
+// largest finite |x| of a BF16 tensor into a running maximum kept as float32 bits (a
+// non-negative float orders like its bit pattern, so atomicMax on the bits is the float
+// maximum); NaN and infinities are skipped. Each thread reduces its 16-byte vectors (plus
+// the scalar tail), then the warp and the CTA, and one atomic per CTA updates the maximum.
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* __restrict__ x8, int64_t n8,
+                                                        const uint16_t* __restrict__ tail, int ntail,
+                                                        uint32_t* __restrict__ amax_bits) {
+    __shared__ uint32_t s_max[kThreads / 32];
+    uint32_t m = 0;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n8; i += stride) {
+        const uint4 v = __ldg(x8 + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+            if (lo < 0x7F80u) m = max(m, lo);
+            if (hi < 0x7F80u) m = max(m, hi);
+        }
+    }
+    if (blockIdx.x == 0 && (int)threadIdx.x < ntail) {
+        const uint32_t b = tail[threadIdx.x] & 0x7FFFu;
+        if (b < 0x7F80u) m = max(m, b);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 1; i < kThreads / 32; ++i) m = max(m, s_max[i]);
+        atomicMax(amax_bits, m << 16);          // BF16 bits -> float32 bits
+    }
+}
+
+// global = amax / (6 * 448), one float32 division rounded to nearest even, clamped into the
+// range the NVFP4 quantiser accepts ([2^-117, 2^100]).
+__global__ void nv_global_kernel(const uint32_t* __restrict__ amax_bits, float* __restrict__ global_scale) {
+    const float g = __fdiv_rn(__uint_as_float(*amax_bits), 2688.0f);
+    *global_scale = fminf(fmaxf(g, 0x1p-117f), 0x1p100f);
+}
+
+// The top-k weighted combine (combine_groups).
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4* __restrict__ y8,
                                                            const int32_t* __restrict__ row_of,
                                                            const float* __restrict__ w,
                                                            uint4* __restrict__ out8, int64_t groups,
                                                            int64_t groups_per_row, int K) {
     pdl_wait();
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < groups; g += stride) {
-        const int64_t t = g / groups_per_row;
-        const int64_t c = g - t * groups_per_row;
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int k = 0; k < K; ++k) {
-            const int32_t r = __ldg(row_of + t * K + k);
-            if (r < 0) continue;
-            const float wk = __ldg(w + t * K + k);
-            const uint4 yv = __ldg(y8 + (int64_t)r * groups_per_row + c);
-            const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wk, bf16_to_f32(yw[i] & 0xFFFFu)));
-                acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wk, bf16_to_f32(yw[i] >> 16)));
-            }
-        }
-        out8[g] = make_uint4(pack2(f32_to_bf16(acc[0]), f32_to_bf16(acc[1])),
-                             pack2(f32_to_bf16(acc[2]), f32_to_bf16(acc[3])),
-                             pack2(f32_to_bf16(acc[4]), f32_to_bf16(acc[5])),
-                             pack2(f32_to_bf16(acc[6]), f32_to_bf16(acc[7])));
-    }
+    combine_groups<false>(y8, row_of, w, out8, groups, groups_per_row, K,
+                          (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
     pdl_launch_dependents();
 }
 
@@ -436,6 +461,19 @@ cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_
     return launch_pdl(act_quant_nv_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
                       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint2*>(codes), sf, blocks, global_scale,
                       clear_word);
+}
+
+cudaError_t launch_nv_calibrate(const uint16_t* x, int64_t n, float* amax, float* global_scale, int num_sms,
+                                cudaStream_t s) {
+    const int64_t n8 = n / 8;
+    const int ntail = (int)(n - 8 * n8);
+    if (n > 0) {
+        amax_kernel<<<grid_for(n8 > 0 ? n8 : 1, num_sms, 4), kThreads, 0, s>>>(
+            reinterpret_cast<const uint4*>(x), n8, x + 8 * n8, ntail, reinterpret_cast<uint32_t*>(amax));
+        if (cudaError_t e = cudaGetLastError()) return e;
+    }
+    nv_global_kernel<<<1, 1, 0, s>>>(reinterpret_cast<const uint32_t*>(amax), global_scale);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,

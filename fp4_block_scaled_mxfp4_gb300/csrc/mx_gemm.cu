@@ -50,6 +50,7 @@
 
 #include "mx_device.cuh"
 #include "mx_internal.h"
+#include "mx_phases.cuh"
 
 namespace mx {
 
@@ -184,29 +185,33 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
-template <bool kL1, bool kBTiled, int kN, bool kNv = false>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
-    static_assert(!kNv || kBTiled, "NVFP4 weights come with tile-layout scales");
+// A CTA's GEMM pipeline in shared and tensor memory. It is set up once per CTA; a persistent
+// kernel runs several GEMMs through it, their barrier phases carried over.
+struct GemmCtx {
+    uint8_t* smem;        // 1024-byte aligned start of the stage ring
+    uint32_t sbase;       // its shared-memory address
+    Ctl* ctl;
+    uint32_t tmem;        // base of the CTA's 512 tensor-memory columns
+};
+
+// A thread's position in the pipeline: the K stages (it) and accumulator tiles (tc) its role
+// has passed, carried from one GEMM to the next.
+struct PipePos {
+    uint32_t it;
+    uint32_t tc;
+};
+
+// Barrier initialisation and tensor-memory allocation; every thread of the CTA calls it.
+template <int kN, bool kNv = false, bool kBTiled = true>
+__device__ __forceinline__ GemmCtx gemm_setup(uint8_t* smem_raw) {
     using C = Cfg<kN, kNv>;
-    constexpr int kBBytes = C::kBBytes;
-    constexpr uint32_t kIdesc = C::kIdesc;
     constexpr int kStages = C::kStages;
-    constexpr int kStageBytes = C::kStageBytes;
-    constexpr int kSfaBytes = C::kSfaBytes;
-    constexpr uint32_t kDescStageStep = C::kDescStageStep;
-    constexpr int kStagingOff = C::kStagingOff;
-    extern __shared__ uint8_t smem_raw[];
+    GemmCtx g;
     const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    const uint32_t sbase = smem_u32(smem);
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)kStagingOff + 8 * kStagingBytes);
-    volatile int* abort_flag = &ctl->abort_flag;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
+    g.smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    g.sbase = smem_u32(g.smem);
+    g.ctl = reinterpret_cast<Ctl*>(g.smem + (size_t)C::kStagingOff + 8 * kStagingBytes);
+    Ctl* ctl = g.ctl;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), kFullArrivals);
@@ -220,22 +225,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_init(smem_u32(&ctl->drain_cp), 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmY);
     }
-    if (warp == 1) {
+    if ((threadIdx.x >> 5) == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = ctl->tmem_base;
-    // Setup done: wait for the kernels before this one, then let the next one be scheduled
-    // (all of this persistent grid's CTAs are resident already, so it cannot take their SMs).
-    pdl_wait();
-    pdl_launch_dependents();
+    g.tmem = ctl->tmem_base;
+    return g;
+}
+
+// One GEMM over its tile list (args), by every thread of the CTA in its role. Returns with the
+// role's pipeline position advanced; the epilogue's output stores are complete.
+template <bool kL1, bool kBTiled, int kN, bool kNv = false>
+__device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                                         const GemmArgs& args, const GemmCtx& g, PipePos& pos) {
+    static_assert(!kNv || kBTiled, "NVFP4 weights come with tile-layout scales");
+    using C = Cfg<kN, kNv>;
+    constexpr int kBBytes = C::kBBytes;
+    constexpr uint32_t kIdesc = C::kIdesc;
+    constexpr int kStages = C::kStages;
+    constexpr int kStageBytes = C::kStageBytes;
+    constexpr int kSfaBytes = C::kSfaBytes;
+    constexpr uint32_t kDescStageStep = C::kDescStageStep;
+    constexpr int kStagingOff = C::kStagingOff;
+    uint8_t* smem = g.smem;
+    const uint32_t sbase = g.sbase;
+    Ctl* ctl = g.ctl;
+    const uint32_t tmem = g.tmem;
+    volatile int* abort_flag = &ctl->abort_flag;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (*abort_flag) return;
 
     const int total = num_mtiles(args) * args.n_tiles;
     const int k_tiles = args.k_tiles;
@@ -243,7 +266,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t& it = pos.it;
             for (int w = blockIdx.x; w < total; w += gridDim.x) {
                 const Tile t = get_tile(args, w / args.n_tiles);
                 const int nt = w % args.n_tiles;
@@ -264,15 +287,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
-            // Tail: wait for the MMA commits that release the last stages, so no
-            // asynchronous arrive reaches this CTA's shared memory after it exits.
-            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i) {
-                if (!mbar_wait(smem_u32(&ctl->empty[i % kStages]), (i / kStages) & 1u, abort_flag, args.status,
-                               kErrWaitEmpty))
-                    break;
-            }
-        producer_done:
-            if (*abort_flag) __nanosleep(20000);   // let copies already in flight land
+        producer_done:;
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -281,7 +296,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t adesc0 = desc_sw128(sbase);
             const uint64_t bdesc0 = desc_sw128(sbase + kABytes);
             const uint32_t sf0 = tmem + kSfTmemBase;
-            uint32_t it = 0, tc = 0;
+            uint32_t& it = pos.it;
+            uint32_t& tc = pos.tc;
             for (int w = blockIdx.x; w < total; w += gridDim.x) {
                 if (!mbar_wait(smem_u32(&ctl->tmem_empty), (tc & 1u) ^ 1u, abort_flag, args.status,
                                kErrWaitTmemEmpty))
@@ -324,17 +340,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_commit(smem_u32(&ctl->tmem_full));
                 ++tc;
             }
-            if (*abort_flag) {
-                // make sure no MMA still writes tensor memory before it is released
-                tc_commit(smem_u32(&ctl->drain));
-                volatile int never = 0;
-                mbar_wait(smem_u32(&ctl->drain), 0, &never, args.status, kErrWaitDrain);
-            }
         }
         __syncwarp();
     } else if (warp == 2) {
         // ---------------- scale-factor loader (A; and B when its scales are row-major) --------
-        uint32_t it = 0;
+        uint32_t& it = pos.it;
         bool aborted = false;
         for (int w = blockIdx.x; w < total && !aborted; w += gridDim.x) {
             const Tile t = get_tile(args, w / args.n_tiles);
@@ -425,12 +435,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
         cp_async_wait<0>();
-        if (*abort_flag && lane == 0) __nanosleep(20000);   // bulk copies already in flight land
         __syncwarp();
     } else if (warp == 3) {
         // ---------------- scale-factor copier (one thread) ----------------
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t& it = pos.it;
             bool ok = true;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
                 for (int kt = 0; kt < k_tiles; ++kt, ++it) {
@@ -459,11 +468,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_commit(smem_u32(&ctl->ready[s]));   // arrives once the copies are in TMEM
                 }
-            }
-            if (*abort_flag) {
-                tc_commit(smem_u32(&ctl->drain_cp));
-                volatile int never = 0;
-                mbar_wait(smem_u32(&ctl->drain_cp), 0, &never, args.status, kErrWaitDrain);
             }
         }
         __syncwarp();
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 return mx_quant32(h, cd);
             }
         };
-        uint32_t tc = 0;
+        uint32_t& tc = pos.tc;
         for (int w = blockIdx.x; w < total; w += gridDim.x, ++tc) {
             const Tile t = get_tile(args, w / args.n_tiles);
             const int nt = w % args.n_tiles;
@@ -650,15 +654,144 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
         }
-        if (lane == 0) bulk_wait_all();   // staged stores complete before the CTA exits
+        if (lane == 0) bulk_wait_all();   // staged stores complete: later readers see them
     }
+}
 
+// End of the CTA's GEMM work: the producer waits for the MMA commits that release the last
+// stages (no asynchronous arrive may reach shared memory after the CTA exits); after an
+// abort, copies in flight land and the tensor pipe drains before tensor memory is released.
+template <int kN, bool kNv = false>
+__device__ __forceinline__ void gemm_finish(const GemmCtx& g, const PipePos& pos, const StatusWords& status) {
+    constexpr int kStages = Cfg<kN, kNv>::kStages;
+    Ctl* ctl = g.ctl;
+    volatile int* abort_flag = &ctl->abort_flag;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (lane == 0 && warp <= 3) {
+        if (warp == 0 && !*abort_flag) {
+            const uint32_t it = pos.it;
+            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0; i < it; ++i)
+                if (!mbar_wait(smem_u32(&ctl->empty[i % kStages]), (i / kStages) & 1u, abort_flag, status,
+                               kErrWaitEmpty))
+                    break;
+        }
+        if (*abort_flag) {
+            if (warp == 0 || warp == 2) __nanosleep(20000);   // TMA and bulk copies in flight land
+            if (warp == 1 || warp == 3) {
+                // no MMA or scale copy may still write tensor memory when it is released
+                const uint32_t bar = smem_u32(warp == 1 ? &ctl->drain : &ctl->drain_cp);
+                tc_commit(bar);
+                volatile int never = 0;
+                mbar_wait(bar, 0, &never, status, kErrWaitDrain);
+            }
+        }
+    }
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(g.tmem, kTmemCols);
     }
+}
+
+// One GEMM per launch: the expert GEMMs of the multi-kernel forward and the dense GEMMs.
+template <bool kL1, bool kBTiled, int kN, bool kNv = false>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmY);
+    }
+    const GemmCtx g = gemm_setup<kN, kNv, kBTiled>(smem_raw);
+    // Setup done: wait for the kernels before this one, then let the next one be scheduled
+    // (all of this persistent grid's CTAs are resident already, so it cannot take their SMs).
+    pdl_wait();
+    pdl_launch_dependents();
+    PipePos pos{0u, 0u};
+    gemm_run<kL1, kBTiled, kN, kNv>(tmA, tmB, tmY, args, g, pos);
+    gemm_finish<kN, kNv>(g, pos, args.status);
+}
+
+// The whole forward in one persistent cooperative launch ("Current Bug: vLLM produces
+// empty/garbage output": the nvfp4-megamoe-kernel plan, "Phase 1: CuTeDSL Shared Expert
+// Kernel": routing, L1 GEMM -> SiLU -> re-quant -> L2 GEMM, scatter), one CTA per SM. The
+// phases are the multi-kernel forward's, with the same device code; where that forward
+// starts a new kernel this one passes a grid-wide barrier:
+//   routed: count chunks | scan (CTA 0) | quantise and gather x | L1 | L2 | combine
+//   shared expert: quantise x | L1 | L2 (writes out)
+// The GEMM pipeline is set up once; L2 continues L1's barrier phases (PipePos). Routing
+// scratch lives in the stage ring, unused until L1.
+template <int kN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_fused_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1,
+                     const __grid_constant__ CUtensorMap ty1, const __grid_constant__ CUtensorMap ta2,
+                     const __grid_constant__ CUtensorMap tb2, const __grid_constant__ CUtensorMap ty2,
+                     const FusedArgs fa) {
+    extern __shared__ uint8_t smem_raw[];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        tma_prefetch_desc(&ta1);
+        tma_prefetch_desc(&tb1);
+        tma_prefetch_desc(&ty1);
+        tma_prefetch_desc(&ta2);
+        tma_prefetch_desc(&tb2);
+        tma_prefetch_desc(&ty2);
+        if (blockIdx.x == 0 && fa.clear_word != nullptr) *fa.clear_word = 0u;
+    }
+    const GemmCtx g = gemm_setup<kN, false, true>(smem_raw);
+    volatile int* abort_flag = &g.ctl->abort_flag;
+    uint32_t target = 0;
+    auto barrier = [&]() {
+        target += gridDim.x;
+        grid_sync(fa.sync, target, abort_flag, fa.status);
+    };
+    int32_t* scratch = reinterpret_cast<int32_t*>(g.smem);
+    const uint4* x8 = reinterpret_cast<const uint4*>(fa.x);
+    const int64_t cta_thread = (int64_t)blockIdx.x * kGemmThreads + tid;
+    const int64_t grid_threads = (int64_t)gridDim.x * kGemmThreads;
+    const bool routed = fa.ids != nullptr;
+    if (routed) {
+        for (int64_t c = blockIdx.x; c < fa.rb.nchunks; c += gridDim.x)
+            route_count_chunk(fa.ids, fa.T * fa.K, fa.E, c, fa.rb.chunk_counts, fa.rb.local_rank, scratch,
+                              scratch + fa.E, tid);
+        barrier();
+        if (blockIdx.x == 0)
+            route_scan(fa.rb.chunk_counts, fa.rb.nchunks, fa.E, fa.rb, scratch, scratch + fa.E,
+                       scratch + 2 * fa.E + 1, tid, kGemmThreads);
+        barrier();
+        for (int64_t t = blockIdx.x; t < fa.T; t += gridDim.x)
+            quant_gather_token<false>(x8, fa.ids, fa.K, fa.E, fa.H / 32, fa.rb, fa.xq, fa.xs, 0.0f, t, scratch, tid,
+                                      kGemmThreads);
+    } else {
+        act_quant_blocks(x8, reinterpret_cast<uint4*>(fa.xq), fa.xs, fa.T * (fa.H / 32), cta_thread, grid_threads);
+    }
+    barrier();
+    PipePos pos{0u, 0u};
+    gemm_run<true, true, kN, false>(ta1, tb1, ty1, fa.g1, g, pos);
+    barrier();
+    gemm_run<false, true, kN, false>(ta2, tb2, ty2, fa.g2, g, pos);
+    if (routed) {
+        barrier();
+        if (!*abort_flag)
+            combine_groups<true>(reinterpret_cast<const uint4*>(fa.y), fa.rb.row_of, fa.topk_w,
+                                 reinterpret_cast<uint4*>(fa.out), fa.T * (fa.H / 8), fa.H / 8, fa.K, cta_thread,
+                                 grid_threads);
+    }
+    gemm_finish<kN, false>(g, pos, fa.status);
+}
+
+// Self-test of the grid barrier's failure path: every CTA waits for one arrival more than the
+// grid has, runs out after the wait limit, records kErrWaitGrid and returns.
+__global__ void __launch_bounds__(32) grid_sync_probe_kernel(uint32_t* counter, StatusWords status) {
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) abort_flag = 0;
+    __syncthreads();
+    grid_sync(counter, gridDim.x + 1, &abort_flag, status);
 }
 
 template <bool kL1, bool kBTiled, int kN, bool kNv = false>
@@ -686,7 +819,56 @@ cudaError_t launch_any(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     return b_tiled ? launch<kL1, true, 256>(ta, tb, ty, a, grid, s) : launch<kL1, false, 256>(ta, tb, ty, a, grid, s);
 }
 
+template <int kN>
+cudaError_t launch_fused(const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ty1,
+                         const CUtensorMap& ta2, const CUtensorMap& tb2, const CUtensorMap& ty2, const FusedArgs& fa,
+                         int num_sms, cudaStream_t s) {
+    static int configured_mask = 0;   // one bit per device
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+        err = cudaFuncSetAttribute(moe_fused_kernel<kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem_bytes<kN>());
+        if (err != cudaSuccess) return err;
+        __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
+    }
+    // Cooperative: the runtime launches the grid only if every CTA can be resident at once,
+    // which the grid-wide barriers need.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = smem_bytes<kN>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_fused_kernel<kN>, ta1, tb1, ty1, ta2, tb2, ty2, fa);
+}
+
 }  // namespace
+
+cudaError_t launch_moe_fused(const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ty1,
+                             const CUtensorMap& ta2, const CUtensorMap& tb2, const CUtensorMap& ty2,
+                             const FusedArgs& fa, int n_cols, int num_sms, cudaStream_t s) {
+    return n_cols == 128 ? launch_fused<128>(ta1, tb1, ty1, ta2, tb2, ty2, fa, num_sms, s)
+                         : launch_fused<256>(ta1, tb1, ty1, ta2, tb2, ty2, fa, num_sms, s);
+}
+
+cudaError_t launch_grid_sync_probe(uint32_t* counter, StatusWords status, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grid_sync_probe_kernel, counter, status);
+}
 
 size_t gemm_smem_bytes() {
     const size_t a = smem_bytes<256>(), b = smem_bytes<128>(), c = smem_bytes<256, true>();

@@ -112,6 +112,18 @@ cudaError_t launch_gemm_nvfp4(const CUtensorMap& ta, const CUtensorMap& tb, cons
 cudaError_t launch_gemm_nvfp4_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                                  const GemmArgs& a, int grid, cudaStream_t s);
 
+// The whole routed (or shared-expert) MXFP4 forward as one persistent cooperative launch:
+// routing, quantisation of x, L1, L2 and the combine, separated by grid-wide barriers.
+// Weight scales in the tile layout; both GEMMs run tiles of kN = n_cols columns.
+struct RouteBufs;
+struct FusedArgs;
+cudaError_t launch_moe_fused(const CUtensorMap& ta1, const CUtensorMap& tb1, const CUtensorMap& ty1,
+                             const CUtensorMap& ta2, const CUtensorMap& tb2, const CUtensorMap& ty2,
+                             const FusedArgs& fa, int n_cols, int num_sms, cudaStream_t s);
+// Failure-path self-test of the grid-wide barrier: a cooperative launch of two CTAs waits on a
+// barrier count no arrival reaches (counter must be zero, in device memory).
+cudaError_t launch_grid_sync_probe(uint32_t* counter, StatusWords status, cudaStream_t s);
+
 // ---- element-wise kernels ----
 // Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][512 B] (kb % 4 == 0).
 cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s);
@@ -129,6 +141,10 @@ cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int
 // NVFP4 activation quantisation with the float32 global (codes [M, K/2], E4M3 sf [M, K/16]).
 cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M,
                                    int64_t K, int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr);
+// NVFP4 activation-global calibration over n BF16 values (x 16-byte aligned): *amax (float32,
+// device) becomes the running maximum of the finite |x|, *global_scale = amax / (6 * 448).
+cudaError_t launch_nv_calibrate(const uint16_t* x, int64_t n, float* amax, float* global_scale, int num_sms,
+                                cudaStream_t s);
 // Failure-path self-test: a bounded wait on a barrier nothing arrives at (see mx_elementwise.cu).
 cudaError_t launch_wait_probe(StatusWords status, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* y, const int32_t* row_of, const float* w, uint16_t* out,
@@ -151,6 +167,24 @@ struct RouteBufs {
 // clear_word: as for launch_act_quant.
 cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, const RouteBufs& rb,
                          cudaStream_t s, uint32_t* clear_word = nullptr);
+// Arguments of the persistent forward (launch_moe_fused).
+struct FusedArgs {
+    GemmArgs g1, g2;             // L1 and L2, as the multi-kernel forward fills them
+    const uint16_t* x;           // BF16 [T, H]
+    const int32_t* ids;          // [T, K], or null: shared expert (uniform tiling)
+    const float* topk_w;         // [T, K]
+    uint16_t* out;               // BF16 [T, H]
+    uint16_t* y;                 // L2's BF16 rows [R, H] (routed)
+    uint8_t* xq;
+    uint8_t* xs;
+    RouteBufs rb;
+    int64_t T, H;
+    int32_t K, E;
+    uint32_t* sync;              // grid-barrier arrival counter, zero at launch
+    uint32_t* clear_word;        // the workspace status word, cleared first
+    StatusWords status;
+};
+
 // Quantise each token row once (MXFP4, or NVFP4 with the float32 global) and write it to the
 // rows of all its routed pairs; also writes row_of (needs launch_route first).
 cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,

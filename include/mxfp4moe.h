@@ -103,6 +103,16 @@ int mx_selftest_wait_timeout(mx_stream_t stream);
 int mx_selftest_wait_timeout_ws(void* workspace, mx_stream_t stream);
 
 /*
+ * mx_selftest_grid_barrier_timeout -- exercises the failure path of the persistent
+ * forward's grid-wide barrier: zeroes the barrier counter of `workspace` (256-byte aligned
+ * device memory of at least 512 bytes) on `stream`, then launches two CTAs cooperatively
+ * that wait, with that barrier's bounded wait (about 2 s), for one arrival more than there
+ * are CTAs. The waits run out, the kernel records MX_ERR_DEVICE_TIMEOUT in the workspace's
+ * status word and the device-wide word, and returns. For tests only.
+ */
+int mx_selftest_grid_barrier_timeout(void* workspace, mx_stream_t stream);
+
+/*
  * mxfp4_dequant -- MXFP4 -> BF16 ([DQ] item 2, [FMT]).
  *   out[r, c] = bf16( E2M1(nibble(codes[r, c/2], c%2)) * 2^(sf[r, c/32] - 127) )
  *   codes uint8 [rows, cols/2], sf uint8 [rows, cols/32], out uint16 [rows, cols].
@@ -211,6 +221,23 @@ int act_quant_nvfp4(const void* x_bf16, float global_scale, uint8_t* codes, uint
                     int64_t M, int64_t K, mx_stream_t stream);
 
 /*
+ * nvfp4_calibrate_global -- the warm-up calibration of an NVFP4 activation global scale
+ * ("Current Bug: vLLM produces empty/garbage output", "Phase 1: CuTeDSL Shared Expert
+ * Kernel": a warm-up-based gs), on the GPU. For a calibration batch x uint16 [M, K] (BF16):
+ *   *amax         = max(*amax, largest finite |x|)      (NaN and infinities are skipped)
+ *   *global_scale = *amax / (6 * 448), one float32 division rounded to nearest even,
+ *                   clamped to [2^-117, 2^100] (the range act_quant_nvfp4 accepts)
+ * so that the largest magnitude seen quantises to the largest NVFP4 value (E2M1 6 times
+ * E4M3 448) without clipping. amax and global_scale are float32 DEVICE pointers (4-byte
+ * aligned); *amax is a running maximum over the warm-up batches: set it to 0 before the
+ * first call, call once per batch (M = 0 just recomputes the global), then read the global
+ * back once and pass it to act_quant_nvfp4 / moe_nvfp4_forward, where it stays a fixed
+ * value (the forward remains graph-capturable). x 16-byte aligned; any K > 0.
+ */
+int nvfp4_calibrate_global(const void* x_bf16, int64_t M, int64_t K, float* amax, float* global_scale,
+                           mx_stream_t stream);
+
+/*
  * Tile layout of a scale tensor (the layout the GEMM's tensor-memory copies read).
  * A scale tensor sf uint8 [rows, cols/32] (one E8M0 byte per 32 columns) becomes
  * ceil(rows/128) x (cols/128) blocks of 512 bytes; block (g, w) sits at ((g*(cols/128)) + w)*512
@@ -298,6 +325,28 @@ int moe_mxfp4_forward(const void* x, const int32_t* topk_ids, const float* topk_
  * (2.48 ms against 1.98 ms).
  */
 int moe_mxfp4_forward_tiled(const void* x, const int32_t* topk_ids, const float* topk_w,
+                            const uint8_t* w13, const uint8_t* s13_tiled, const uint8_t* w2,
+                            const uint8_t* s2_tiled, void* out, int64_t T, int64_t H, int64_t I,
+                            int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                            mx_stream_t stream);
+
+/*
+ * moe_mxfp4_forward_fused -- moe_mxfp4_forward_tiled as ONE persistent kernel launch (the
+ * single-launch MoE kernel of "Current Bug: vLLM produces empty/garbage output", the
+ * nvfp4-megamoe-kernel plan, "Phase 1: CuTeDSL Shared Expert Kernel"): one CTA per SM runs
+ * the routing, the quantisation of x, the L1 GEMM with its fused SiLU and re-quant, the L2
+ * GEMM and the weighted combine, with a grid-wide barrier where the multi-kernel forward
+ * starts a new kernel. The phases run the same device code in the same order, so the output
+ * is bit-identical to moe_mxfp4_forward_tiled's.
+ *   Same arguments, layouts, workspace (moe_mxfp4_workspace_size) and errors as
+ * moe_mxfp4_forward_tiled; the weight scales must be in the tile layout. The launch is
+ * cooperative (the runtime refuses it, MX_ERR_CUDA, unless every CTA can be resident at
+ * once) and is preceded on `stream` by a 4-byte memset of the workspace's barrier counter;
+ * both can be captured in a CUDA graph. Each barrier wait is bounded like the pipeline
+ * waits: past the limit the kernel records MX_ERR_DEVICE_TIMEOUT in the workspace's status
+ * word (mx_check_workspace) and returns.
+ */
+int moe_mxfp4_forward_fused(const void* x, const int32_t* topk_ids, const float* topk_w,
                             const uint8_t* w13, const uint8_t* s13_tiled, const uint8_t* w2,
                             const uint8_t* s2_tiled, void* out, int64_t T, int64_t H, int64_t I,
                             int64_t E, int64_t K, void* workspace, size_t ws_bytes,

@@ -30,6 +30,7 @@ from .mxfp4_oracle import (  # noqa: F401
     moe_route,
     swiglu_bf16,
     moe_flops_per_pair,
+    nvfp4_activation_global,
     nvfp4_dequant,
     nvfp4_gemm_bf16,
     nvfp4_gemm_f64,

@@ -91,6 +91,10 @@ R18 MXFP8 activations (E4M3 elements, one E8M0 scale per 32; the pages do not na
     saturating at +-448, sign kept (-0 -> 0x80); a block holding a NaN or an infinity gets
     E = 255 and elements sign|0x7F. The MXFP8 MoE forward is R1, R3-R5 with MXFP8 in both
     activation quantisations and the MXFP4 weights unchanged.
+R19 The warm-up-based activation global ([GS]'s "warmup-based gs"; the pages give no
+    formula): the largest finite |x| over the calibration batches, divided by 6 * 448 (the
+    largest NVFP4 magnitude) in one float32 division, clamped into R15's range. NaN and
+    infinities are skipped (a non-finite input would leave no usable global).
 
 Parity status: every function below is pinned by the ``-m "not gpu"`` tests (tables from
 the OCP MX definitions and torch's float8 conversions, one-hot nibble/scale tests, the
@@ -108,6 +112,7 @@ __all__ = [
     "act_quant_mxfp4", "mxfp4_gemm_bf16", "mxfp4_gemm_blockint", "moe_route", "moe_forward",
     "nvfp4_values", "nvfp4_dequant", "nvfp4_gemm_f64", "nvfp4_gemm_bf16",
     "e4m3_round_code", "nvfp4_quantize", "moe_nvfp4_forward", "nvfp4_gemm_segments_bf16",
+    "nvfp4_activation_global",
     "act_quant_mxfp8", "mxfp8_values", "moe_mxfp8_forward", "mxfp8_mxfp4_gemm_bf16",
     "moe_flops_per_pair", "moe_l1_exact", "swiglu_bf16", "moe_l2_bf16", "moe_combine",
 ]
@@ -371,6 +376,22 @@ def nvfp4_quantize(x_bits, global_scale):
     sf = np.where(finite, S, 0x7F).astype(np.uint8)
     code = code.reshape(M, K)
     return (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8), sf
+
+
+def nvfp4_activation_global(batches) -> float:
+    """Warm-up calibration of an NVFP4 activation global by reading R19: over every BF16
+    batch (uint16 [M, K] each), amax = the largest finite |x|; the global is amax / (6 * 448)
+    rounded once to float32 (nearest even), clamped to [2^-117, 2^100] (R15's range).
+    6 * 448 is the largest NVFP4 magnitude (E2M1 6 times E4M3 448), so the largest input
+    quantises to it without clipping."""
+    amax = 0.0
+    for xb in batches:
+        x = bf16_bits_to_f64(np.asarray(xb, dtype=np.uint16))
+        x = np.abs(x[np.isfinite(x)])
+        if x.size:
+            amax = max(amax, float(x.max()))
+    g = np.float32(np.float32(amax) / np.float32(6 * 448))     # one float32 division
+    return float(np.clip(g, np.float32(2.0 ** -117), np.float32(2.0 ** 100)))
 
 
 # --------------------------------------------------------------------------------------

@@ -174,3 +174,48 @@ def test_nvfp4_graph_capture_replays_bit_identical(mx):
     g.replay()
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bf16_host(d.out), eager)
+
+
+# ----------------------------------------------------------------------------- calibration
+
+def test_nvfp4_calibrate_global_bit_exact(mx):
+    """The device calibration (running maximum of the finite |x| over warm-up batches, then
+    amax / (6 * 448) in float32) equals the oracle's (reading R19), bit for bit: batches of
+    odd sizes (a scalar tail after the 16-byte vectors), NaN and infinities skipped, an
+    empty batch, and the running maximum carried across calls."""
+    import torch
+    rng = np.random.default_rng(93)
+    shapes = [(3, 37), (64, 7168), (0, 16), (5, 8), (1000, 96)]
+    batches = []
+    for i, (M, K) in enumerate(shapes):
+        x = (rng.standard_normal((M, K)) * np.exp2(rng.uniform(-20, 20, size=(M, 1)))).astype(np.float32)
+        xb = f32_to_bf16_bits(x)
+        if M > 2:
+            xb[1, 2], xb[2, 0] = 0x7FC0, 0xFF80                  # NaN, -inf: skipped
+        batches.append(xb)
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    for i, xb in enumerate(batches):
+        xd = dev(xb).view(torch.bfloat16) if xb.size else torch.empty(xb.shape, dtype=torch.bfloat16, device="cuda")
+        mx.nvfp4_calibrate_global(xd, amax, g)
+        want = oracle.nvfp4_activation_global(batches[: i + 1])
+        assert float(g.cpu()[0]) == want, (i, float(g.cpu()[0]), want)
+    finite = np.concatenate([oracle.bf16_bits_to_f64(b).ravel() for b in batches])
+    assert float(amax.cpu()[0]) == np.abs(finite[np.isfinite(finite)]).max()
+
+
+def test_nvfp4_forward_with_the_device_calibrated_global(mx):
+    """The activation global the forward runs with comes from the device calibration of the
+    batch itself (no host-side numpy step): it equals the workload's, and the forward checks
+    out step by step against the oracle with it."""
+    import torch
+    inp = make_nvfp4_config_inputs("tiny")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    mx.nvfp4_calibrate_global(dev(inp.x).view(torch.bfloat16), amax, g)
+    x_global = float(g.cpu()[0])
+    assert x_global == inp.x_global
+    inp.x_global = x_global
+    d = NvDev(mx, inp)
+    d.run(mx)
+    print("nvfp4 tiny, device-calibrated global", check_nvfp4_moe_run(mx, d))

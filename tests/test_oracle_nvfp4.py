@@ -374,3 +374,59 @@ def test_gemm_segments_single_segment_is_the_gemm():
     sb = rng.integers(0x20, 0x50, size=(32, 8), dtype=np.uint8)
     np.testing.assert_array_equal(oracle.nvfp4_gemm_segments_bf16(a, sa, 0.5, b, sb, [0.25], [32]),
                                   oracle.nvfp4_gemm_bf16(a, sa, 0.5, b, sb, 0.25))
+
+
+# ----------------------------------------------------------------------------- calibration (R19)
+
+def _e4m3_byte(v):
+    import torch
+    return int(torch.tensor([v], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+
+
+def test_calibrated_global_maps_the_largest_input_to_the_largest_nvfp4_value():
+    """With the calibrated global, the block holding the batch's largest |x| gets the largest
+    E4M3 scale (448, torch's encoding) and that element the largest E2M1 code (6.0, the OCP
+    table), the dequantised value equals that |x| up to the float32 rounding of the global,
+    and no block's scale goes past 448: the whole range is used, nothing is clipped."""
+    rng = np.random.default_rng(191)
+    from workloads import f32_to_bf16_bits
+    x = (rng.standard_normal((37, 256)) * np.exp2(rng.uniform(-6, 6, size=(37, 1)))).astype(np.float32)
+    xb = f32_to_bf16_bits(x)
+    g = oracle.nvfp4_activation_global([xb])
+    q, sf = oracle.nvfp4_quantize(xb, g)
+    xv = oracle.bf16_bits_to_f64(xb)
+    r, c = np.unravel_index(np.argmax(np.abs(xv)), xv.shape)
+    top = _e4m3_byte(448.0)
+    assert sf[r, c // 16] == top
+    assert (sf <= top).all()
+    nib = oracle.unpack_nibbles(q)[r, c]
+    table = _e2m1_table()
+    assert abs(table[nib & 7]) == 6.0
+    deq = 6.0 * 448.0 * g
+    assert abs(deq - abs(xv[r, c])) <= abs(xv[r, c]) * 2.0 ** -23
+
+
+def test_calibration_running_maximum_skips_non_finite_and_clamps():
+    from workloads import f32_to_bf16_bits
+    rng = np.random.default_rng(192)
+    xb = f32_to_bf16_bits(rng.standard_normal((60, 64)).astype(np.float32) * 3)
+    whole = oracle.nvfp4_activation_global([xb])
+    parts = [xb[:10], xb[10:45], xb[45:]]
+    assert oracle.nvfp4_activation_global(parts) == whole
+    assert oracle.nvfp4_activation_global(parts[::-1]) == whole
+    bad = xb.copy()
+    bad[3, 5], bad[7, 9], bad[8, 1] = 0x7FC0, 0x7F80, 0xFF80           # NaN, +inf, -inf
+    assert oracle.nvfp4_activation_global([bad]) == whole
+    assert oracle.nvfp4_activation_global([np.zeros((4, 16), np.uint16)]) == 2.0 ** -117
+    big = f32_to_bf16_bits(np.full((1, 16), 1e35, np.float32))
+    assert oracle.nvfp4_activation_global([big]) == float(np.float32(2.0 ** 100))
+    # one float32 division, nearest even: the largest finite BF16 magnitude of 1.5 gives
+    # 1.5 / 2688 rounded once
+    one = f32_to_bf16_bits(np.array([[1.5, -0.25] + [0.0] * 14], np.float32))
+    assert oracle.nvfp4_activation_global([one]) == float(np.float32(1.5) / np.float32(2688.0))
+
+
+def test_generator_global_is_the_calibration_of_its_batch():
+    from workloads import make_nvfp4_config_inputs
+    inp = make_nvfp4_config_inputs("tiny")
+    assert inp.x_global == oracle.nvfp4_activation_global([inp.x])
