@@ -656,7 +656,52 @@ def measure_extra(mx, torch, dev, stream):
         del x, ids, w, W, out, ws, flush
         torch.cuda.empty_cache()
     res.update(measure_nvfp4_forward(mx, torch, dev, stream, timeit))
+    res.update(measure_mxfp8_forward(mx, torch, dev, stream, timeit))
     return res
+
+
+def measure_mxfp8_forward(mx, torch, dev, stream, timeit):
+    """The routed prefill forward with MXFP8 activations over the same MXFP4 weights (the
+    step's workload), against the FP8 tensor rate: kind::mxf8f6f4 runs at the E4M3 rate, one
+    third of the FP4 one (nominal 4.5 : 13.5)."""
+    inp = make_config_inputs("prefill")
+    c = CONFIGS["prefill"]
+    T, H, I, E, K = c["T"], c["H"], c["I"], c["E"], c["K"]
+    x = torch.from_numpy(inp.x).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(inp.topk_ids).to(dev)
+    w = torch.from_numpy(inp.topk_w).to(dev)
+    w13, w2 = torch.from_numpy(inp.w13).to(dev), torch.from_numpy(inp.w2).to(dev)
+    s13t = torch.empty(mx.mxfp4_tiled_scales_bytes(E * 2 * I, H), dtype=torch.uint8, device=dev)
+    s2t = torch.empty(mx.mxfp4_tiled_scales_bytes(E * H, I), dtype=torch.uint8, device=dev)
+    mx.mxfp4_scales_to_tiled(torch.from_numpy(inp.s13.reshape(-1, H // 32)).to(dev), s13t)
+    mx.mxfp4_scales_to_tiled(torch.from_numpy(inp.s2.reshape(-1, I // 32)).to(dev), s2t)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mx.moe_mxfp4w_mxfp8a_workspace_size(T, H, I, E, K, True), dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record(stream)              # create the underlying CUDA events
+
+    def fwd(events=None):
+        mx.moe_mxfp4w_mxfp8a_forward(x, ids, w, w13, s13t, w2, s2t, out, ws, stream=stream, events=events)
+
+    ms = timeit(fwd, reps=20)
+    fwd(ev)
+    torch.cuda.synchronize()
+    pairs = int(((inp.topk_ids >= 0) & (inp.topk_ids < E)).sum())
+    flop = pairs * flops_per_pair(H, I)
+    l1_ms = ev[2].elapsed_time(ev[3])
+    l1_tflops = pairs * 2 * H * 2 * I / l1_ms / 1e9
+    fp8_peak = fp4_peak_tflops(measured_peaks()[0]) / 3.0
+    r = {"mxfp8_activation_forward": {
+        "workload": "routed prefill T=8192, H=7168, I=3072, 48 experts, top-8, MXFP8 activations x MXFP4 weights",
+        "ms": ms, "TFLOP/s": flop / ms / 1e9,
+        "phases_ms": {k: ev[i].elapsed_time(ev[i + 1]) for i, k in
+                      enumerate(("route", "quant_gather", "l1_gemm", "l2_gemm", "combine"))},
+        "l1_TFLOP/s": l1_tflops, "l1_frac_fp8_peak": l1_tflops / fp8_peak,
+        "fp8_peak_source": "measured bf16_tflops (burst) x 2 (nominal FP8:BF16)"}}
+    del x, ids, w, w13, w2, s13t, s2t, out, ws
+    torch.cuda.empty_cache()
+    return r
 
 
 def measure_nvfp4_forward(mx, torch, dev, stream, timeit):

@@ -8,6 +8,7 @@ and marshals torch tensors into its calls.
 from ._native import (  # noqa: F401
     MXError,
     act_quant_mxfp4,
+    act_quant_mxfp8,
     act_quant_nvfp4,
     check_workspace,
     device_status,
@@ -18,6 +19,9 @@ from ._native import (  # noqa: F401
     moe_mxfp4_route,
     moe_mxfp4_workspace_layout,
     moe_mxfp4_workspace_size,
+    moe_mxfp4w_mxfp8a_forward,
+    moe_mxfp4w_mxfp8a_workspace_layout,
+    moe_mxfp4w_mxfp8a_workspace_size,
     moe_nvfp4_forward,
     moe_nvfp4_workspace_layout,
     moe_nvfp4_workspace_size,
@@ -25,6 +29,7 @@ from ._native import (  # noqa: F401
     mxfp4_gemm_bf16,
     mxfp4_scales_to_tiled,
     mxfp4_tiled_scales_bytes,
+    mxfp8_mxfp4_gemm_bf16,
     nvfp4_calibrate_global,
     nvfp4_dequant,
     nvfp4_gemm_bf16,

@@ -37,6 +37,17 @@ _SIGNATURES = {
                                              ctypes.c_int, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "act_quant_mxfp4": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
     "act_quant_nvfp4": (ctypes.c_int, [_c_ptr, ctypes.c_float, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "act_quant_mxfp8": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr]),
+    "mxfp8_mxfp4_gemm_bf16": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_ptr]),
+    "moe_mxfp4w_mxfp8a_workspace_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
+    "moe_mxfp4w_mxfp8a_workspace_layout": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int,
+                                                           _c_ptr]),
+    "moe_mxfp4w_mxfp8a_forward": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                                 _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr, ctypes.c_size_t,
+                                                 _c_ptr]),
+    "moe_mxfp4w_mxfp8a_forward_timed": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                                       _c_ptr, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _c_ptr,
+                                                       ctypes.c_size_t, _c_ptr, _c_ptr]),
     "nvfp4_calibrate_global": (ctypes.c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr]),
     "moe_nvfp4_workspace_size": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int]),
     "moe_nvfp4_workspace_layout": (ctypes.c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_i64, ctypes.c_int, _c_ptr]),
@@ -268,6 +279,74 @@ def nvfp4_calibrate_global(x, amax, global_scale, stream=None) -> None:
     _need(global_scale, torch.float32, (1,), "global_scale")
     _check(lib().nvfp4_calibrate_global(_ptr(x), M, K, _ptr(amax), _ptr(global_scale), _stream(stream)),
            "nvfp4_calibrate_global")
+
+
+def act_quant_mxfp8(x, codes, sf, stream=None) -> None:
+    """BF16 [M, K] -> MXFP8 codes uint8 [M, K] (E4M3) + E8M0 scales uint8 [M, K/32]."""
+    import torch
+    M, K = x.shape
+    _need(x, x.dtype, (M, K), "x")
+    _need(codes, torch.uint8, (M, K), "codes")
+    _need(sf, torch.uint8, (M, K // 32), "sf")
+    _check(lib().act_quant_mxfp8(_ptr(x), _ptr(codes), _ptr(sf), M, K, _stream(stream)), "act_quant_mxfp8")
+
+
+def mxfp8_mxfp4_gemm_bf16(a, sa, b, sb_tiled, d, stream=None) -> None:
+    """D = bf16(A . B^T): MXFP8 A (codes [M, K], scales [M, K/32]), MXFP4 B (codes [N, K/2],
+    tile-layout scales)."""
+    import torch
+    M, K = a.shape
+    N = b.shape[0]
+    _need(a, torch.uint8, (M, K), "a")
+    _need(sa, torch.uint8, (M, K // 32), "sa")
+    _need(b, torch.uint8, (N, K // 2), "b")
+    if sb_tiled.dtype != torch.uint8 or sb_tiled.numel() < mxfp4_tiled_scales_bytes(N, K):
+        raise ValueError("sb_tiled: expected the tile layout of B's scales")
+    _need(d, d.dtype, (M, N), "d")
+    _check(lib().mxfp8_mxfp4_gemm_bf16(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb_tiled), _ptr(d), M, N, K,
+                                       _stream(stream)), "mxfp8_mxfp4_gemm_bf16")
+
+
+def moe_mxfp4w_mxfp8a_workspace_size(T: int, H: int, I: int, E: int, K: int, routed: bool = True) -> int:
+    return int(lib().moe_mxfp4w_mxfp8a_workspace_size(T, H, I, E, K, 1 if routed else 0))
+
+
+def moe_mxfp4w_mxfp8a_workspace_layout(T: int, H: int, I: int, E: int, K: int, routed: bool = True) -> dict:
+    """Byte offsets of the intermediates an MXFP8-activation forward leaves in its workspace."""
+    buf = (ctypes.c_int64 * 8)()
+    _check(lib().moe_mxfp4w_mxfp8a_workspace_layout(T, H, I, E, K, 1 if routed else 0, ctypes.addressof(buf)),
+           "moe_mxfp4w_mxfp8a_workspace_layout")
+    names = ("xq", "xs", "hq", "hs", "y", "row_of", "counts", "offsets")
+    return {n: int(v) for n, v in zip(names, buf)}
+
+
+def moe_mxfp4w_mxfp8a_forward(x, topk_ids, topk_w, w13, s13_tiled, w2, s2_tiled, out, workspace, stream=None,
+                              events=None) -> None:
+    """MoE expert FFN with MXFP8 activations over MXFP4 weights (tile-layout weight scales);
+    topk_ids/topk_w None selects the shared expert. ``events`` as in moe_mxfp4_forward."""
+    import torch
+    T, H = x.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    K = topk_ids.shape[1] if topk_ids is not None else 1
+    _need(x, x.dtype, (T, H), "x")
+    if topk_ids is not None:
+        _need(topk_ids, torch.int32, (T, K), "topk_ids")
+        _need(topk_w, torch.float32, (T, K), "topk_w")
+    _need(w13, torch.uint8, (E, 2 * I, H // 2), "w13")
+    _need(w2, torch.uint8, (E, H, I // 2), "w2")
+    for t, r, c, n in ((s13_tiled, E * 2 * I, H, "s13_tiled"), (s2_tiled, E * H, I, "s2_tiled")):
+        if t.dtype != torch.uint8 or t.numel() < mxfp4_tiled_scales_bytes(r, c) or not t.is_cuda:
+            raise ValueError(f"{n}: expected the tile layout of the scales")
+    _need(out, out.dtype, (T, H), "out")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    args = (_ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13_tiled), _ptr(w2), _ptr(s2_tiled), _ptr(out),
+            T, H, I, E, K, _ptr(workspace), ws_bytes, _stream(stream))
+    if events is not None:
+        evs = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else 0) for e in events])
+        _check(lib().moe_mxfp4w_mxfp8a_forward_timed(*args, ctypes.addressof(evs)), "moe_mxfp4w_mxfp8a_forward_timed")
+    else:
+        _check(lib().moe_mxfp4w_mxfp8a_forward(*args), "moe_mxfp4w_mxfp8a_forward")
 
 
 def mxfp4_tiled_scales_bytes(rows: int, cols: int) -> int:

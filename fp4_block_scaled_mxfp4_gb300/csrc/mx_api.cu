@@ -84,6 +84,36 @@ int make_tmap_w13(CUtensorMap* m, const void* base, int64_t H, int64_t I, int64_
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// E2M1 codes [rows, K/2 bytes] read as K 4-bit elements per row through the type that spreads
+// each 8 bytes of 16 codes over 16 bytes of shared memory (the layout kind::mxf8f6f4 reads):
+// boxes of 128 elements (128 bytes in shared memory) x box_rows, 128-byte swizzle. The base
+// must be 32-byte aligned and K a multiple of 128.
+int make_tmap_fp4s(CUtensorMap* m, const void* base, int64_t K, int64_t rows, uint32_t box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    cuuint32_t box[2] = {128u, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+// The stacked w13 of make_tmap_w13 in that spread form: [E][2][I][H] elements.
+int make_tmap_w13_fp4s(CUtensorMap* m, const void* base, int64_t H, int64_t I, int64_t E, uint32_t box_rows) {
+    const cuuint64_t row = (cuuint64_t)(H / 2);
+    cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)E};
+    cuuint64_t strides[3] = {row, row * (cuuint64_t)I, row * (cuuint64_t)I * 2};
+    cuuint32_t box[4] = {128u, box_rows, 2u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
 // 2-D output [rows, cols] written in boxes of 32 rows x box_bytes (32: 16 BF16 or 32 code
 // bytes; 16: 16 code bytes), no swizzle.
 int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool bf16 = true, uint32_t box_bytes = 32) {
@@ -118,7 +148,9 @@ struct WsLayout {
            total = 0;
 };
 
-WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool routed, int sf_div = 32) {
+// code_div: activation elements per code byte (2 for E2M1, 1 for the MXFP8 path's E4M3).
+WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool routed, int sf_div = 32,
+                   int code_div = 2) {
     WsLayout L;
     L.R = routed ? T * K : T;
     L.nchunks = routed ? (L.R + kRouteChunk - 1) / kRouteChunk : 0;
@@ -143,9 +175,9 @@ WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool r
         L.tile_row0 = take(4 * (size_t)L.max_mtiles);
         L.tile_rows = take(4 * (size_t)L.max_mtiles);
     }
-    L.xq = take((size_t)L.R * (size_t)(H / 2));
+    L.xq = take((size_t)L.R * (size_t)(H / code_div));
     L.xs = take((size_t)L.R * (size_t)(H / sf_div));
-    L.hq = take((size_t)L.R * (size_t)(I / 2));
+    L.hq = take((size_t)L.R * (size_t)(I / code_div));
     L.hs = take((size_t)L.R * (size_t)(I / sf_div));
     if (routed) L.y = take((size_t)L.R * (size_t)H * 2);
     L.total = off;
@@ -367,6 +399,18 @@ int act_quant_mxfp4(const void* x_bf16, uint8_t* codes, uint8_t* sf, int64_t M, 
                                         static_cast<cudaStream_t>(stream)));
 }
 
+int act_quant_mxfp8(const void* x_bf16, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K, mx_stream_t stream) {
+    if (M < 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (K % 32) return MX_ERR_UNSUPPORTED;
+    if (M == 0) return MX_OK;
+    if (!x_bf16 || !codes || !sf) return MX_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(codes)) return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    return cuda_status(launch_act_quant_mxfp8(static_cast<const uint16_t*>(x_bf16), codes, sf, M, K, d->num_sms,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 size_t mxfp4_tiled_scales_bytes(int64_t rows, int64_t cols) {
     if (rows < 0 || cols <= 0 || cols % 128) return 0;
     return tiled_bytes(rows, cols / 32);
@@ -482,6 +526,34 @@ int mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const
                                       nw, static_cast<cudaStream_t>(stream)));
 }
 
+int mxfp8_mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb_tiled,
+                          void* d_bf16, int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (K % 128 || N % 16) return MX_ERR_UNSUPPORTED;
+    if (M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 24)) return MX_ERR_UNSUPPORTED;
+    if (M == 0) return MX_OK;
+    if (!a || !sa || !b || !sb_tiled || !d_bf16) return MX_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned32(b) || !aligned16(sa) || !aligned16(sb_tiled) || !aligned16(d_bf16))
+        return MX_ERR_MISALIGNED;
+    DeviceInfo* d;
+    if (int e = device_info(&d)) return e;
+    CUtensorMap ta, tb, ty;
+    if (make_tmap(&ta, a, K, M, 128) || make_tmap_fp4s(&tb, b, K, N, 256) || make_tmap_out(&ty, d_bf16, N, M))
+        return MX_ERR_CUDA;
+    GemmArgs g = base_args(sa, sb_tiled, K, M, N, d->status);
+    g.k_tiles = (int32_t)(K / 128);
+    g.k_tail_half = 0;
+    g.num_mtiles_host = (int32_t)((M + kBM - 1) / kBM);
+    g.m_total = M;
+    g.n_tiles = (int32_t)((N + kBN - 1) / kBN);
+    g.b_rows_per_expert = N;
+    g.n_valid = N;
+    g.y = static_cast<uint16_t*>(d_bf16);
+    g.ld_y = N;
+    return cuda_status(launch_gemm_a8(ta, tb, ty, g, grid_for((int64_t)g.num_mtiles_host * g.n_tiles, d->num_sms),
+                                      false, static_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_mxfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed) {
     if (check_moe_dims(T, H, I, E, K, routed != 0) != MX_OK) return 0;
     return ws_layout(T, H, I, E, K, routed != 0).total;
@@ -543,7 +615,8 @@ struct NvGlobals {
 int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
                  const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, void* out, int64_t T, int64_t H,
                  int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes, mx_stream_t stream,
-                 void* const* events, bool scales_tiled, const NvGlobals* nv = nullptr, bool fused = false) {
+                 void* const* events, bool scales_tiled, const NvGlobals* nv = nullptr, bool fused = false,
+                 bool a8 = false) {
     const bool routed = topk_ids != nullptr;
     if (routed != (topk_w != nullptr)) return MX_ERR_INVALID_ARG;
     if (int e = check_moe_dims(T, H, I, E, K, routed)) return e;
@@ -554,8 +627,10 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     if (!aligned16(x) || !aligned16(w13) || !aligned16(s13) || !aligned16(w2) || !aligned16(s2) ||
         !aligned16(out))
         return MX_ERR_MISALIGNED;
+    if (a8 && (!aligned32(w13) || !aligned32(w2))) return MX_ERR_MISALIGNED;
     const int sf_div = nv ? 16 : 32;
-    const WsLayout L = ws_layout(T, H, I, E, K, routed, sf_div);
+    const int code_div = a8 ? 1 : 2;
+    const WsLayout L = ws_layout(T, H, I, E, K, routed, sf_div, code_div);
     if (!workspace || ws_bytes < L.total) return MX_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
     DeviceInfo* d;
@@ -608,25 +683,37 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     // uniform tiling: the routed tile count is known on the device alone, and its bound
     // max_mtiles counts an extra tile per expert. NVFP4 runs 256-column tiles only. The
     // persistent forward runs both GEMMs through one pipeline, so one width for both.
-    int n1 = routed || nv ? kBN : tile_cols(max_mtiles * (I / 128), d->num_sms);
-    int n2 = routed || nv ? kBN : tile_cols(max_mtiles * ((H + kBN - 1) / kBN), d->num_sms);
+    int n1 = routed || nv || a8 ? kBN : tile_cols(max_mtiles * (I / 128), d->num_sms);
+    int n2 = routed || nv || a8 ? kBN : tile_cols(max_mtiles * ((H + kBN - 1) / kBN), d->num_sms);
     if (fused && (n1 == 128 || n2 == 128)) n1 = n2 = 128;
 
     // L1: [R, H] x [2I, H]^T per expert, fused SiLU(gate) * up and MX re-quant.
     CUtensorMap ta1, tb1, ty1, ta2, tb2, ty2;
-    if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap_w13(&tb1, w13, H, I, E, (uint32_t)(n1 / 2)) ||
-        make_tmap_out(&ty1, hq, I / 2, R, false, n1 == 128 ? 16u : 32u))
+    if (a8) {
+        // E4M3 activations (one byte per element), E2M1 weights spread for kind::mxf8f6f4
+        if (make_tmap(&ta1, xq, H, R, 128) || make_tmap_w13_fp4s(&tb1, w13, H, I, E, (uint32_t)(n1 / 2)) ||
+            make_tmap_out(&ty1, hq, I, R, false, 32u))
+            return MX_ERR_CUDA;
+        g1.k_tiles = (int32_t)(H / 128);
+        g1.k_tail_half = 0;
+        g2.k_tiles = (int32_t)(I / 128);
+        g2.k_tail_half = 0;
+    } else if (make_tmap(&ta1, xq, H / 2, R, 128) || make_tmap_w13(&tb1, w13, H, I, E, (uint32_t)(n1 / 2)) ||
+               make_tmap_out(&ty1, hq, I / 2, R, false, n1 == 128 ? 16u : 32u)) {
         return MX_ERR_CUDA;
+    }
     g1.n_tiles = (int32_t)(I / (n1 / 2));
     g1.b_rows_per_expert = 2 * I;
     g1.n_half = I;
     g1.n_valid = I;
     g1.hq = hq;
     g1.hs = hs;
-    g1.ld_hq = I / 2;
+    g1.ld_hq = I / code_div;
     g1.ld_hs = I / sf_div;
     // L2: [R, I] x [H, I]^T per expert, BF16 out (to `out` directly without routing).
-    if (make_tmap(&ta2, hq, I / 2, R, 128) || make_tmap(&tb2, w2, I / 2, E * H, (uint32_t)n2)) return MX_ERR_CUDA;
+    if (a8 ? (make_tmap(&ta2, hq, I, R, 128) || make_tmap_fp4s(&tb2, w2, I, E * H, (uint32_t)n2))
+           : (make_tmap(&ta2, hq, I / 2, R, 128) || make_tmap(&tb2, w2, I / 2, E * H, (uint32_t)n2)))
+        return MX_ERR_CUDA;
     g2.n_tiles = (int32_t)((H + n2 - 1) / n2);
     g2.b_rows_per_expert = H;
     g2.n_valid = H;
@@ -635,6 +722,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     if (make_tmap_out(&ty2, g2.y, H, R)) return MX_ERR_CUDA;
 
     if (fused) {
+        if (nv || a8) return MX_ERR_UNSUPPORTED;
         FusedArgs fa;
         std::memset(&fa, 0, sizeof(fa));
         fa.g1 = g1;
@@ -661,26 +749,28 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     if (!mark(0)) return MX_ERR_CUDA;
     if (routed) {
         if (launch_route(topk_ids, T, K, E, rb, s, ws_status) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
-        if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s, nv != nullptr,
-                                nv ? nv->x_global : 0.0f) != cudaSuccess)
+        if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s,
+                                nv ? 1 : (a8 ? 2 : 0), nv ? nv->x_global : 0.0f) != cudaSuccess)
             return MX_ERR_CUDA;
     } else {
         if (!mark(1)) return MX_ERR_CUDA;
-        const cudaError_t qe =
-            nv ? launch_act_quant_nvfp4(static_cast<const uint16_t*>(x), nv->x_global, xq, xs, T, H, d->num_sms, s,
-                                        ws_status)
-               : launch_act_quant(static_cast<const uint16_t*>(x), xq, xs, T, H, d->num_sms, s, ws_status);
+        const uint16_t* xb = static_cast<const uint16_t*>(x);
+        const cudaError_t qe = nv ? launch_act_quant_nvfp4(xb, nv->x_global, xq, xs, T, H, d->num_sms, s, ws_status)
+                               : a8 ? launch_act_quant_mxfp8(xb, xq, xs, T, H, d->num_sms, s, ws_status)
+                                    : launch_act_quant(xb, xq, xs, T, H, d->num_sms, s, ws_status);
         if (qe != cudaSuccess) return MX_ERR_CUDA;
     }
     if (!mark(2)) return MX_ERR_CUDA;
     const int grid1 = grid_for(max_mtiles * g1.n_tiles, d->num_sms);
-    if ((nv ? launch_gemm_nvfp4_l1(ta1, tb1, ty1, g1, grid1, s) : launch_gemm_l1(ta1, tb1, ty1, g1, grid1, scales_tiled,
-                                                                                  n1, s)) != cudaSuccess ||
+    if ((nv   ? launch_gemm_nvfp4_l1(ta1, tb1, ty1, g1, grid1, s)
+         : a8 ? launch_gemm_a8(ta1, tb1, ty1, g1, grid1, true, s)
+              : launch_gemm_l1(ta1, tb1, ty1, g1, grid1, scales_tiled, n1, s)) != cudaSuccess ||
         !mark(3))
         return MX_ERR_CUDA;
     const int grid2 = grid_for(max_mtiles * g2.n_tiles, d->num_sms);
-    if ((nv ? launch_gemm_nvfp4(ta2, tb2, ty2, g2, grid2, s) : launch_gemm_l2(ta2, tb2, ty2, g2, grid2, scales_tiled,
-                                                                              n2, s)) != cudaSuccess ||
+    if ((nv   ? launch_gemm_nvfp4(ta2, tb2, ty2, g2, grid2, s)
+         : a8 ? launch_gemm_a8(ta2, tb2, ty2, g2, grid2, false, s)
+              : launch_gemm_l2(ta2, tb2, ty2, g2, grid2, scales_tiled, n2, s)) != cudaSuccess ||
         !mark(4))
         return MX_ERR_CUDA;
     if (routed) {
@@ -724,6 +814,43 @@ int moe_mxfp4_forward_fused(const void* x, const int32_t* topk_ids, const float*
                             size_t ws_bytes, mx_stream_t stream) {
     return forward_impl(x, topk_ids, topk_w, w13, s13_tiled, w2, s2_tiled, out, T, H, I, E, K, workspace, ws_bytes,
                         stream, nullptr, true, nullptr, true);
+}
+
+size_t moe_mxfp4w_mxfp8a_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed) {
+    if (check_moe_dims(T, H, I, E, K, routed != 0) != MX_OK) return 0;
+    return ws_layout(T, H, I, E, K, routed != 0, 32, 1).total;
+}
+
+int moe_mxfp4w_mxfp8a_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed,
+                                       int64_t* out) {
+    if (!out) return MX_ERR_INVALID_ARG;
+    if (int e = check_moe_dims(T, H, I, E, K, routed != 0)) return e;
+    const WsLayout L = ws_layout(T, H, I, E, K, routed != 0, 32, 1);
+    out[0] = (int64_t)L.xq;
+    out[1] = (int64_t)L.xs;
+    out[2] = (int64_t)L.hq;
+    out[3] = (int64_t)L.hs;
+    out[4] = routed ? (int64_t)L.y : -1;
+    out[5] = routed ? (int64_t)L.row_of : -1;
+    out[6] = routed ? (int64_t)L.counts : -1;
+    out[7] = routed ? (int64_t)L.offsets : -1;
+    return MX_OK;
+}
+
+int moe_mxfp4w_mxfp8a_forward_timed(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                                    const uint8_t* s13_tiled, const uint8_t* w2, const uint8_t* s2_tiled, void* out,
+                                    int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, void* workspace,
+                                    size_t ws_bytes, mx_stream_t stream, void* const* events) {
+    return forward_impl(x, topk_ids, topk_w, w13, s13_tiled, w2, s2_tiled, out, T, H, I, E, K, workspace, ws_bytes,
+                        stream, events, true, nullptr, false, true);
+}
+
+int moe_mxfp4w_mxfp8a_forward(const void* x, const int32_t* topk_ids, const float* topk_w, const uint8_t* w13,
+                              const uint8_t* s13_tiled, const uint8_t* w2, const uint8_t* s2_tiled, void* out,
+                              int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, void* workspace,
+                              size_t ws_bytes, mx_stream_t stream) {
+    return moe_mxfp4w_mxfp8a_forward_timed(x, topk_ids, topk_w, w13, s13_tiled, w2, s2_tiled, out, T, H, I, E, K,
+                                           workspace, ws_bytes, stream, nullptr);
 }
 
 size_t moe_nvfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, int routed) {

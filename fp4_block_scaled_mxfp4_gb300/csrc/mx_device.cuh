@@ -123,6 +123,52 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&f)[32], uint4& code
     return E;
 }
 
+// MXFP8 quantiser (E4M3 elements, one E8M0 scale per 32): the OCP MX rule with E4M3's
+// largest exponent 8. Scale byte floor(log2 amax) - 8 + 127, clamped at 0 (the biased
+// exponent of a normal float amax, minus 8); elements E4M3 nearest-even of x * 2^(127 - E)
+// (exact: a power-of-two scaling), saturating at +-448, sign kept (-0 -> 0x80); a block
+// holding a NaN or an infinity gets scale 255 and elements sign|0x7F. Quantises one block
+// held by this thread (floats that are BF16 numbers) into 32 code bytes (element 0 in the
+// lowest byte of codes[0].x); returns the scale byte.
+__device__ __forceinline__ uint32_t mx8_quant32(const float (&f)[32], uint4 (&codes)[2]) {
+    float amax = 0.0f;
+    uint32_t bad = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        bad |= (uint32_t)((__float_as_uint(f[i]) & 0x7F800000u) == 0x7F800000u);
+        amax = fmaxf(amax, fabsf(f[i]));
+    }
+    uint32_t w[8];
+    uint32_t E;
+    if (bad) {
+        E = 255u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            w[k] = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[k] |= (((__float_as_uint(f[4 * k + i]) >> 24) & 0x80u) | 0x7Fu) << (8 * i);
+        }
+    } else {
+        E = (uint32_t)max((int)(__float_as_uint(amax) >> 23) - 8, 0);
+        const float inv = mx_inv_scale(E);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            uint32_t lo, hi;   // the second source of each conversion lands in the low byte
+            asm("{\n\t.reg .b16 a, b;\n\t"
+                "cvt.rn.satfinite.e4m3x2.f32 a, %3, %2;\n\t"
+                "cvt.rn.satfinite.e4m3x2.f32 b, %5, %4;\n\t"
+                "cvt.u32.u16 %0, a;\n\t"
+                "cvt.u32.u16 %1, b;\n\t}"
+                : "=r"(lo), "=r"(hi)
+                : "f"(f[4 * k] * inv), "f"(f[4 * k + 1] * inv), "f"(f[4 * k + 2] * inv), "f"(f[4 * k + 3] * inv));
+            w[k] = lo | (hi << 16);
+        }
+    }
+    codes[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    codes[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    return E;
+}
+
 // E4M3 byte of a float 0 <= t <= 448: round to nearest, ties to even (the second source
 // of the x2 conversion lands in the low byte).
 __device__ __forceinline__ uint32_t e4m3_rn(float t) {
@@ -410,6 +456,11 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
            ((uint32_t)(M >> 4) << 24);
 }
+// Instruction descriptor of kind::mxf8f6f4 block-scaled MMA with E4M3 A (type 0) and E2M1 B
+// (type 5), both K-major, E8M0 scales, FP32 accumulation implied by the kind, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e2m1(int M, int N) {
+    return (0u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
 __device__ __forceinline__ uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
     return idesc | (b_id << 4) | (a_id << 29);
 }
@@ -421,6 +472,20 @@ __device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uin
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// MXFP8 x MXFP4 block-scaled MMA (K = 32): E4M3 A, E2M1 B (held in shared memory as 16
+// values per 16 bytes, the second 8 bytes of each 16 unused), one E8M0 scale per 32 elements
+// of K: each MMA reads one byte of the rows' scale words, chosen by the idesc scale ids.
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");

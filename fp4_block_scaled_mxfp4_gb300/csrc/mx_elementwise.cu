@@ -281,6 +281,18 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __rest
     pdl_launch_dependents();
 }
 
+// One thread per 32-element block, MXFP8 (act_quant8_blocks).
+__global__ void __launch_bounds__(kThreads) act_quant8_kernel(const uint4* __restrict__ x8,
+                                                              uint4* __restrict__ codes16,
+                                                              uint8_t* __restrict__ sf, int64_t blocks,
+                                                              uint32_t* clear_word) {
+    pdl_wait();
+    if (clear_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *clear_word = 0u;
+    act_quant8_blocks(x8, codes16, sf, blocks, (int64_t)blockIdx.x * kThreads + threadIdx.x,
+                      (int64_t)gridDim.x * kThreads);
+    pdl_launch_dependents();
+}
+
 // Self-test of the failure path: one thread waits, with the bounded wait every pipeline of
 // the GEMMs uses, on a freshly initialised mbarrier that nothing arrives at. The wait runs
 // out after its limit, records kErrWaitFull in the status word and the kernel returns, so
@@ -446,6 +458,14 @@ cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int
     const int64_t blocks = M * (K / 32);
     if (blocks == 0) return cudaSuccess;
     return launch_pdl(act_quant_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
+                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks, clear_word);
+}
+
+cudaError_t launch_act_quant_mxfp8(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
+                                   int num_sms, cudaStream_t s, uint32_t* clear_word) {
+    const int64_t blocks = M * (K / 32);
+    if (blocks == 0) return cudaSuccess;
+    return launch_pdl(act_quant8_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
                       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks, clear_word);
 }
 

@@ -86,16 +86,29 @@ constexpr int kMaxStages = 5;
 // copies, twice the TMEM columns per slot, and three stages. The accumulator is scaled by
 // the operands' global scales in the epilogue (L1: per expert, gate and up separately), and
 // L1 re-quantises h to NVFP4 (E4M3 per 16 against h's global).
-template <int kN, bool kNv = false>
+//
+// kA8: MXFP8 activations over the MXFP4 weights (kind::mxf8f6f4, scale_vec::1X): A holds E4M3
+// codes, one byte per element; B's E2M1 codes come through a TMA map that spreads each 8
+// bytes of 16 codes over 16 bytes of shared memory, the layout this MMA kind reads. A stage
+// then covers 128 elements of K (128 bytes per row of A and of B's image), four MMAs of
+// K = 32, and one scale word per row (one E8M0 byte per MMA, chosen by the scale ids).
+template <int kN, bool kNv = false, bool kA8 = false>
 struct Cfg {
+    static_assert(!(kNv && kA8), "one operand format per kernel");
     static constexpr int kStages = kNv ? 3 : (kN == 256 ? 4 : 5);
     static constexpr int kBBytes = kN * kBK / 2;                    // 32 or 16 KB
-    static constexpr int kWords = kNv ? 4 : 2;                      // scale words per row and stage
+    static constexpr int kKStage = kA8 ? 128 : kBK;                 // elements of K per stage
+    // bytes B's TMA box delivers: with kA8 the packed 8-byte chunks only (the 8-byte gap after
+    // each is left unwritten), half of the box's 128 bytes per row of shared memory
+    static constexpr int kBTxBytes = kA8 ? kBBytes / 2 : kBBytes;
+    static constexpr int kWords = kNv ? 4 : (kA8 ? 1 : 2);          // scale words per row and stage
     static constexpr int kWordsHalf = kWords / 2;                   // ... at a K tail of 128
-    static constexpr int kSfaBytes = (kWords / 2) * 4096;           // wide images of two words each
+    static constexpr int kImages = (kWords + 1) / 2;                // A's wide images, two words each
+    static constexpr int kSfaBytes = kImages * 4096;
     static constexpr int kSfbBytes = (kN / 128) * kWords * 512;     // per 128 rows: kWords x 512 B
     static constexpr int kSfCols = kNv ? 48 : kSfColsPerStage;      // A: 4 per word; B: 8 per word
-    static constexpr uint32_t kIdesc = kNv ? (idesc_mxf4(kBM, kN) & ~(1u << 23)) : idesc_mxf4(kBM, kN);
+    static constexpr uint32_t kIdesc = kNv ? (idesc_mxf4(kBM, kN) & ~(1u << 23))
+                                           : (kA8 ? idesc_mxf8_e2m1(kBM, kN) : idesc_mxf4(kBM, kN));
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static constexpr uint32_t kDescStageStep = kStageBytes >> 4;
     static constexpr int kStagingOff = kStages * kStageBytes;
@@ -134,10 +147,17 @@ struct Ctl {
     int abort_flag;
 };
 
-template <int kN, bool kNv = false>
+template <int kN, bool kNv = false, bool kA8 = false>
 constexpr size_t smem_bytes() {
-    return (size_t)Cfg<kN, kNv>::kStagingOff + 8 * kStagingBytes + sizeof(Ctl) + 1024;
+    return (size_t)Cfg<kN, kNv, kA8>::kStagingOff + 8 * kStagingBytes + sizeof(Ctl) + 1024;
 }
+
+// Every configuration within the 227 KB of dynamic shared memory a CTA may have.
+constexpr size_t kMaxDynSmem = 232448;
+static_assert(smem_bytes<256>() <= kMaxDynSmem, "MXFP4 256-column tile");
+static_assert(smem_bytes<128>() <= kMaxDynSmem, "MXFP4 128-column tile");
+static_assert(smem_bytes<256, true>() <= kMaxDynSmem, "NVFP4 tile");
+static_assert(smem_bytes<256, false, true>() <= kMaxDynSmem, "MXFP8-activation tile");
 
 struct Tile {
     int32_t expert;
@@ -202,9 +222,9 @@ struct PipePos {
 };
 
 // Barrier initialisation and tensor-memory allocation; every thread of the CTA calls it.
-template <int kN, bool kNv = false, bool kBTiled = true>
+template <int kN, bool kNv = false, bool kBTiled = true, bool kA8 = false>
 __device__ __forceinline__ GemmCtx gemm_setup(uint8_t* smem_raw) {
-    using C = Cfg<kN, kNv>;
+    using C = Cfg<kN, kNv, kA8>;
     constexpr int kStages = C::kStages;
     GemmCtx g;
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -239,11 +259,13 @@ __device__ __forceinline__ GemmCtx gemm_setup(uint8_t* smem_raw) {
 
 // One GEMM over its tile list (args), by every thread of the CTA in its role. Returns with the
 // role's pipeline position advanced; the epilogue's output stores are complete.
-template <bool kL1, bool kBTiled, int kN, bool kNv = false>
+template <bool kL1, bool kBTiled, int kN, bool kNv = false, bool kA8 = false>
 __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                                          const GemmArgs& args, const GemmCtx& g, PipePos& pos) {
     static_assert(!kNv || kBTiled, "NVFP4 weights come with tile-layout scales");
-    using C = Cfg<kN, kNv>;
+    static_assert(!kA8 || (kBTiled && kN == 256), "MXFP8 activations: tile-layout weight scales, 256-column tiles");
+    using C = Cfg<kN, kNv, kA8>;
+    constexpr int kXStage = kA8 ? C::kKStage : kBK / 2;    // TMA x step per stage (bytes of A, elements of B for kA8)
     constexpr int kBBytes = C::kBBytes;
     constexpr uint32_t kIdesc = C::kIdesc;
     constexpr int kStages = C::kStages;
@@ -276,13 +298,13 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                         goto producer_done;
                     const uint32_t st = sbase + s * kStageBytes;
                     const uint32_t bar = smem_u32(&ctl->full[s]);
-                    mbar_arrive_expect_tx(bar, kABytes + kBBytes);
-                    tma_load_2d(st, &tmA, kt * (kBK / 2), (int32_t)t.row0, bar);
+                    mbar_arrive_expect_tx(bar, kABytes + C::kBTxBytes);
+                    tma_load_2d(st, &tmA, kt * kXStage, (int32_t)t.row0, bar);
                     if (kL1) {
                         // w13 as [E][2][I][H/2]: kN / 2 gate rows then the matching up rows
-                        tma_load_4d(st + kABytes, &tmB, kt * (kBK / 2), nt * (kN / 2), 0, t.expert, bar);
+                        tma_load_4d(st + kABytes, &tmB, kt * kXStage, nt * (kN / 2), 0, t.expert, bar);
                     } else {
-                        tma_load_2d(st + kABytes, &tmB, kt * (kBK / 2),
+                        tma_load_2d(st + kABytes, &tmB, kt * kXStage,
                                     (int32_t)b_tile_row<false, kN>(args, t.expert, nt, 0), bar);
                     }
                 }
@@ -316,7 +338,16 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     const uint32_t sfa = sf0 + s * C::kSfCols;
                     const uint32_t sfb = sfa + (kNv ? 16 : 8);
                     const uint32_t acc0 = kt != 0;
-                    // 64 E2M1 elements (32 bytes) of K per MMA, inside the 128-byte swizzle atom
+                    // 32 bytes of K per MMA, inside the 128-byte swizzle atom: 64 E2M1 elements, or
+                    // with kA8 32 E4M3 elements of A and 32 spread E2M1 elements of B
+                    if constexpr (kA8) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma_mxf8(tmem, adesc + 2 * k, bdesc + 2 * k, idesc_with_sf_ids(kIdesc, k, k), sfa, sfb,
+                                        k == 0 ? acc0 : 1u);
+                        tc_commit(smem_u32(&ctl->empty[s]));
+                        continue;
+                    }
                     if constexpr (kNv) {
                         // one scale word per MMA: A's at +4k, B's at +8k; two MMAs at a K tail
                         const int nk = (args.k_tail_half && kt == k_tiles - 1) ? 2 : 4;
@@ -459,7 +490,7 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     const uint32_t sfa_t = tmem + kSfTmemBase + s * C::kSfCols;
                     const uint32_t sfb_t = sfa_t + (kNv ? 16 : 8);
 #pragma unroll
-                    for (int i = 0; i < C::kWords / 2; ++i)                                   // A, two K-words each
+                    for (int i = 0; i < C::kImages; ++i)                                      // A, two K-words each
                         tc_cp_128x256b(sfa_t + 8 * i, desc_sf_wide(sfa_s + 4096 * i));
                     for (int wd = 0; wd < nwords; ++wd) {
                         tc_cp_32x128b_x4(sfb_t + 8 * wd, desc_sf(sfb_s + wd * 512));          // B rows 0-127
@@ -581,6 +612,38 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                 }
                 continue;
             }
+            if (kA8 && kL1 && 32 * q + 32 <= t.rows) {
+                // MXFP8 re-quant: 32 code bytes per 32 columns of h, one TMA store of 32 rows
+                // x 32 bytes per block through the warp's staging block
+                const int64_t grow = t.row0 + row_in_tile;
+                const int64_t col0 = (int64_t)nt * (kN / 2) + (kN / 4) * hf;   // first column of h
+                uint32_t es[kHB];
+#pragma unroll
+                for (int b = 0; b < kHB; ++b) {
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) h[i] = h_value(v[b][i], v[2 + b][i]);
+                    uint4 c8[2];
+                    es[b] = mx8_quant32(h, c8);
+                    if (lane == 0) bulk_wait_read();   // the previous store has read the block
+                    __syncwarp();
+                    uint4* row = reinterpret_cast<uint4*>(staging + lane * 32);
+                    row[0] = c8[0];
+                    row[1] = c8[1];
+                    fence_proxy_async_smem();          // generic writes -> the TMA engine's reads
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, staging_s, (int32_t)(col0 + 32 * b), (int32_t)(t.row0 + 32 * q));
+                        bulk_commit();
+                    }
+                }
+                if (kHB == 2)
+                    *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col0 / 32) =
+                        (uint16_t)(es[0] | (es[kHB - 1] << 8));
+                else
+                    args.hs[grow * args.ld_hs + col0 / 32] = (uint8_t)es[0];
+                continue;
+            }
             if (kL1 && 32 * q + 32 <= t.rows) {
                 // all 32 rows of this warp are in the tile: codes through a staged TMA store
                 // of 32 rows x 16 kHB bytes
@@ -624,9 +687,18 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     float h[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) h[i] = h_value(v[b][i], v[2 + b][i]);
+                    const int64_t col = (int64_t)nt * (kN / 2) + (kN / 4) * hf + 32 * b;   // column of h
+                    if constexpr (kA8) {
+                        uint4 c8[2];
+                        const uint32_t E = mx8_quant32(h, c8);
+                        uint4* dst = reinterpret_cast<uint4*>(args.hq + grow * args.ld_hq + col);
+                        dst[0] = c8[0];
+                        dst[1] = c8[1];
+                        args.hs[grow * args.ld_hs + col / 32] = (uint8_t)E;
+                        continue;
+                    }
                     uint4 codes;
                     const uint32_t E = requant32(h, codes);
-                    const int64_t col = (int64_t)nt * (kN / 2) + (kN / 4) * hf + 32 * b;   // column of h
                     *reinterpret_cast<uint4*>(args.hq + grow * args.ld_hq + col / 2) = codes;
                     if (kNv)
                         *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col / 16) = (uint16_t)E;
@@ -661,9 +733,9 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
 // End of the CTA's GEMM work: the producer waits for the MMA commits that release the last
 // stages (no asynchronous arrive may reach shared memory after the CTA exits); after an
 // abort, copies in flight land and the tensor pipe drains before tensor memory is released.
-template <int kN, bool kNv = false>
+template <int kN, bool kNv = false, bool kA8 = false>
 __device__ __forceinline__ void gemm_finish(const GemmCtx& g, const PipePos& pos, const StatusWords& status) {
-    constexpr int kStages = Cfg<kN, kNv>::kStages;
+    constexpr int kStages = Cfg<kN, kNv, kA8>::kStages;
     Ctl* ctl = g.ctl;
     volatile int* abort_flag = &ctl->abort_flag;
     const int warp = threadIdx.x >> 5;
@@ -697,7 +769,7 @@ __device__ __forceinline__ void gemm_finish(const GemmCtx& g, const PipePos& pos
 }
 
 // One GEMM per launch: the expert GEMMs of the multi-kernel forward and the dense GEMMs.
-template <bool kL1, bool kBTiled, int kN, bool kNv = false>
+template <bool kL1, bool kBTiled, int kN, bool kNv = false, bool kA8 = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
@@ -707,14 +779,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmY);
     }
-    const GemmCtx g = gemm_setup<kN, kNv, kBTiled>(smem_raw);
+    const GemmCtx g = gemm_setup<kN, kNv, kBTiled, kA8>(smem_raw);
     // Setup done: wait for the kernels before this one, then let the next one be scheduled
     // (all of this persistent grid's CTAs are resident already, so it cannot take their SMs).
     pdl_wait();
     pdl_launch_dependents();
     PipePos pos{0u, 0u};
-    gemm_run<kL1, kBTiled, kN, kNv>(tmA, tmB, tmY, args, g, pos);
-    gemm_finish<kN, kNv>(g, pos, args.status);
+    gemm_run<kL1, kBTiled, kN, kNv, kA8>(tmA, tmB, tmY, args, g, pos);
+    gemm_finish<kN, kNv, kA8>(g, pos, args.status);
 }
 
 // The whole forward in one persistent cooperative launch ("Current Bug: vLLM produces
@@ -765,7 +837,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                        scratch + 2 * fa.E + 1, tid, kGemmThreads);
         barrier();
         for (int64_t t = blockIdx.x; t < fa.T; t += gridDim.x)
-            quant_gather_token<false>(x8, fa.ids, fa.K, fa.E, fa.H / 32, fa.rb, fa.xq, fa.xs, 0.0f, t, scratch, tid,
+            quant_gather_token<kQMx4>(x8, fa.ids, fa.K, fa.E, fa.H / 32, fa.rb, fa.xq, fa.xs, 0.0f, t, scratch, tid,
                                       kGemmThreads);
     } else {
         act_quant_blocks(x8, reinterpret_cast<uint4*>(fa.xq), fa.xs, fa.T * (fa.H / 32), cta_thread, grid_threads);
@@ -794,7 +866,7 @@ __global__ void __launch_bounds__(32) grid_sync_probe_kernel(uint32_t* counter, 
     grid_sync(counter, gridDim.x + 1, &abort_flag, status);
 }
 
-template <bool kL1, bool kBTiled, int kN, bool kNv = false>
+template <bool kL1, bool kBTiled, int kN, bool kNv = false, bool kA8 = false>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a, int grid,
                    cudaStream_t s) {
     static int configured_mask = 0;   // one bit per device
@@ -802,12 +874,13 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
-        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1, kBTiled, kN, kNv>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<kN, kNv>());
+        err = cudaFuncSetAttribute(mxf4_gemm_kernel<kL1, kBTiled, kN, kNv, kA8>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<kN, kNv, kA8>());
         if (err != cudaSuccess) return err;
         __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
-    return launch_pdl(mxf4_gemm_kernel<kL1, kBTiled, kN, kNv>, dim3(grid), dim3(kGemmThreads), smem_bytes<kN, kNv>(), s,
+    return launch_pdl(mxf4_gemm_kernel<kL1, kBTiled, kN, kNv, kA8>, dim3(grid), dim3(kGemmThreads),
+                      smem_bytes<kN, kNv, kA8>(), s,
                       ta, tb, ty, a);
 }
 
@@ -871,8 +944,10 @@ cudaError_t launch_grid_sync_probe(uint32_t* counter, StatusWords status, cudaSt
 }
 
 size_t gemm_smem_bytes() {
-    const size_t a = smem_bytes<256>(), b = smem_bytes<128>(), c = smem_bytes<256, true>();
-    return a > b ? (a > c ? a : c) : (b > c ? b : c);
+    const size_t a = smem_bytes<256>(), b = smem_bytes<128>(), c = smem_bytes<256, true>(),
+                 d = smem_bytes<256, false, true>();
+    const size_t ab = a > b ? a : b, cd = c > d ? c : d;
+    return ab > cd ? ab : cd;
 }
 
 cudaError_t launch_gemm_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
@@ -893,6 +968,12 @@ cudaError_t launch_gemm_nvfp4(const CUtensorMap& ta, const CUtensorMap& tb, cons
 cudaError_t launch_gemm_nvfp4_l1(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty,
                                  const GemmArgs& a, int grid, cudaStream_t s) {
     return launch<true, true, 256, true>(ta, tb, ty, a, grid, s);
+}
+
+cudaError_t launch_gemm_a8(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                           int grid, bool l1, cudaStream_t s) {
+    return l1 ? launch<true, true, 256, false, true>(ta, tb, ty, a, grid, s)
+              : launch<false, true, 256, false, true>(ta, tb, ty, a, grid, s);
 }
 
 }  // namespace mx

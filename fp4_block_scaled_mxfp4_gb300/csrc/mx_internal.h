@@ -124,6 +124,14 @@ cudaError_t launch_moe_fused(const CUtensorMap& ta1, const CUtensorMap& tb1, con
 // barrier count no arrival reaches (counter must be zero, in device memory).
 cudaError_t launch_grid_sync_probe(uint32_t* counter, StatusWords status, cudaStream_t s);
 
+// MXFP8 activations over MXFP4 weights (kind::mxf8f6f4, 256-column tiles, tile-layout weight
+// scales; K % 128 == 0, k_tiles = K / 128): ta E4M3 codes [rows, K] in boxes of 128 rows x
+// 128 bytes; tb the E2M1 weights through a 16U4_ALIGN16B map (boxes of 128 elements, L1 the
+// 4-D w13 view); L1 re-quantises h to MXFP8 (codes [rows, I], ty in boxes of 32 rows x 32
+// bytes), L2 writes BF16.
+cudaError_t launch_gemm_a8(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ty, const GemmArgs& a,
+                           int grid, bool l1, cudaStream_t s);
+
 // ---- element-wise kernels ----
 // Scale tensor [rows, kb] -> tile layout [ceil(rows/128)][kb/4][512 B] (kb % 4 == 0).
 cudaError_t launch_sf_tile(const uint8_t* sf, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t s);
@@ -138,6 +146,9 @@ cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* ou
 // to zero once this kernel may touch global memory (the forward's first kernel does this).
 cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
                              int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr);
+// MXFP8 activation quantisation (E4M3 codes [M, K], E8M0 sf [M, K/32]).
+cudaError_t launch_act_quant_mxfp8(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
+                                   int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr);
 // NVFP4 activation quantisation with the float32 global (codes [M, K/2], E4M3 sf [M, K/16]).
 cudaError_t launch_act_quant_nvfp4(const uint16_t* x, float global_scale, uint8_t* codes, uint8_t* sf, int64_t M,
                                    int64_t K, int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr);
@@ -187,8 +198,9 @@ struct FusedArgs {
 
 // Quantise each token row once (MXFP4, or NVFP4 with the float32 global) and write it to the
 // rows of all its routed pairs; also writes row_of (needs launch_route first).
+// fmt: 0 MXFP4, 1 NVFP4 (with the global), 2 MXFP8 (E4M3 codes [rows, H]).
 cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,
                                 int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs,
-                                cudaStream_t s, bool nvfp4 = false, float global_scale = 0.0f);
+                                cudaStream_t s, int fmt = 0, float global_scale = 0.0f);
 
 }  // namespace mx

@@ -132,17 +132,21 @@ __device__ __forceinline__ void load_bf16_block(const uint4* __restrict__ src, f
     }
 }
 
-// 3. Token t: row_of for its K pairs and the quantisation of its row (MXFP4, or NVFP4 against
-// the global g), written to the rows of all its routed pairs. One thread per block of the
-// row: 16-byte code stores (8 for NVFP4) and a scale byte per destination row, so a warp
-// writes contiguous codes and scales per row. s_rows: kMaxTopK ints of shared memory.
-template <bool kNv>
+// Activation formats of the quantisers: MXFP4 (E2M1 codes, E8M0 per 32), NVFP4 (E2M1, E4M3
+// per 16 against a float32 global) and MXFP8 (E4M3 codes, E8M0 per 32).
+enum QFmt : int { kQMx4 = 0, kQNv4 = 1, kQMx8 = 2 };
+
+// 3. Token t: row_of for its K pairs and the quantisation of its row in format kFmt (NVFP4
+// against the global g), written to the rows of all its routed pairs. One thread per block
+// of the row (32 elements; 16 for NVFP4): its codes (16, 8 or 32 bytes) and a scale byte per
+// destination row, so a warp writes contiguous codes and scales per row. s_rows: kMaxTopK
+// ints of shared memory.
+template <int kFmt>
 __device__ __forceinline__ void quant_gather_token(const uint4* __restrict__ x8, const int32_t* __restrict__ ids,
                                                    int K, int E, int64_t blocks_per_row, const RouteBufs& rb,
                                                    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, float g,
                                                    int64_t t, int32_t* s_rows, int tid, int nthreads) {
-    using Codes = typename std::conditional<kNv, uint2, uint4>::type;
-    constexpr int kLoads = kNv ? 2 : 4;
+    constexpr int kLoads = kFmt == kQNv4 ? 2 : 4;
     if (tid < K) {
         const int64_t p = t * K + tid;
         const int32_t e = __ldg(ids + p);
@@ -154,22 +158,39 @@ __device__ __forceinline__ void quant_gather_token(const uint4* __restrict__ x8,
     __syncthreads();
     if (x8 != nullptr) {
         const uint4* xrow = x8 + t * blocks_per_row * kLoads;
-        Codes* xqc = reinterpret_cast<Codes*>(xq);
-        const float r = kNv ? __frcp_rn(__fmul_rn(6.0f, g)) : 0.0f;
+        const float r = kFmt == kQNv4 ? __frcp_rn(__fmul_rn(6.0f, g)) : 0.0f;
         for (int64_t b = tid; b < blocks_per_row; b += nthreads) {
             float f[8 * kLoads];
             load_bf16_block<kLoads>(xrow + kLoads * b, f);
-            Codes codes;
-            uint32_t sb;
-            if constexpr (kNv)
-                sb = nv_quant16(f, g, r, codes);
-            else
-                sb = mx_quant32(f, codes);
-            for (int k = 0; k < K; ++k) {
-                const int32_t row = s_rows[k];
-                if (row < 0) continue;
-                xqc[(int64_t)row * blocks_per_row + b] = codes;
-                xs[(int64_t)row * blocks_per_row + b] = (uint8_t)sb;
+            if constexpr (kFmt == kQNv4) {
+                uint2 codes;
+                const uint32_t sb = nv_quant16(f, g, r, codes);
+                for (int k = 0; k < K; ++k) {
+                    const int32_t row = s_rows[k];
+                    if (row < 0) continue;
+                    reinterpret_cast<uint2*>(xq)[(int64_t)row * blocks_per_row + b] = codes;
+                    xs[(int64_t)row * blocks_per_row + b] = (uint8_t)sb;
+                }
+            } else if constexpr (kFmt == kQMx8) {
+                uint4 codes[2];
+                const uint32_t sb = mx8_quant32(f, codes);
+                for (int k = 0; k < K; ++k) {
+                    const int32_t row = s_rows[k];
+                    if (row < 0) continue;
+                    uint4* dst = reinterpret_cast<uint4*>(xq) + 2 * ((int64_t)row * blocks_per_row + b);
+                    dst[0] = codes[0];
+                    dst[1] = codes[1];
+                    xs[(int64_t)row * blocks_per_row + b] = (uint8_t)sb;
+                }
+            } else {
+                uint4 codes;
+                const uint32_t sb = mx_quant32(f, codes);
+                for (int k = 0; k < K; ++k) {
+                    const int32_t row = s_rows[k];
+                    if (row < 0) continue;
+                    reinterpret_cast<uint4*>(xq)[(int64_t)row * blocks_per_row + b] = codes;
+                    xs[(int64_t)row * blocks_per_row + b] = (uint8_t)sb;
+                }
             }
         }
     }
@@ -187,6 +208,21 @@ __device__ __forceinline__ void act_quant_blocks(const uint4* __restrict__ x8, u
         uint4 codes;
         sf[b] = (uint8_t)mx_quant32(f, codes);
         codes16[b] = codes;
+    }
+}
+
+// MXFP8 quantisation of 32-element blocks [first, blocks) with stride `stride`: four 16-byte
+// loads, two 16-byte code stores and a scale byte per block.
+__device__ __forceinline__ void act_quant8_blocks(const uint4* __restrict__ x8, uint4* __restrict__ codes16,
+                                                  uint8_t* __restrict__ sf, int64_t blocks, int64_t first,
+                                                  int64_t stride) {
+    for (int64_t b = first; b < blocks; b += stride) {
+        float f[32];
+        load_bf16_block<4>(x8 + 4 * b, f);
+        uint4 codes[2];
+        sf[b] = (uint8_t)mx8_quant32(f, codes);
+        codes16[2 * b] = codes[0];
+        codes16[2 * b + 1] = codes[1];
     }
 }
 

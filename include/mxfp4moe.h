@@ -221,6 +221,33 @@ int act_quant_nvfp4(const void* x_bf16, float global_scale, uint8_t* codes, uint
                     int64_t M, int64_t K, mx_stream_t stream);
 
 /*
+ * act_quant_mxfp8 -- BF16 -> MXFP8 activation quantisation, for the MXFP8-activation variant
+ * of the expert FFN (the FP8 reading of the "re-quant" of [PIPE]; the pages leave the format
+ * open): the OCP MX rule with E4M3 elements. Per row and 32-column block:
+ *   E = clamp(floor(log2 amax) - 8 + 127, 0, 254) (E = 0 when amax = 0);
+ *   code = E4M3 ("fn") nearest-even of x * 2^(127 - E), saturating at +-448, sign kept
+ *   (-0 -> 0x80). A block holding NaN/Inf gets E = 255 and codes sign|0x7F.
+ *   x uint16 [M, K], codes uint8 [M, K] (one E4M3 byte per element), sf uint8 [M, K/32].
+ *   K must be a positive multiple of 32; x and codes 16-byte aligned.
+ */
+int act_quant_mxfp8(const void* x_bf16, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
+                    mx_stream_t stream);
+
+/*
+ * mxfp8_mxfp4_gemm_bf16 -- D = bf16(A . B^T) with MXFP8 A (act_quant_mxfp8's codes and
+ * scales) and MXFP4 B on the tcgen05 tensor cores (kind::mxf8f6f4, scale_vec::1X: E4M3 x E2M1
+ * products, one E8M0 scale per 32 elements of K on each side, float32 accumulation, one BF16
+ * rounding): the GEMM of the MXFP8-activation expert FFN.
+ *   A codes uint8 [M, K] + sa uint8 [M, K/32] (row-major); B codes uint8 [N, K/2] (two E2M1
+ *   per byte, lower nibble first) + its scales in the tile layout (mxfp4_scales_to_tiled of
+ *   [N, K/32]); D uint16 [M, N]. K must be a positive multiple of 128, N of 16; M >= 0.
+ *   B must be 32-byte aligned (the tensor-memory-access unit reads it through its 4-bit
+ *   type, which needs that), the other pointers 16-byte aligned (MX_ERR_MISALIGNED).
+ */
+int mxfp8_mxfp4_gemm_bf16(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb_tiled,
+                          void* d_bf16, int64_t M, int64_t N, int64_t K, mx_stream_t stream);
+
+/*
  * nvfp4_calibrate_global -- the warm-up calibration of an NVFP4 activation global scale
  * ("Current Bug: vLLM produces empty/garbage output", "Phase 1: CuTeDSL Shared Expert
  * Kernel": a warm-up-based gs), on the GPU. For a calibration batch x uint16 [M, K] (BF16):
@@ -413,6 +440,40 @@ int moe_nvfp4_forward_timed(const void* x, const int32_t* topk_ids, const float*
                             float x_global, float h_global, void* out, int64_t T, int64_t H,
                             int64_t I, int64_t E, int64_t K, void* workspace, size_t ws_bytes,
                             mx_stream_t stream, void* const* events);
+
+/*
+ * moe_mxfp4w_mxfp8a_forward -- the MoE expert FFN of moe_mxfp4_forward_tiled with MXFP8
+ * activations over the same MXFP4 weights (the FP8 reading of [PIPE]'s "re-quant": both
+ * activation quantisations use act_quant_mxfp8's rule; the GEMMs are
+ * mxfp8_mxfp4_gemm_bf16's):
+ *   xq = act_quant_mxfp8(x); g, u = xq[t] . w13[e]^T (gate, up);
+ *   h = bf16(silu(bf16(g)) * bf16(u)), hq = act_quant_mxfp8(h) (fused epilogue);
+ *   y = bf16(hq . w2[e]^T); out[t] = bf16(sum_k topk_w[t, k] * y(t, k)).
+ *   Arguments, routing, shared-expert mode and errors as moe_mxfp4_forward_tiled (weight
+ *   scales in the tile layout), with the workspace of moe_mxfp4w_mxfp8a_workspace_size; H
+ *   and I multiples of 128; w13 and w2 32-byte aligned (MX_ERR_MISALIGNED).
+ */
+int moe_mxfp4w_mxfp8a_forward(const void* x, const int32_t* topk_ids, const float* topk_w,
+                              const uint8_t* w13, const uint8_t* s13_tiled, const uint8_t* w2,
+                              const uint8_t* s2_tiled, void* out, int64_t T, int64_t H, int64_t I,
+                              int64_t E, int64_t K, void* workspace, size_t ws_bytes,
+                              mx_stream_t stream);
+
+/* moe_mxfp4w_mxfp8a_forward recording the six phase events of moe_mxfp4_forward_timed. */
+int moe_mxfp4w_mxfp8a_forward_timed(const void* x, const int32_t* topk_ids, const float* topk_w,
+                                    const uint8_t* w13, const uint8_t* s13_tiled, const uint8_t* w2,
+                                    const uint8_t* s2_tiled, void* out, int64_t T, int64_t H,
+                                    int64_t I, int64_t E, int64_t K, void* workspace,
+                                    size_t ws_bytes, mx_stream_t stream, void* const* events);
+
+/*
+ * moe_mxfp4w_mxfp8a_workspace_size / _layout -- as the moe_mxfp4_ pair, for
+ * moe_mxfp4w_mxfp8a_forward: xq [R, H] and hq [R, I] hold one E4M3 byte per element.
+ */
+size_t moe_mxfp4w_mxfp8a_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K,
+                                        int routed);
+int moe_mxfp4w_mxfp8a_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K,
+                                       int routed, int64_t* out);
 
 /*
  * moe_nvfp4_workspace_size / moe_nvfp4_workspace_layout -- as the moe_mxfp4_ pair, for

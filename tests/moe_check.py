@@ -34,15 +34,76 @@ ACC_ALLOW = 2.0 ** -14      # float32 accumulation allowance, relative to sum |a
 SILU_ALLOW = 2.0 ** -20     # float32 SiLU / product allowance, relative
 # Re-quant blocks allowed to differ from the oracle's decision (step 2). A block differs
 # only where the float32 accumulation or SiLU moves one of its BF16 or E2M1 decisions
-# across a boundary; measured on the full-size shared, decode and prefill configs in both
-# formats that is 1.6e-4 to 6e-4 of the blocks. The cap is 2^-9 (about 2e-3), three to
-# twelve times that, with a floor of 4 blocks for small samples.
+# across a boundary; measured on the full-size shared, decode and prefill configs with
+# E2M1 codes (MXFP4 and NVFP4) that is 1.6e-4 to 6e-4 of the blocks. The cap is 2^-9
+# (about 2e-3), three to twelve times that, with a floor of 4 blocks for small samples.
+# E4M3 codes (MXFP8 activations, reading R18) carry 3 mantissa bits against E2M1's 1, so
+# their decision boundaries are 4x denser and a one-ULP change of h moves a code 4x as
+# often: the cap scales by that factor to 2^-7 (measured 6.7e-4 to 2.2e-3).
 FLIP_FRAC = 2.0 ** -9
+FLIP_FRAC_E4M3 = FLIP_FRAC * 4
 FLIP_MIN = 4
 
 
-def flip_cap(blocks: int) -> int:
-    return max(FLIP_MIN, int(FLIP_FRAC * blocks))
+def flip_cap(blocks: int, frac: float = FLIP_FRAC) -> int:
+    return max(FLIP_MIN, int(frac * blocks))
+
+
+def check_mx8_requant_decisions(g, u, absg, absu, hq_gpu, hs_gpu):
+    """Step 2 for MXFP8 activations (reading R18): every GPU block (E8M0 scale + 32 E4M3
+    codes) must be the MXFP8 quantisation of some h' in the interval the float32
+    accumulation and SiLU allow around the oracle's h. Returns (differ [n, I/32], at_risk)
+    as check_requant_decisions."""
+    n, I = g.shape
+    h_lo, h_hi = _h_interval(g, u, absg, absu)
+    mag_lo = np.where((h_lo <= 0) & (h_hi >= 0), 0.0, np.minimum(np.abs(h_lo), np.abs(h_hi)))
+    mag_hi = np.maximum(np.abs(h_lo), np.abs(h_hi))
+    nb = I // 32
+
+    def scale_byte(amax):
+        _, e = np.frexp(amax)
+        return np.where(amax > 0, np.clip(e - 1 - 8 + 127, 0, 254), 0)
+
+    E_lo = scale_byte(mag_lo.reshape(n, nb, 32).max(-1))
+    E_hi = scale_byte(mag_hi.reshape(n, nb, 32).max(-1))
+    hs = hs_gpu.astype(np.int64)
+    bad_scale = (hs < E_lo) | (hs > E_hi) | (hs == 255)
+    assert not bad_scale.any(), (f"MXFP8 re-quant scale outside the admissible range at "
+                                 f"{np.argwhere(bad_scale)[0].tolist()}")
+    mult = np.repeat(np.ldexp(1.0, 127 - hs), 32, axis=1)
+    table = oracle.e4m3fn_decode(np.arange(256))
+    v_gpu = table[hq_gpu]
+
+    def qv(h):
+        sv = h * mult
+        mag = oracle.e4m3_round_code(np.minimum(np.abs(sv), 448.0))
+        return np.where(np.signbit(sv), -1.0, 1.0) * table[mag]
+
+    v_lo, v_hi = qv(h_lo), qv(h_hi)
+    bad = (v_gpu < np.minimum(v_lo, v_hi)) | (v_gpu > np.maximum(v_lo, v_hi))
+    assert not bad.any(), (f"MXFP8 re-quant code outside the admissible range at {np.argwhere(bad)[0].tolist()}: "
+                           f"gpu {v_gpu[bad][0]}, admissible [{v_lo[bad][0]}, {v_hi[bad][0]}]")
+    ref_q, ref_s = oracle.act_quant_mxfp8(oracle.swiglu_bf16(g, u))
+    differ = (ref_s != hs_gpu) | (ref_q.reshape(n, nb, 32) != hq_gpu.reshape(n, nb, 32)).any(-1)
+    at_risk = (E_lo != E_hi) | (v_lo != v_hi).reshape(n, nb, 32).any(-1)
+    return differ, int(at_risk.sum())
+
+
+def _h_interval(g, u, absg, absu):
+    """The extreme BF16 candidates of h = bf16(silu(bf16(g')) * bf16(u')) for g', u' within the
+    float32 accumulation allowance of the exact g, u, with the float32 SiLU allowance."""
+    to = oracle.bf16_bits_to_f64
+    fr = oracle.bf16_bits_from_f64
+    eg, eu = absg * ACC_ALLOW, absu * ACC_ALLOW
+    gs = [to(fr(g - eg)), to(fr(g + eg))]
+    us = [to(fr(u - eu)), to(fr(u + eu))]
+    with np.errstate(over="ignore"):
+        corners = np.stack([gg / (1.0 + np.exp(-gg)) * uu for gg in gs for uu in us])
+    lo = corners.min(0)
+    hi = corners.max(0)
+    lo = lo - np.abs(lo) * SILU_ALLOW
+    hi = hi + np.abs(hi) * SILU_ALLOW
+    return to(fr(lo)), to(fr(hi))
 
 
 def tile_edge_tokens(topk_ids, E: int, tail_tiles: int = 2, per_tail: int = 4, tile_rows: int = 128):
@@ -132,13 +193,18 @@ def check_requant_decisions(g, u, absg, absu, hq_gpu, hs_gpu):
     return differ, int(at_risk.sum())
 
 
-def check_moe_run(mx, d, tokens=None) -> dict:
-    """d: a test `Dev` holding the device inputs, output and workspace of a finished run."""
+def check_moe_run(mx, d, tokens=None, mxfp8=False) -> dict:
+    """d: a test `Dev` holding the device inputs, output and workspace of a finished run.
+    mxfp8: the run was moe_mxfp4w_mxfp8a_forward (MXFP8 activations, reading R18)."""
     inp = d.inp
     T, H, I, E, K = inp.T, inp.H, inp.I, inp.E, inp.K
     routed = inp.topk_ids is not None
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
-    L = mx.moe_mxfp4_workspace_layout(T, H, I, E, K, routed)
+    cdiv = 1 if mxfp8 else 2                                   # activation elements per code byte
+    quant = oracle.act_quant_mxfp8 if mxfp8 else oracle.act_quant_mxfp4
+    values = oracle.mxfp8_values if mxfp8 else oracle.mxfp4_values
+    decisions = check_mx8_requant_decisions if mxfp8 else check_requant_decisions
+    L = (mx.moe_mxfp4w_mxfp8a_workspace_layout if mxfp8 else mx.moe_mxfp4_workspace_layout)(T, H, I, E, K, routed)
     R = T * K if routed else T
     out_gpu = bf16_host(d.out)[tok]
     ids = inp.topk_ids[tok].astype(np.int64) if routed else np.zeros((tok.size, 1), np.int64)
@@ -148,10 +214,10 @@ def check_moe_run(mx, d, tokens=None) -> dict:
         row_of = tok[:, None]
 
     # 1. first quantisation, bit-exact
-    xq_ref, xs_ref = oracle.act_quant_mxfp4(inp.x[tok])
-    xq_all = _ws_view(d.ws, L["xq"], R, H // 2)
+    xq_ref, xs_ref = quant(inp.x[tok])
+    xq_all = _ws_view(d.ws, L["xq"], R, H // cdiv)
     xs_all = _ws_view(d.ws, L["xs"], R, H // 32)
-    hq_all = _ws_view(d.ws, L["hq"], R, I // 2)
+    hq_all = _ws_view(d.ws, L["hq"], R, I // cdiv)
     hs_all = _ws_view(d.ws, L["hs"], R, I // 32)
     y_all = _ws_view(d.ws, L["y"], R, H, "bf16") if routed else None
     for j in range(ids.shape[1]):
@@ -159,9 +225,9 @@ def check_moe_run(mx, d, tokens=None) -> dict:
         rows = row_of[live, j]
         np.testing.assert_array_equal(xq_all[rows], xq_ref[live], err_msg="xq")
         np.testing.assert_array_equal(xs_all[rows], xs_ref[live], err_msg="xs")
-    xv = oracle.mxfp4_values(xq_ref, xs_ref)
+    xv = values(xq_ref, xs_ref)
 
-    flips = _Flips(tok.size, ids.shape[1])
+    flips = _Flips(tok.size, ids.shape[1], FLIP_FRAC_E4M3 if mxfp8 else FLIP_FRAC)
     y_cond = np.zeros((tok.size, ids.shape[1], H))
     for e in range(E):
         sel = np.argwhere((ids == e))
@@ -173,11 +239,10 @@ def check_moe_run(mx, d, tokens=None) -> dict:
         gu = xv[i_s] @ W13.T
         agu = np.abs(xv[i_s]) @ np.abs(W13).T
         del W13
-        flips.add(i_s, k_s, *check_requant_decisions(gu[:, :I], gu[:, I:], agu[:, :I], agu[:, I:], hq_all[rows],
-                                                      hs_all[rows]))
+        flips.add(i_s, k_s, *decisions(gu[:, :I], gu[:, I:], agu[:, :I], agu[:, I:], hq_all[rows], hs_all[rows]))
         # 3. L2 on the GPU's own decisions
         W2 = oracle.mxfp4_values(inp.w2[e], inp.s2[e])
-        hv = oracle.mxfp4_values(hq_all[rows], hs_all[rows])
+        hv = values(hq_all[rows], hs_all[rows])
         exact = hv @ W2.T
         if routed:
             assert_gemm_close(y_all[rows], exact, np.abs(hv) @ np.abs(W2).T, f"L2 expert {e}")
@@ -189,7 +254,8 @@ def check_moe_run(mx, d, tokens=None) -> dict:
     else:
         stats = assert_moe_close(out_gpu, oracle.bf16_bits_from_f64(y_cond[:, 0]),
                                  "out vs oracle on the GPU's re-quant decisions")
-    ref = oracle.moe_forward(inp.x, inp.topk_ids, inp.topk_w, inp.w13, inp.s13, inp.w2, inp.s2, I, tokens=tok)
+    forward = oracle.moe_mxfp8_forward if mxfp8 else oracle.moe_forward
+    ref = forward(inp.x, inp.topk_ids, inp.topk_w, inp.w13, inp.s13, inp.w2, inp.s2, I, tokens=tok)
     return _unconditioned(stats, flips, out_gpu, ref)
 
 
@@ -197,8 +263,9 @@ class _Flips:
     """Step 2's tally: blocks checked, blocks whose decision differs from the oracle's, blocks
     at risk, and which (token, slot) rows hold a differing block."""
 
-    def __init__(self, n, K):
+    def __init__(self, n, K, frac=FLIP_FRAC):
         self.blocks = self.differ = self.at_risk = 0
+        self.frac = frac
         self.row = np.zeros((n, K), dtype=bool)
 
     def add(self, i_s, k_s, differ, at_risk):
@@ -208,7 +275,7 @@ class _Flips:
         self.row[i_s, k_s] |= differ.any(-1)
 
     def check(self):
-        cap = flip_cap(self.blocks)
+        cap = flip_cap(self.blocks, self.frac)
         assert self.differ <= cap, (f"{self.differ} of {self.blocks} re-quant blocks differ from the oracle's "
                                     f"decision (cap {cap}; {self.at_risk} at risk)")
         return cap

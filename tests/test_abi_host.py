@@ -52,6 +52,26 @@ def test_check_workspace_validation(lib):
     assert lib.mx_selftest_wait_timeout_ws(FAKE + 16, None) == MX_ERR_MISALIGNED
 
 
+def test_mxfp8_path_validation(lib):
+    assert lib.act_quant_mxfp8(FAKE, FAKE, FAKE, 4, 48, None) == MX_ERR_UNSUPPORTED              # K % 32
+    assert lib.act_quant_mxfp8(ODD, FAKE, FAKE, 4, 64, None) == MX_ERR_MISALIGNED
+    assert lib.act_quant_mxfp8(FAKE, FAKE, FAKE, 0, 64, None) == MX_OK                           # nothing to do
+    assert lib.mxfp8_mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 256, 192, None) == MX_ERR_UNSUPPORTED
+    assert lib.mxfp8_mxfp4_gemm_bf16(FAKE, FAKE, FAKE + 16, FAKE, FAKE, 8, 256, 256, None) == MX_ERR_MISALIGNED
+    assert lib.mxfp8_mxfp4_gemm_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 256, 256, None) == MX_OK
+    # the forward: B operands must be 32-byte aligned; workspace sized for one code byte per element
+    T, H, I, E, K = 8, 256, 256, 4, 2
+    n8 = lib.moe_mxfp4w_mxfp8a_workspace_size(T, H, I, E, K, 1)
+    n4 = lib.moe_mxfp4_workspace_size(T, H, I, E, K, 1)
+    assert n8 > n4 > 0
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, T, H, I, E, K]
+    assert lib.moe_mxfp4w_mxfp8a_forward(*args, FAKE, n8 - 1, None) == MX_ERR_WORKSPACE
+    bad = list(args)
+    bad[3] = FAKE + 16                                                                        # w13
+    assert lib.moe_mxfp4w_mxfp8a_forward(*bad, FAKE, n8, None) == MX_ERR_MISALIGNED
+    assert lib.moe_mxfp4w_mxfp8a_forward(FAKE, FAKE, None, *args[3:], FAKE, n8, None) == MX_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     assert lib.mx_status_string(0) == b"MX_OK"
     assert lib.mx_status_string(4) == b"MX_ERR_WORKSPACE"
