@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstring>
 #include <mutex>
 
@@ -54,6 +56,29 @@ int device_info(DeviceInfo** out) {
     *out = &d;
     return MX_OK;
 }
+
+// NVTX ranges (domain "mxfp4moe") around each call's launch sequence and each phase of a
+// forward, so a timeline profiler shows which launches belong to which step. They mark the
+// host side only; without a profiler attached a range costs a null-pointer check.
+nvtxDomainHandle_t nvtx_domain() {
+    static nvtxDomainHandle_t d = nvtxDomainCreateA("mxfp4moe");
+    return d;
+}
+
+struct NvtxRange {
+    explicit NvtxRange(const char* name) {
+        nvtxEventAttributes_t a;
+        std::memset(&a, 0, sizeof(a));
+        a.version = NVTX_VERSION;
+        a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        a.message.ascii = name;
+        nvtxDomainRangePushEx(nvtx_domain(), &a);
+    }
+    ~NvtxRange() { nvtxDomainRangePop(nvtx_domain()); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -635,6 +660,10 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MX_ERR_MISALIGNED;
     DeviceInfo* d;
     if (int e = device_info(&d)) return e;
+    const NvtxRange range(fused ? "moe_mxfp4_forward_fused"
+                          : nv  ? "moe_nvfp4_forward"
+                          : a8  ? "moe_mxfp4w_mxfp8a_forward"
+                                : "moe_mxfp4_forward");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     auto mark = [&](int i) -> bool {
         return !(events && events[i]) || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
@@ -748,11 +777,13 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
 
     if (!mark(0)) return MX_ERR_CUDA;
     if (routed) {
+        const NvtxRange r("route + quantise");
         if (launch_route(topk_ids, T, K, E, rb, s, ws_status) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
         if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s,
                                 nv ? 1 : (a8 ? 2 : 0), nv ? nv->x_global : 0.0f) != cudaSuccess)
             return MX_ERR_CUDA;
     } else {
+        const NvtxRange r("quantise");
         if (!mark(1)) return MX_ERR_CUDA;
         const uint16_t* xb = static_cast<const uint16_t*>(x);
         const cudaError_t qe = nv ? launch_act_quant_nvfp4(xb, nv->x_global, xq, xs, T, H, d->num_sms, s, ws_status)
@@ -761,6 +792,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
         if (qe != cudaSuccess) return MX_ERR_CUDA;
     }
     if (!mark(2)) return MX_ERR_CUDA;
+    const NvtxRange r_gemm("L1 + L2 + combine");
     const int grid1 = grid_for(max_mtiles * g1.n_tiles, d->num_sms);
     if ((nv   ? launch_gemm_nvfp4_l1(ta1, tb1, ty1, g1, grid1, s)
          : a8 ? launch_gemm_a8(ta1, tb1, ty1, g1, grid1, true, s)
