@@ -394,6 +394,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+// 8 bytes (both addresses 8-byte aligned); bytes past src_bytes (0, 4 or 8) are zero-filled.
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
 // Arrive on `bar` once every cp.async this thread issued before has completed; the
 // arrival counts toward the barrier's expected count (which must include it).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -412,22 +412,25 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                                       args.sfb + (grp[h] * args.kw + C::kWords * kt) * 512, sf_bytes, bar);
                 }
                 if (kBTiled && kN == 128) {
-                    // B scales in tile layout for a 128-row tile of two 64-row pieces (L1) that
-                    // need not share a 128-row group: per 32-row chunk c, this lane's word of
-                    // row 32 c + lane, at byte lane * 16 + 4 j of its group's block
+                    // B scales in tile layout for a 128-row tile of two 64-row pieces p (L1: gate
+                    // and up) that need not share a 128-row group. A piece starts on a 64-row
+                    // boundary, so in its group's block this lane's words of rows r0 + lane and
+                    // r0 + 32 + lane are 8 contiguous bytes; they go to bytes 8 p .. 8 p + 7 of
+                    // the lane's 16 (rows 64 p + lane, 64 p + 32 + lane of the tile), zero past
+                    // the last row of B
                     const uint32_t sfb_s = st + kABytes + kBBytes + kSfaBytes;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int64_t r0 = b_tile_row<kL1, kN>(args, t.expert, nt, 32 * c);   // multiple of 32
-                        const bool valid = r0 + lane < args.b_rows;
-                        const uint8_t* src = args.sfb + (valid ? ((r0 >> 7) * args.kw + 2 * kt) * 512 + lane * 16 +
-                                                                      ((r0 & 127) >> 5) * 4
-                                                                : 0);
+                    for (int p = 0; p < 2; ++p) {
+                        const int64_t r0 = b_tile_row<kL1, kN>(args, t.expert, nt, 64 * p);   // multiple of 64
+                        const uint32_t n = (r0 + lane < args.b_rows ? 4u : 0u) +
+                                           (r0 + 32 + lane < args.b_rows ? 4u : 0u);
+                        const uint8_t* src = args.sfb + (n ? ((r0 >> 7) * args.kw + 2 * kt) * 512 + lane * 16 +
+                                                                  ((r0 & 127) >> 5) * 4
+                                                            : 0);
 #pragma unroll
                         for (int wd = 0; wd < 2; ++wd) {
-                            const bool ok = valid && (wd == 0 || !half);
-                            cp_async_4(sfb_s + wd * 512 + lane * 16 + c * 4, ok ? src + 512 * wd : args.sfb,
-                                       ok ? 4u : 0u);
+                            const uint32_t nb = (wd == 0 || !half) ? n : 0u;
+                            cp_async_8(sfb_s + wd * 512 + lane * 16 + p * 8, nb ? src + 512 * wd : args.sfb, nb);
                         }
                     }
                 }
