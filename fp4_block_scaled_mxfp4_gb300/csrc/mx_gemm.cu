@@ -434,23 +434,25 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                         }
                     }
                 }
-                // Row r = 32 j + lane of a 128-row group. B's dense blocks: 512 bytes per
-                // K-word, byte lane * 16 + j * 4. A's wide image: wide_off(r, K-word).
+                // A's wide image: K-word wd of tile row r at wide_off(r, wd). Adjacent lanes take
+                // the kWords words of one row, which lie side by side in the row-major scales, so
+                // one instruction touches 32 / kWords rows' cache lines rather than 32.
                 {
                     const uint32_t sfa_s = st + kABytes + kBBytes;
+                    constexpr int kRowsPerInst = 32 / C::kWords;
+                    const int wd = lane % C::kWords;
+                    const bool word_ok = wd < C::kWordsHalf || !half;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int64_t grow = t.row0 + 32 * j + lane;
-                        const bool valid = grow < args.a_rows;
-                        const uint8_t* src = args.sfa + (valid ? grow * args.ld_sf + kcol : 0);
-#pragma unroll
-                        for (int wd = 0; wd < C::kWords; ++wd) {
-                            const bool ok = valid && (wd < C::kWordsHalf || !half);
-                            const uint32_t dst = sfa_s + 4096 * (wd >> 1) + wide_off(32 * j + lane, wd & 1);
-                            cp_async_4(dst, ok ? src + 4 * wd : args.sfa, ok ? 4u : 0u);
-                        }
+                    for (int i = 0; i < 4 * C::kWords; ++i) {
+                        const int r = kRowsPerInst * i + lane / C::kWords;
+                        const int64_t grow = t.row0 + r;
+                        const bool ok = grow < args.a_rows && word_ok;
+                        const uint32_t dst = sfa_s + 4096 * (wd >> 1) + wide_off(r, wd & 1);
+                        cp_async_4(dst, ok ? args.sfa + grow * args.ld_sf + kcol + 4 * wd : args.sfa, ok ? 4u : 0u);
                     }
                 }
+                // B's dense blocks (row-major B scales): 512 bytes per K-word, row r = 32 j + lane
+                // of a 128-row group at byte lane * 16 + j * 4.
                 if (!kBTiled) {
                     const uint32_t sfb_s = st + kABytes + kBBytes + kSfaBytes;
 #pragma unroll
