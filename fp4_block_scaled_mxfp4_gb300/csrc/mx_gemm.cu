@@ -451,24 +451,21 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                         cp_async_4(dst, ok ? args.sfa + grow * args.ld_sf + kcol + 4 * wd : args.sfa, ok ? 4u : 0u);
                     }
                 }
-                // B's dense blocks (row-major B scales): 512 bytes per K-word, row r = 32 j + lane
-                // of a 128-row group at byte lane * 16 + j * 4.
+                // B's dense blocks (row-major B scales): 512 bytes per K-word, row r of a 128-row
+                // group at byte (r % 32) * 16 + (r / 32) * 4. As for A, adjacent lanes take the
+                // two K-words of one row.
                 if (!kBTiled) {
                     const uint32_t sfb_s = st + kABytes + kBBytes + kSfaBytes;
+                    const int wd = lane & 1;
+                    const bool word_ok = wd == 0 || !half;
 #pragma unroll
-                    for (int h = 0; h < kN / 128; ++h) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int64_t brow = b_tile_row<kL1, kN>(args, t.expert, nt, 128 * h + 32 * j + lane);
-                            const bool valid = brow < args.b_rows;
-                            const uint8_t* src = args.sfb + (valid ? brow * args.ld_sf + kcol : 0);
-#pragma unroll
-                            for (int wd = 0; wd < 2; ++wd) {
-                                const bool ok = valid && (wd == 0 || !half);
-                                const uint32_t dst = sfb_s + h * 1024 + wd * 512 + lane * 16 + j * 4;
-                                cp_async_4(dst, ok ? src + 4 * wd : args.sfb, ok ? 4u : 0u);
-                            }
-                        }
+                    for (int i = 0; i < 8 * (kN / 128); ++i) {
+                        const int r = 16 * i + (lane >> 1);              // row of the tile
+                        const int h = r >> 7, rr = r & 127;
+                        const int64_t brow = b_tile_row<kL1, kN>(args, t.expert, nt, r);
+                        const bool ok = brow < args.b_rows && word_ok;
+                        const uint32_t dst = sfb_s + h * 1024 + wd * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
+                        cp_async_4(dst, ok ? args.sfb + brow * args.ld_sf + kcol + 4 * wd : args.sfb, ok ? 4u : 0u);
                     }
                 }
                 cp_async_arrive_noinc(smem_u32(&ctl->sf_full[s]));
