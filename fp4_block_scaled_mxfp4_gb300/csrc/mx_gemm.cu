@@ -240,7 +240,9 @@ __device__ __forceinline__ GemmCtx gemm_setup(uint8_t* smem_raw) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), kFullArrivals);
             mbar_init(smem_u32(&ctl->empty[s]), 1);  // MMA commit
-            mbar_init(smem_u32(&ctl->sf_full[s]), kSfArrivals + (kBTiled && kN == 256 ? 1 : 0));
+            // + lane 0 of the loader once more with tile-layout B scales (their bulk copies'
+            // byte count, or a plain arrival where they are gathered)
+            mbar_init(smem_u32(&ctl->sf_full[s]), kSfArrivals + (kBTiled ? 1 : 0));
             mbar_init(smem_u32(&ctl->ready[s]), 1);   // scale copier commit
         }
         mbar_init(smem_u32(&ctl->tmem_full), 1);
@@ -393,25 +395,27 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                 const bool half = args.k_tail_half && (kt == k_tiles - 1);
                 const uint32_t st = sbase + s * kStageBytes;
                 const int64_t kcol = (int64_t)kt * 4 * C::kWords;   // first scale byte of this stage
-                if (kBTiled && kN == 256 && lane == 0) {
+                if (kBTiled && (kN == 256 || !kL1) && lane == 0) {
                     // B scales: the stage's kWords K-words of each 128-row group (half of them at
-                    // the K tail); each 128-row half of the tile is one whole group of the tile
-                    // layout
+                    // the K tail); each 128-row part of the tile is one whole group of the tile
+                    // layout (L1's 128-column tiles are not: their gate and up halves are
+                    // gathered below)
+                    constexpr int kGroups = kN / 128;
                     const uint32_t sf_bytes = (uint32_t)((half ? C::kWordsHalf : C::kWords) * 512);
                     const uint32_t bar = smem_u32(&ctl->sf_full[s]);
-                    int64_t grp[2];
+                    int64_t grp[kGroups];
                     uint32_t tx = 0;
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < kGroups; ++h) {
                         grp[h] = b_tile_row<kL1, kN>(args, t.expert, nt, 128 * h) / 128;
                         if (grp[h] < args.b_groups) tx += sf_bytes;
                     }
                     mbar_arrive_expect_tx(bar, tx);
-                    for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < kGroups; ++h)
                         if (grp[h] < args.b_groups)
                             bulk_load(st + kABytes + kBBytes + kSfaBytes + h * (C::kWords * 512),
                                       args.sfb + (grp[h] * args.kw + C::kWords * kt) * 512, sf_bytes, bar);
                 }
-                if (kBTiled && kN == 128) {
+                if (kBTiled && kN == 128 && kL1) {
                     // B scales in tile layout for a 128-row tile of two 64-row pieces p (L1: gate
                     // and up) that need not share a 128-row group. A piece starts on a 64-row
                     // boundary, so in its group's block this lane's words of rows r0 + lane and
@@ -433,6 +437,7 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                             cp_async_8(sfb_s + wd * 512 + lane * 16 + p * 8, nb ? src + 512 * wd : args.sfb, nb);
                         }
                     }
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->sf_full[s]));   // the count's bulk share
                 }
                 // A's wide image: K-word wd of tile row r at wide_off(r, wd). Adjacent lanes take
                 // the kWords words of one row, which lie side by side in the row-major scales, so
