@@ -140,15 +140,17 @@ int make_tmap_w13_fp4s(CUtensorMap* m, const void* base, int64_t H, int64_t I, i
 bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // 2-D output [rows, cols] written in boxes of 32 rows x box_bytes (32: 16 BF16 or 32 code
-// bytes; 16: 16 code bytes), no swizzle.
+// bytes; 16: 16 code bytes). BF16 boxes use the 32-byte swizzle: in shared memory the two
+// 16-byte halves of box row r trade places when bit 2 of r is set, so that the 32 lanes of
+// a warp, each writing one row, spread over all banks (the GEMM epilogue writes them so).
 int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool bf16 = true, uint32_t box_bytes = 32) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * (bf16 ? 2 : 1)};
     cuuint32_t box[2] = {bf16 ? box_bytes / 2 : box_bytes, 32u};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims,
-                          strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          bf16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }

@@ -23,22 +23,23 @@
 //               tensor core's instruction queue is short, and any other work between two
 //               MMAs leaves the pipe idle.
 //   warp 2      scale-factor loader: cp.async from the plain row-major [rows, K/32] scales
-//               of A (and of B when they are not in tile layout) into the 32-lane x 16-byte
-//               blocks tcgen05.cp reads; each lane's copies arrive on the stage's scale
-//               barrier when they land (cp.async.mbarrier.arrive), so it never blocks. With
-//               B's scales in tile layout (kBTiled) and kN = 256, lane 0 fetches them with
-//               two 1 KB bulk copies (one per 128-row group) on the same barrier; with
-//               kN = 128 each lane copies its 4-byte words.
+//               of A (and of B when they are not in tile layout) into the layouts
+//               tcgen05.cp reads, adjacent lanes taking the K-words of one row; each lane's
+//               copies arrive on the stage's scale barrier when they land
+//               (cp.async.mbarrier.arrive), so it never blocks. With B's scales in tile layout
+//               (kBTiled), lane 0 fetches each 128-row group's blocks with one bulk copy on the
+//               same barrier, except for L1's 128-column tiles, whose gate and up halves each
+//               lane takes as 8-byte pieces.
 //   warp 3      scale-factor copier: lane 0 waits for a stage's operands and scale tiles,
 //               moves the scales into that stage's TMEM slot (tcgen05.cp) and commits the
 //               copies to the stage's ready barrier, which the MMA thread waits on.
 //   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, each owning half of the
 //               columns; they drain the accumulator to registers, release it, then compute.
 //               Outputs leave through a 1 KB shared staging block per warp and an
-//               asynchronous TMA store (L2: 32 rows x 16 BF16 columns; L1: 32 rows x 32
-//               bytes of codes, 16 at kN = 128), so the warp never waits for its stores (32
-//               scattered 16-byte row pieces per store instruction otherwise); a warp whose
-//               32 rows are not all in the tile stores directly.
+//               asynchronous TMA store (L2: 32 rows x 16 BF16 columns, 32-byte swizzle;
+//               L1: 32 rows x 32 bytes of codes, 16 at kN = 128), so the warp never waits
+//               for its stores (32 scattered 16-byte row pieces per store instruction
+//               otherwise); a warp whose 32 rows are not all in the tile stores directly.
 // TMEM: columns [0, kN) accumulator; [256 + 24 s, 256 + 24 s + 24) the scale factors of
 // stage s (A: 2 K-words x 4 columns, B: 2 K-words x 8 columns).
 //
@@ -610,9 +611,13 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                         if (col + 16 * c >= args.n_valid) break;
                         if (lane == 0) bulk_wait_read();   // the previous store has read the block
                         __syncwarp();
+                        // the output map's 32-byte swizzle: row `lane`'s halves swap when bit 2
+                        // of the row is set, which keeps the warp's 16-byte writes free of bank
+                        // conflicts (4 wavefronts each instead of 8)
+                        const int sw = (lane >> 2) & 1;
                         uint4* row = reinterpret_cast<uint4*>(staging + lane * 32);
-                        row[0] = make_uint4(p[8 * c + 0], p[8 * c + 1], p[8 * c + 2], p[8 * c + 3]);
-                        row[1] = make_uint4(p[8 * c + 4], p[8 * c + 5], p[8 * c + 6], p[8 * c + 7]);
+                        row[sw] = make_uint4(p[8 * c + 0], p[8 * c + 1], p[8 * c + 2], p[8 * c + 3]);
+                        row[sw ^ 1] = make_uint4(p[8 * c + 4], p[8 * c + 5], p[8 * c + 6], p[8 * c + 7]);
                         fence_proxy_async_smem();          // generic writes -> the TMA engine's reads
                         __syncwarp();
                         if (lane == 0) {
