@@ -873,6 +873,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_finish<kN, false>(g, pos, fa.status);
 }
 
+// The persistent forward's routing scratch (count, scan, and the quantise-gather's K row
+// indices) lives in the stage ring, which it must fit for the largest expert count.
+static_assert(route_count_smem(kMaxExperts) <= (size_t)Cfg<128>::kStagingOff &&
+                  route_scan_smem(kMaxExperts) <= (size_t)Cfg<128>::kStagingOff &&
+                  (size_t)kMaxTopK * 4 <= (size_t)Cfg<128>::kStagingOff,
+              "routing scratch must fit in the stage ring");
+static_assert(Cfg<128>::kStagingOff <= Cfg<256>::kStagingOff, "the 128-column ring is the smaller");
+
 // Self-test of the grid barrier's failure path: every CTA waits for one arrival more than the
 // grid has, runs out after the wait limit, records kErrWaitGrid and returns.
 __global__ void __launch_bounds__(32) grid_sync_probe_kernel(uint32_t* counter, StatusWords status) {
