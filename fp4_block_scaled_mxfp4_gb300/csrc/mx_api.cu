@@ -150,8 +150,8 @@ int make_tmap_out(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool b
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          bf16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          bf16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
@@ -171,8 +171,8 @@ constexpr size_t kWsSyncOff = 256;
 struct WsLayout {
     int64_t R = 0, nchunks = 0, max_mtiles = 0;
     size_t status = 0, sync = 0, num_mtiles = 0, counts = 0, offsets = 0, chunk_counts = 0, chunk_base = 0, local_rank = 0,
-           row_of = 0, tile_expert = 0, tile_row0 = 0, tile_rows = 0, xq = 0, xs = 0, hq = 0, hs = 0, y = 0,
-           total = 0;
+           row_of = 0, tile_expert = 0, tile_row0 = 0, tile_rows = 0, tile_base = 0, xq = 0, xs = 0, hq = 0, hs = 0,
+           y = 0, total = 0;
 };
 
 // code_div: activation elements per code byte (2 for E2M1, 1 for the MXFP8 path's E4M3).
@@ -201,11 +201,19 @@ WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool r
         L.tile_expert = take(4 * (size_t)L.max_mtiles);
         L.tile_row0 = take(4 * (size_t)L.max_mtiles);
         L.tile_rows = take(4 * (size_t)L.max_mtiles);
+        L.tile_base = take(4 * (size_t)(E + 1));
     }
+    // The routed MXFP4 forward (sf_div 32, code_div 2) keeps xs and hs stage-major: whole M
+    // tiles x K stages x two 512-byte words, which also holds them row-major
+    const bool stage_major = routed && sf_div == 32 && code_div == 2;
+    auto scale_bytes = [&](int64_t cols) {
+        return stage_major ? (size_t)L.max_mtiles * (size_t)((cols + kBK - 1) / kBK) * 1024
+                           : (size_t)L.R * (size_t)(cols / sf_div);
+    };
     L.xq = take((size_t)L.R * (size_t)(H / code_div));
-    L.xs = take((size_t)L.R * (size_t)(H / sf_div));
+    L.xs = take(scale_bytes(H));
     L.hq = take((size_t)L.R * (size_t)(I / code_div));
-    L.hs = take((size_t)L.R * (size_t)(I / sf_div));
+    L.hs = take(scale_bytes(I));
     if (routed) L.y = take((size_t)L.R * (size_t)H * 2);
     L.total = off;
     return L;
@@ -228,6 +236,7 @@ RouteBufs route_bufs(void* ws, const WsLayout& L) {
     rb.tile_row0 = at<int32_t>(ws, L.tile_row0);
     rb.tile_rows = at<int32_t>(ws, L.tile_rows);
     rb.num_mtiles = at<int32_t>(ws, L.num_mtiles);
+    rb.tile_base = at<int32_t>(ws, L.tile_base);
     rb.nchunks = L.nchunks;
     return rb;
 }
@@ -777,12 +786,19 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
         return cuda_status(launch_moe_fused(ta1, tb1, ty1, ta2, tb2, ty2, fa, n1, d->num_sms, s));
     }
 
+    // Routed MXFP4: x's and h's scales stage-major, in the order the GEMMs' scale loaders read
+    // them. (Without routing the stage-major writes cost the short quantiser more than the
+    // GEMMs gain.)
+    const bool stage_major = routed && !nv && !a8;
+    const int64_t sm_k_tiles = stage_major ? g1.k_tiles : 0;
+    g1.a_sm = g2.a_sm = stage_major ? 1 : 0;
+    g1.hs_k_tiles = stage_major ? g2.k_tiles : 0;
     if (!mark(0)) return MX_ERR_CUDA;
     if (routed) {
         const NvtxRange r("route + quantise");
         if (launch_route(topk_ids, T, K, E, rb, s, ws_status) != cudaSuccess || !mark(1)) return MX_ERR_CUDA;
         if (launch_quant_gather(static_cast<const uint16_t*>(x), topk_ids, T, K, E, H, rb, xq, xs, s,
-                                nv ? 1 : (a8 ? 2 : 0), nv ? nv->x_global : 0.0f) != cudaSuccess)
+                                nv ? 1 : (a8 ? 2 : 0), nv ? nv->x_global : 0.0f, sm_k_tiles) != cudaSuccess)
             return MX_ERR_CUDA;
     } else {
         const NvtxRange r("quantise");
@@ -790,7 +806,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
         const uint16_t* xb = static_cast<const uint16_t*>(x);
         const cudaError_t qe = nv ? launch_act_quant_nvfp4(xb, nv->x_global, xq, xs, T, H, d->num_sms, s, ws_status)
                                : a8 ? launch_act_quant_mxfp8(xb, xq, xs, T, H, d->num_sms, s, ws_status)
-                                    : launch_act_quant(xb, xq, xs, T, H, d->num_sms, s, ws_status);
+                                    : launch_act_quant(xb, xq, xs, T, H, d->num_sms, s, ws_status, sm_k_tiles);
         if (qe != cudaSuccess) return MX_ERR_CUDA;
     }
     if (!mark(2)) return MX_ERR_CUDA;

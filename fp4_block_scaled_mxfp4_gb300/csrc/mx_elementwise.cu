@@ -273,11 +273,12 @@ __global__ void __launch_bounds__(kThreads) fp8_dequant_kernel(const uint8_t* __
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint4* __restrict__ x8,
                                                              uint4* __restrict__ codes16,
                                                              uint8_t* __restrict__ sf, int64_t blocks,
-                                                             uint32_t* clear_word) {
+                                                             uint32_t* clear_word, int64_t blocks_per_row,
+                                                             int64_t sm_k_tiles) {
     pdl_wait();
     if (clear_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *clear_word = 0u;
     act_quant_blocks(x8, codes16, sf, blocks, (int64_t)blockIdx.x * kThreads + threadIdx.x,
-                     (int64_t)gridDim.x * kThreads);
+                     (int64_t)gridDim.x * kThreads, blocks_per_row, sm_k_tiles);
     pdl_launch_dependents();
 }
 
@@ -454,11 +455,12 @@ cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* ou
 }
 
 cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
-                             int num_sms, cudaStream_t s, uint32_t* clear_word) {
+                             int num_sms, cudaStream_t s, uint32_t* clear_word, int64_t sm_k_tiles) {
     const int64_t blocks = M * (K / 32);
     if (blocks == 0) return cudaSuccess;
     return launch_pdl(act_quant_kernel, dim3(grid_for(blocks, num_sms)), dim3(kThreads), 0, s,
-                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks, clear_word);
+                      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(codes), sf, blocks, clear_word,
+                      K / 32, sm_k_tiles);
 }
 
 cudaError_t launch_act_quant_mxfp8(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,

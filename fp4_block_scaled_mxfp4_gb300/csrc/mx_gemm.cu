@@ -440,10 +440,28 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     }
                     if (lane == 0) mbar_arrive(smem_u32(&ctl->sf_full[s]));   // the count's bulk share
                 }
-                // A's wide image: K-word wd of tile row r at wide_off(r, wd). Adjacent lanes take
-                // the kWords words of one row, which lie side by side in the row-major scales, so
-                // one instruction touches 32 / kWords rows' cache lines rather than 32.
-                {
+                // A's wide image: K-word wd of tile row r at wide_off(r, wd).
+                if (!kNv && !kA8 && args.a_sm) {
+                    // Stage-major scales (MXFP4 forward): per K-word the tile's 128 rows' words are
+                    // 512 contiguous bytes. Instruction i takes rows (lane % 8) + 8 i + 32 (lane / 8):
+                    // four 32-byte runs to read, and in the image every lane a different bank
+                    // (row r's word sits in bank 4 (r % 8) + r / 32).
+                    const uint32_t sfa_s = st + kABytes + kBBytes;
+                    const int64_t mt = (int64_t)(w / args.n_tiles);
+#pragma unroll
+                    for (int wd = 0; wd < 2; ++wd) {
+                        const bool ok = wd == 0 || !half;
+                        const uint8_t* src = args.sfa + ((mt * k_tiles + kt) * 2 + wd) * 512;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = (lane & 7) + 8 * i + 32 * (lane >> 3);
+                            cp_async_4(sfa_s + wide_off(r, wd), ok ? src + 4 * r : args.sfa, ok ? 4u : 0u);
+                        }
+                    }
+                } else {
+                    // Row-major scales: adjacent lanes take the kWords words of one row, which lie
+                    // side by side, so one instruction touches 32 / kWords rows' cache lines
+                    // rather than 32.
                     const uint32_t sfa_s = st + kABytes + kBBytes;
                     constexpr int kRowsPerInst = 32 / C::kWords;
                     const int wd = lane % C::kWords;
@@ -547,6 +565,11 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
             const float g = round_bf16(kNv ? __fmul_rn(__uint_as_float(acc_g), alpha_a) : __uint_as_float(acc_g));
             const float u = round_bf16(kNv ? __fmul_rn(__uint_as_float(acc_u), alpha_b) : __uint_as_float(acc_u));
             return round_bf16(silu_f32(g) * u);
+        };
+        // Byte of h's MXFP4 scale for block b (32 columns) of global row grow, tile row r of M
+        // tile mt: stage-major (hs_k_tiles > 0) or row-major
+        auto hs_off = [&](int64_t grow, int r, int64_t mt, int64_t b) -> int64_t {
+            return args.hs_k_tiles > 0 ? sm_scale_off(mt, r, b, args.hs_k_tiles) : grow * args.ld_hs + b;
         };
         // Re-quantisation of 32 columns of h: 16 code bytes; the scale byte (MXFP4) or the two
         // E4M3 bytes of the two 16-column blocks, low byte first (NVFP4)
@@ -688,11 +711,11 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                 if (kNv)      // four E4M3 bytes: 64 columns of h, 16 per byte
                     *reinterpret_cast<uint32_t*>(args.hs + grow * args.ld_hs + col0 / 16) =
                         es[0] | (es[kHB - 1] << 16);
-                else if (kHB == 2)
-                    *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col0 / 32) =
+                else if (kHB == 2)   // two scale bytes of one stage-major word (col0 / 32 is even)
+                    *reinterpret_cast<uint16_t*>(args.hs + hs_off(grow, row_in_tile, w / args.n_tiles, col0 / 32)) =
                         (uint16_t)(es[0] | (es[kHB - 1] << 8));
                 else
-                    args.hs[grow * args.ld_hs + col0 / 32] = (uint8_t)es[0];
+                    args.hs[hs_off(grow, row_in_tile, w / args.n_tiles, col0 / 32)] = (uint8_t)es[0];
                 continue;
             }
             if (row_in_tile >= t.rows) continue;
@@ -719,7 +742,7 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     if (kNv)
                         *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col / 16) = (uint16_t)E;
                     else
-                        args.hs[grow * args.ld_hs + col / 32] = (uint8_t)E;
+                        args.hs[hs_off(grow, row_in_tile, w / args.n_tiles, col / 32)] = (uint8_t)E;
                 }
             } else {
 #pragma unroll
@@ -877,7 +900,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // indices) lives in the stage ring, which it must fit for the largest expert count.
 static_assert(route_count_smem(kMaxExperts) <= (size_t)Cfg<128>::kStagingOff &&
                   route_scan_smem(kMaxExperts) <= (size_t)Cfg<128>::kStagingOff &&
-                  (size_t)kMaxTopK * 4 <= (size_t)Cfg<128>::kStagingOff,
+                  (size_t)kMaxTopK * 8 <= (size_t)Cfg<128>::kStagingOff,
               "routing scratch must fit in the stage ring");
 static_assert(Cfg<128>::kStagingOff <= Cfg<256>::kStagingOff, "the 128-column ring is the smaller");
 

@@ -90,6 +90,11 @@ struct GemmArgs {
     int32_t nseg;
     int32_t seg_end[kMaxSegments];
     float seg_alpha[kMaxSegments];
+    // MXFP4 forward: A's scales in the stage-major layout (sm_scale_off) instead of row-major
+    // [a_rows, K/32]; with hs_k_tiles > 0, L1 writes h's scales that way too (hs_k_tiles =
+    // ceil(I / 256), the K stages of L2).
+    int32_t a_sm;
+    int32_t hs_k_tiles;
 };
 
 size_t gemm_smem_bytes();
@@ -144,8 +149,9 @@ cudaError_t launch_fp8_dequant(const uint8_t* q, const uint8_t* sf, uint16_t* ou
                                int64_t cols, int num_sms, cudaStream_t s);
 // The activation quantisers; clear_word (optional): a forward's workspace status word, set
 // to zero once this kernel may touch global memory (the forward's first kernel does this).
+// sm_k_tiles > 0 (launch_act_quant only): sf in the stage-major layout with that many K stages.
 cudaError_t launch_act_quant(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
-                             int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr);
+                             int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr, int64_t sm_k_tiles = 0);
 // MXFP8 activation quantisation (E4M3 codes [M, K], E8M0 sf [M, K/32]).
 cudaError_t launch_act_quant_mxfp8(const uint16_t* x, uint8_t* codes, uint8_t* sf, int64_t M, int64_t K,
                                    int num_sms, cudaStream_t s, uint32_t* clear_word = nullptr);
@@ -173,6 +179,7 @@ struct RouteBufs {
     int32_t* tile_row0;
     int32_t* tile_rows;
     int32_t* num_mtiles;     // [1]
+    int32_t* tile_base;      // [E+1]: index of each expert's first M tile
     int64_t nchunks;
 };
 // clear_word: as for launch_act_quant.
@@ -199,8 +206,9 @@ struct FusedArgs {
 // Quantise each token row once (MXFP4, or NVFP4 with the float32 global) and write it to the
 // rows of all its routed pairs; also writes row_of (needs launch_route first).
 // fmt: 0 MXFP4, 1 NVFP4 (with the global), 2 MXFP8 (E4M3 codes [rows, H]).
+// sm_k_tiles > 0 (MXFP4): xs in the stage-major layout with that many K stages.
 cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,
                                 int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs,
-                                cudaStream_t s, int fmt = 0, float global_scale = 0.0f);
+                                cudaStream_t s, int fmt = 0, float global_scale = 0.0f, int64_t sm_k_tiles = 0);
 
 }  // namespace mx

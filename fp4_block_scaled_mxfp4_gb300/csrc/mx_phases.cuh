@@ -22,6 +22,15 @@ namespace mx {
 constexpr int kCountThreads = 256;                 // threads that count one chunk
 constexpr int kCountWarps = kCountThreads / 32;
 
+// Stage-major layout of an MXFP4 activation's E8M0 scales, the order the GEMM's scale loader
+// reads them in: for M tile mt (128 rows), K stage kt (256 columns, 8 blocks of 32) and scale
+// word w of the stage (4 blocks), the 128 rows' words lie in row order, 512 bytes. Block b of
+// tile row r is at this byte offset; k_tiles = ceil(K / 256). It holds as many bytes per row as
+// the row-major [rows, K/32] layout, rounded up to whole tiles and stages.
+__host__ __device__ __forceinline__ int64_t sm_scale_off(int64_t mt, int64_t r, int64_t b, int64_t k_tiles) {
+    return (((mt * k_tiles + (b >> 3)) * 2 + ((b >> 2) & 1)) * 128 + r) * 4 + (b & 3);
+}
+
 // Shared-memory scratch of route_count_chunk: s_run [E] and s_warp [kCountWarps][E].
 __host__ __device__ constexpr size_t route_count_smem(int E) { return (size_t)(1 + kCountWarps) * E * 4; }
 
@@ -101,12 +110,14 @@ __device__ __forceinline__ void route_scan(const int32_t* __restrict__ chunk_cou
         s_off[E] = off;
         s_toff[E] = toff;
         rb.offsets[E] = off;
+        rb.tile_base[E] = toff;
         *rb.num_mtiles = toff;
     }
     __syncthreads();
     for (int e = tid; e < E; e += nthreads) {
         rb.counts[e] = s_cnt[e];
         rb.offsets[e] = s_off[e];
+        rb.tile_base[e] = s_toff[e];
         const int32_t nt = (s_cnt[e] + kBM - 1) / kBM;
         for (int32_t m = 0; m < nt; ++m) {
             const int32_t idx = s_toff[e] + m;
@@ -145,14 +156,22 @@ template <int kFmt>
 __device__ __forceinline__ void quant_gather_token(const uint4* __restrict__ x8, const int32_t* __restrict__ ids,
                                                    int K, int E, int64_t blocks_per_row, const RouteBufs& rb,
                                                    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, float g,
-                                                   int64_t t, int32_t* s_rows, int tid, int nthreads) {
+                                                   int64_t t, int32_t* s_rows, int tid, int nthreads,
+                                                   int64_t sm_k_tiles = 0) {
     constexpr int kLoads = kFmt == kQNv4 ? 2 : 4;
+    // s_rows[k]: routed row of slot k (-1: dropped); s_rows[kMaxTopK + k]: with stage-major
+    // scales, that row's M tile * 128 + row in the tile
     if (tid < K) {
         const int64_t p = t * K + tid;
         const int32_t e = __ldg(ids + p);
-        int32_t row = -1;
-        if (e >= 0 && e < E) row = rb.offsets[e] + rb.chunk_base[(p / kRouteChunk) * E + e] + rb.local_rank[p];
+        int32_t row = -1, tile_pos = 0;
+        if (e >= 0 && e < E) {
+            const int32_t local = rb.chunk_base[(p / kRouteChunk) * E + e] + rb.local_rank[p];
+            row = rb.offsets[e] + local;
+            tile_pos = (rb.tile_base[e] + local / kBM) * kBM + local % kBM;
+        }
         s_rows[tid] = row;
+        s_rows[kMaxTopK + tid] = tile_pos;
         rb.row_of[p] = row;
     }
     __syncthreads();
@@ -189,7 +208,10 @@ __device__ __forceinline__ void quant_gather_token(const uint4* __restrict__ x8,
                     const int32_t row = s_rows[k];
                     if (row < 0) continue;
                     reinterpret_cast<uint4*>(xq)[(int64_t)row * blocks_per_row + b] = codes;
-                    xs[(int64_t)row * blocks_per_row + b] = (uint8_t)sb;
+                    const int32_t pos = s_rows[kMaxTopK + k];
+                    const int64_t at = sm_k_tiles ? sm_scale_off(pos / kBM, pos % kBM, b, sm_k_tiles)
+                                                  : (int64_t)row * blocks_per_row + b;
+                    xs[at] = (uint8_t)sb;
                 }
             }
         }
@@ -199,14 +221,22 @@ __device__ __forceinline__ void quant_gather_token(const uint4* __restrict__ x8,
 
 // MX quantisation of 32-element blocks [first, blocks) with stride `stride` (one block per
 // thread and step: four 16-byte loads, a 16-byte code store and a scale byte).
+// With sm_k_tiles > 0 the scales go to the stage-major layout (rows of blocks_per_row blocks).
 __device__ __forceinline__ void act_quant_blocks(const uint4* __restrict__ x8, uint4* __restrict__ codes16,
                                                  uint8_t* __restrict__ sf, int64_t blocks, int64_t first,
-                                                 int64_t stride) {
+                                                 int64_t stride, int64_t blocks_per_row = 0,
+                                                 int64_t sm_k_tiles = 0) {
     for (int64_t b = first; b < blocks; b += stride) {
         float f[32];
         load_bf16_block<4>(x8 + 4 * b, f);
         uint4 codes;
-        sf[b] = (uint8_t)mx_quant32(f, codes);
+        const uint8_t e = (uint8_t)mx_quant32(f, codes);
+        if (sm_k_tiles) {
+            const int64_t row = b / blocks_per_row, blk = b - row * blocks_per_row;
+            sf[sm_scale_off(row / kBM, row % kBM, blk, sm_k_tiles)] = e;
+        } else {
+            sf[b] = e;
+        }
         codes16[b] = codes;
     }
 }

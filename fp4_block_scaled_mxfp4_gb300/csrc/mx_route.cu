@@ -44,11 +44,11 @@ constexpr int kGatherThreads = 256;
 template <int kFmt>
 __global__ void __launch_bounds__(kGatherThreads) quant_gather_kernel(
     const uint4* __restrict__ x8, const int32_t* __restrict__ ids, int K, int E, int64_t blocks_per_row,
-    RouteBufs rb, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, float g) {
-    __shared__ int32_t s_rows[kMaxTopK];
+    RouteBufs rb, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, float g, int64_t sm_k_tiles) {
+    __shared__ int32_t s_rows[2 * kMaxTopK];
     pdl_wait();
     quant_gather_token<kFmt>(x8, ids, K, E, blocks_per_row, rb, xq, xs, g, blockIdx.x, s_rows, threadIdx.x,
-                             kGatherThreads);
+                             kGatherThreads, sm_k_tiles);
     pdl_launch_dependents();
 }
 
@@ -66,17 +66,17 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, co
 
 cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T, int64_t K, int64_t E,
                                 int64_t H, const RouteBufs& rb, uint8_t* xq, uint8_t* xs, cudaStream_t s,
-                                int fmt, float global_scale) {
+                                int fmt, float global_scale, int64_t sm_k_tiles) {
     if (T == 0) return cudaSuccess;
     const uint4* x8 = reinterpret_cast<const uint4*>(x);
     if (fmt == kQNv4)
         return launch_pdl(quant_gather_kernel<kQNv4>, dim3((unsigned)T), dim3(kGatherThreads), 0, s, x8, ids, (int)K,
-                          (int)E, (int64_t)(H / 16), rb, xq, xs, global_scale);
+                          (int)E, (int64_t)(H / 16), rb, xq, xs, global_scale, (int64_t)0);
     if (fmt == kQMx8)
         return launch_pdl(quant_gather_kernel<kQMx8>, dim3((unsigned)T), dim3(kGatherThreads), 0, s, x8, ids, (int)K,
-                          (int)E, (int64_t)(H / 32), rb, xq, xs, 0.0f);
+                          (int)E, (int64_t)(H / 32), rb, xq, xs, 0.0f, (int64_t)0);
     return launch_pdl(quant_gather_kernel<kQMx4>, dim3((unsigned)T), dim3(kGatherThreads), 0, s, x8, ids, (int)K,
-                      (int)E, (int64_t)(H / 32), rb, xq, xs, 0.0f);
+                      (int)E, (int64_t)(H / 32), rb, xq, xs, 0.0f, sm_k_tiles);
 }
 
 }  // namespace mx

@@ -301,9 +301,15 @@ size_t moe_mxfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int6
  * tensors a moe_mxfp4_forward call leaves behind (for inspection and tests; the layout may
  * change between library versions). R = T*K when routed, T otherwise. Writes 8 values:
  *   out[0] xq  uint8  [R, H/2]   MX-quantised x (routed: rows in expert-grouped order)
- *   out[1] xs  uint8  [R, H/32]  its E8M0 scales
+ *   out[1] xs  uint8             its E8M0 scales, stage-major when routed (below)
  *   out[2] hq  uint8  [R, I/2]   MX-re-quantised h = bf16(silu(g) * u)
- *   out[3] hs  uint8  [R, I/32]  its E8M0 scales
+ *   out[3] hs  uint8             its E8M0 scales, stage-major when routed
+ *   Stage-major, the order the GEMMs read the scales in: rows form M tiles of 128 (routed:
+ *   each expert's rows from its first row on, experts in order, so expert e's rows start at
+ *   tile sum_{e' < e} ceil(counts[e'] / 128)); the scale of 32-column block b of tile row r
+ *   in tile mt is at byte (((mt * S + b / 8) * 2 + (b / 4) % 2) * 128 + r) * 4 + b % 4,
+ *   S = ceil(cols / 256). Without routing, and in moe_mxfp4_forward_fused, they are row-major
+ *   [R, cols/32].
  *   out[4] y   uint16 [R, H]     BF16 L2 output (routed mode; -1 otherwise)
  *   out[5] row_of int32 [T, K], out[6] counts int32 [E], out[7] offsets int32 [E+1]
  *          (routed mode; -1 otherwise)
