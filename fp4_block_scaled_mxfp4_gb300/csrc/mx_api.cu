@@ -203,11 +203,12 @@ WsLayout ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K, bool r
         L.tile_rows = take(4 * (size_t)L.max_mtiles);
         L.tile_base = take(4 * (size_t)(E + 1));
     }
-    // The routed MXFP4 forward (sf_div 32, code_div 2) keeps xs and hs stage-major: whole M
-    // tiles x K stages x two 512-byte words, which also holds them row-major
-    const bool stage_major = routed && sf_div == 32 && code_div == 2;
+    // The routed MXFP4 and NVFP4 forwards (code_div 2) keep xs and hs stage-major: whole M
+    // tiles x K stages x 2 (MXFP4) or 4 (NVFP4) 512-byte words, which also holds them row-major
+    const bool stage_major = routed && code_div == 2;
+    const size_t words = sf_div == 16 ? 4 : 2;
     auto scale_bytes = [&](int64_t cols) {
-        return stage_major ? (size_t)L.max_mtiles * (size_t)((cols + kBK - 1) / kBK) * 1024
+        return stage_major ? (size_t)L.max_mtiles * (size_t)((cols + kBK - 1) / kBK) * words * 512
                            : (size_t)L.R * (size_t)(cols / sf_div);
     };
     L.xq = take((size_t)L.R * (size_t)(H / code_div));
@@ -786,10 +787,10 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_w, co
         return cuda_status(launch_moe_fused(ta1, tb1, ty1, ta2, tb2, ty2, fa, n1, d->num_sms, s));
     }
 
-    // Routed MXFP4: x's and h's scales stage-major, in the order the GEMMs' scale loaders read
-    // them. (Without routing the stage-major writes cost the short quantiser more than the
-    // GEMMs gain.)
-    const bool stage_major = routed && !nv && !a8;
+    // Routed MXFP4 and NVFP4: x's and h's scales stage-major, in the order the GEMMs' scale
+    // loaders read them. (Without routing the stage-major writes cost the short quantiser more
+    // than the GEMMs gain.)
+    const bool stage_major = routed && !a8;
     const int64_t sm_k_tiles = stage_major ? g1.k_tiles : 0;
     g1.a_sm = g2.a_sm = stage_major ? 1 : 0;
     g1.hs_k_tiles = stage_major ? g2.k_tiles : 0;

@@ -441,21 +441,22 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     if (lane == 0) mbar_arrive(smem_u32(&ctl->sf_full[s]));   // the count's bulk share
                 }
                 // A's wide image: K-word wd of tile row r at wide_off(r, wd).
-                if (!kNv && !kA8 && args.a_sm) {
-                    // Stage-major scales (MXFP4 forward): per K-word the tile's 128 rows' words are
-                    // 512 contiguous bytes. Instruction i takes rows (lane % 8) + 8 i + 32 (lane / 8):
-                    // four 32-byte runs to read, and in the image every lane a different bank
-                    // (row r's word sits in bank 4 (r % 8) + r / 32).
+                if (!kA8 && args.a_sm) {
+                    // Stage-major scales (routed MXFP4 and NVFP4 forwards): per K-word the tile's 128
+                    // rows' words are 512 contiguous bytes. Instruction i takes rows (lane % 8) + 8 i +
+                    // 32 (lane / 8): four 32-byte runs to read, and in the image every lane a
+                    // different bank (row r's word sits in bank 4 (r % 8) + r / 32).
                     const uint32_t sfa_s = st + kABytes + kBBytes;
                     const int64_t mt = (int64_t)(w / args.n_tiles);
 #pragma unroll
-                    for (int wd = 0; wd < 2; ++wd) {
-                        const bool ok = wd == 0 || !half;
-                        const uint8_t* src = args.sfa + ((mt * k_tiles + kt) * 2 + wd) * 512;
+                    for (int wd = 0; wd < C::kWords; ++wd) {
+                        const bool ok = wd < C::kWordsHalf || !half;
+                        const uint8_t* src = args.sfa + ((mt * k_tiles + kt) * C::kWords + wd) * 512;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int r = (lane & 7) + 8 * i + 32 * (lane >> 3);
-                            cp_async_4(sfa_s + wide_off(r, wd), ok ? src + 4 * r : args.sfa, ok ? 4u : 0u);
+                            cp_async_4(sfa_s + 4096 * (wd >> 1) + wide_off(r, wd & 1), ok ? src + 4 * r : args.sfa,
+                                       ok ? 4u : 0u);
                         }
                     }
                 } else {
@@ -569,7 +570,8 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
         // Byte of h's MXFP4 scale for block b (32 columns) of global row grow, tile row r of M
         // tile mt: stage-major (hs_k_tiles > 0) or row-major
         auto hs_off = [&](int64_t grow, int r, int64_t mt, int64_t b) -> int64_t {
-            return args.hs_k_tiles > 0 ? sm_scale_off(mt, r, b, args.hs_k_tiles) : grow * args.ld_hs + b;
+            if (args.hs_k_tiles <= 0) return grow * args.ld_hs + b;
+            return kNv ? sm_scale_off<4>(mt, r, b, args.hs_k_tiles) : sm_scale_off<2>(mt, r, b, args.hs_k_tiles);
         };
         // Re-quantisation of 32 columns of h: 16 code bytes; the scale byte (MXFP4) or the two
         // E4M3 bytes of the two 16-column blocks, low byte first (NVFP4)
@@ -708,8 +710,8 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     tma_store_2d(&tmY, staging_s, (int32_t)(col0 / 2), (int32_t)(t.row0 + 32 * q));
                     bulk_commit();
                 }
-                if (kNv)      // four E4M3 bytes: 64 columns of h, 16 per byte
-                    *reinterpret_cast<uint32_t*>(args.hs + grow * args.ld_hs + col0 / 16) =
+                if (kNv)      // four E4M3 bytes, one word: 64 columns of h, 16 per byte
+                    *reinterpret_cast<uint32_t*>(args.hs + hs_off(grow, row_in_tile, w / args.n_tiles, col0 / 16)) =
                         es[0] | (es[kHB - 1] << 16);
                 else if (kHB == 2)   // two scale bytes of one stage-major word (col0 / 32 is even)
                     *reinterpret_cast<uint16_t*>(args.hs + hs_off(grow, row_in_tile, w / args.n_tiles, col0 / 32)) =
@@ -739,8 +741,9 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     uint4 codes;
                     const uint32_t E = requant32(h, codes);
                     *reinterpret_cast<uint4*>(args.hq + grow * args.ld_hq + col / 2) = codes;
-                    if (kNv)
-                        *reinterpret_cast<uint16_t*>(args.hs + grow * args.ld_hs + col / 16) = (uint16_t)E;
+                    if (kNv)   // two E4M3 bytes of one word (col / 16 is even)
+                        *reinterpret_cast<uint16_t*>(args.hs + hs_off(grow, row_in_tile, w / args.n_tiles, col / 16)) =
+                            (uint16_t)E;
                     else
                         args.hs[hs_off(grow, row_in_tile, w / args.n_tiles, col / 32)] = (uint8_t)E;
                 }

@@ -22,13 +22,15 @@ namespace mx {
 constexpr int kCountThreads = 256;                 // threads that count one chunk
 constexpr int kCountWarps = kCountThreads / 32;
 
-// Stage-major layout of an MXFP4 activation's E8M0 scales, the order the GEMM's scale loader
-// reads them in: for M tile mt (128 rows), K stage kt (256 columns, 8 blocks of 32) and scale
-// word w of the stage (4 blocks), the 128 rows' words lie in row order, 512 bytes. Block b of
-// tile row r is at this byte offset; k_tiles = ceil(K / 256). It holds as many bytes per row as
-// the row-major [rows, K/32] layout, rounded up to whole tiles and stages.
+// Stage-major layout of an activation's block scales, the order the GEMM's scale loader reads
+// them in: for M tile mt (128 rows), K stage kt (256 columns) and scale word w of the stage (4
+// scale bytes), the 128 rows' words lie in row order, 512 bytes. kWords = words per stage: 2 for
+// MXFP4 (blocks of 32 columns), 4 for NVFP4 (blocks of 16). Block b of tile row r is at this
+// byte offset; k_tiles = ceil(K / 256). It holds as many bytes per row as the row-major
+// [rows, K / block] layout, rounded up to whole tiles and stages.
+template <int kWords = 2>
 __host__ __device__ __forceinline__ int64_t sm_scale_off(int64_t mt, int64_t r, int64_t b, int64_t k_tiles) {
-    return (((mt * k_tiles + (b >> 3)) * 2 + ((b >> 2) & 1)) * 128 + r) * 4 + (b & 3);
+    return (((mt * k_tiles + b / (4 * kWords)) * kWords + (b >> 2) % kWords) * 128 + r) * 4 + (b & 3);
 }
 
 // Shared-memory scratch of route_count_chunk: s_run [E] and s_warp [kCountWarps][E].
@@ -188,7 +190,10 @@ __device__ __forceinline__ void quant_gather_token(const uint4* __restrict__ x8,
                     const int32_t row = s_rows[k];
                     if (row < 0) continue;
                     reinterpret_cast<uint2*>(xq)[(int64_t)row * blocks_per_row + b] = codes;
-                    xs[(int64_t)row * blocks_per_row + b] = (uint8_t)sb;
+                    const int32_t pos = s_rows[kMaxTopK + k];
+                    const int64_t at = sm_k_tiles ? sm_scale_off<4>(pos / kBM, pos % kBM, b, sm_k_tiles)
+                                                  : (int64_t)row * blocks_per_row + b;
+                    xs[at] = (uint8_t)sb;
                 }
             } else if constexpr (kFmt == kQMx8) {
                 uint4 codes[2];

@@ -71,7 +71,7 @@ cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* ids, int64_t T
     const uint4* x8 = reinterpret_cast<const uint4*>(x);
     if (fmt == kQNv4)
         return launch_pdl(quant_gather_kernel<kQNv4>, dim3((unsigned)T), dim3(kGatherThreads), 0, s, x8, ids, (int)K,
-                          (int)E, (int64_t)(H / 16), rb, xq, xs, global_scale, (int64_t)0);
+                          (int)E, (int64_t)(H / 16), rb, xq, xs, global_scale, sm_k_tiles);
     if (fmt == kQMx8)
         return launch_pdl(quant_gather_kernel<kQMx8>, dim3((unsigned)T), dim3(kGatherThreads), 0, s, x8, ids, (int)K,
                           (int)E, (int64_t)(H / 32), rb, xq, xs, 0.0f, (int64_t)0);

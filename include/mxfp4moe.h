@@ -483,7 +483,10 @@ int moe_mxfp4w_mxfp8a_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t 
 
 /*
  * moe_nvfp4_workspace_size / moe_nvfp4_workspace_layout -- as the moe_mxfp4_ pair, for
- * moe_nvfp4_forward: xs [R, H/16] and hs [R, I/16] hold E4M3 scales (one per 16 columns).
+ * moe_nvfp4_forward: xs and hs hold E4M3 scales, one per 16 columns. Routed, they are
+ * stage-major with four words per stage: the scale of 16-column block b of tile row r in
+ * tile mt is at byte (((mt * S + b / 16) * 4 + (b / 4) % 4) * 128 + r) * 4 + b % 4,
+ * S = ceil(cols / 256); without routing they are row-major [R, cols/16].
  */
 size_t moe_nvfp4_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t K,
                                 int routed);

@@ -129,10 +129,12 @@ def tile_edge_tokens(topk_ids, E: int, tail_tiles: int = 2, per_tail: int = 4, t
     return np.array(sorted(pick), dtype=np.int64)
 
 
-def _ws_scales_stage_major(ws, L, off, R, cols, routed, E, T):
-    """An MXFP4 forward's x or h scales (cols = H or I) from the workspace's stage-major layout,
-    as row-major [R, cols/32]: per M tile (128 rows of one expert), K stage (256 columns) and
-    scale word (4 blocks), the tile's 128 rows' words in row order."""
+def _ws_scales_stage_major(ws, L, off, R, cols, routed, E, T, block=32):
+    """A routed forward's x or h scales (cols = H or I) from the workspace's stage-major layout,
+    as row-major [R, cols/block]: per M tile (128 rows of one expert), K stage (256 columns) and
+    scale word (4 blocks), the tile's 128 rows' words in row order. block 32: MXFP4 (2 words
+    per stage); 16: NVFP4 (4 words per stage)."""
+    words = 256 // block // 4
     if routed:
         counts = _ws_view(ws, L["counts"], 1, E, "i32")[0].astype(np.int64)
         offsets = _ws_view(ws, L["offsets"], 1, E + 1, "i32")[0].astype(np.int64)
@@ -141,14 +143,15 @@ def _ws_scales_stage_major(ws, L, off, R, cols, routed, E, T):
     ntiles = (counts + 127) // 128
     tile_base = np.concatenate([[0], np.cumsum(ntiles)])
     k_tiles = -(-cols // 256)
-    raw = _ws_view(ws, off, 1, int(tile_base[-1]) * k_tiles * 1024)[0]
+    raw = _ws_view(ws, off, 1, int(tile_base[-1]) * k_tiles * words * 512)[0]
     mt, r = np.zeros(R, np.int64), np.zeros(R, np.int64)
     for e in range(counts.size):
         i = np.arange(counts[e])
         mt[offsets[e] + i] = tile_base[e] + i // 128
         r[offsets[e] + i] = i % 128
-    b = np.arange(cols // 32)
-    byte = (((mt[:, None] * k_tiles + b[None, :] // 8) * 2 + (b[None, :] // 4) % 2) * 128 + r[:, None]) * 4 + b[None, :] % 4
+    b = np.arange(cols // block)
+    byte = (((mt[:, None] * k_tiles + b[None, :] // (4 * words)) * words + (b[None, :] // 4) % words) * 128
+            + r[:, None]) * 4 + b[None, :] % 4
     return raw[byte]
 
 
@@ -407,9 +410,13 @@ def check_nvfp4_moe_run(mx, d, tokens=None) -> dict:
     # 1. first quantisation, bit-exact
     xq_ref, xs_ref = oracle.nvfp4_quantize(inp.x[tok], inp.x_global)
     xq_all = _ws_view(d.ws, L["xq"], R, H // 2)
-    xs_all = _ws_view(d.ws, L["xs"], R, H // 16)
     hq_all = _ws_view(d.ws, L["hq"], R, I // 2)
-    hs_all = _ws_view(d.ws, L["hs"], R, I // 16)
+    if routed:   # the routed NVFP4 forward keeps them stage-major
+        xs_all = _ws_scales_stage_major(d.ws, L, L["xs"], R, H, routed, E, T, block=16)
+        hs_all = _ws_scales_stage_major(d.ws, L, L["hs"], R, I, routed, E, T, block=16)
+    else:
+        xs_all = _ws_view(d.ws, L["xs"], R, H // 16)
+        hs_all = _ws_view(d.ws, L["hs"], R, I // 16)
     y_all = _ws_view(d.ws, L["y"], R, H, "bf16") if routed else None
     for j in range(ids.shape[1]):
         live = (ids[:, j] >= 0) & (ids[:, j] < E)
