@@ -275,17 +275,34 @@ __device__ __forceinline__ void combine_groups(const uint4* __restrict__ y8, con
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int k = 0; k < K; ++k) {
-            const int32_t r = kFresh ? __ldcg(row_of + t * K + k) : __ldg(row_of + t * K + k);
-            if (r < 0) continue;
-            const float wk = __ldg(w + t * K + k);
-            const uint4 yv = kFresh ? __ldcg(y8 + (int64_t)r * groups_per_row + c)
-                                    : __ldg(y8 + (int64_t)r * groups_per_row + c);
-            const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+        // eight slots at a time: every row index, then every y load, are issued before the
+        // first sum, so the slots' DRAM reads overlap; the sums still run in slot order
+        for (int k0 = 0; k0 < K; k0 += 8) {
+            int32_t r[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wk, bf16_to_f32(yw[i] & 0xFFFFu)));
-                acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wk, bf16_to_f32(yw[i] >> 16)));
+            for (int j = 0; j < 8; ++j)
+                r[j] = k0 + j < K ? (kFresh ? __ldcg(row_of + t * K + k0 + j) : __ldg(row_of + t * K + k0 + j)) : -1;
+            uint4 yv[8];
+            float wk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                yv[j] = make_uint4(0u, 0u, 0u, 0u);
+                wk[j] = 0.0f;
+                if (r[j] >= 0) {
+                    wk[j] = __ldg(w + t * K + k0 + j);
+                    yv[j] = kFresh ? __ldcg(y8 + (int64_t)r[j] * groups_per_row + c)
+                                   : __ldg(y8 + (int64_t)r[j] * groups_per_row + c);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (r[j] < 0) continue;
+                const uint32_t yw[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(wk[j], bf16_to_f32(yw[i] & 0xFFFFu)));
+                    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(wk[j], bf16_to_f32(yw[i] >> 16)));
+                }
             }
         }
         out8[g] = make_uint4(f32_to_bf16(acc[0]) | (f32_to_bf16(acc[1]) << 16),
