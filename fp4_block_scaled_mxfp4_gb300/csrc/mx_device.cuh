@@ -52,7 +52,13 @@ __device__ __forceinline__ uint32_t f32_to_bf16(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-__device__ __forceinline__ float round_bf16(float f) { return bf16_to_f32(f32_to_bf16(f)); }
+// Two values to packed BF16 (lo in the low half), round to nearest even by the hardware
+// conversion; a NaN becomes the positive 0x7FFF.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 
 // Two values to packed BF16 (a in the low half), round to nearest even; the hardware
 // conversion, with NaN written as sign | 0x7FC0 like f32_to_bf16.

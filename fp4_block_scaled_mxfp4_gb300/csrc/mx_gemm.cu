@@ -561,11 +561,28 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
             }
             return a;
         };
-        // L1's h = bf16(silu(bf16(g)) * bf16(u)) from the gate and up accumulator words
-        auto h_value = [&](uint32_t acc_g, uint32_t acc_u) {
-            const float g = round_bf16(kNv ? __fmul_rn(__uint_as_float(acc_g), alpha_a) : __uint_as_float(acc_g));
-            const float u = round_bf16(kNv ? __fmul_rn(__uint_as_float(acc_u), alpha_b) : __uint_as_float(acc_u));
-            return round_bf16(silu_f32(g) * u);
+        // L1's h = bf16(silu(bf16(g)) * bf16(u)) for the 32 columns of one block, from the gate
+        // and up accumulator words. Every BF16 rounding is done two values at a time by the
+        // packed conversion (nearest even), which writes any NaN as a positive NaN: a NaN h is
+        // re-quantised with sign 0, whatever produced it (a NaN g or u, silu(-inf), 0 * inf).
+        auto h_block = [&](const uint32_t (&vg)[32], const uint32_t (&vu)[32], float (&h)[32]) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float g0 = __uint_as_float(vg[i]), g1 = __uint_as_float(vg[i + 1]);
+                float u0 = __uint_as_float(vu[i]), u1 = __uint_as_float(vu[i + 1]);
+                if (kNv) {
+                    g0 = __fmul_rn(g0, alpha_a);
+                    g1 = __fmul_rn(g1, alpha_a);
+                    u0 = __fmul_rn(u0, alpha_b);
+                    u1 = __fmul_rn(u1, alpha_b);
+                }
+                const uint32_t gp = bf16x2_rn(g0, g1), up = bf16x2_rn(u0, u1);
+                const float s0 = silu_f32(__uint_as_float(gp << 16));
+                const float s1 = silu_f32(__uint_as_float(gp & 0xFFFF0000u));
+                const uint32_t hp = bf16x2_rn(s0 * __uint_as_float(up << 16), s1 * __uint_as_float(up & 0xFFFF0000u));
+                h[i] = __uint_as_float(hp << 16);
+                h[i + 1] = __uint_as_float(hp & 0xFFFF0000u);
+            }
         };
         // Byte of h's MXFP4 scale for block b (32 columns) of global row grow, tile row r of M
         // tile mt: stage-major (hs_k_tiles > 0) or row-major
@@ -662,8 +679,7 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
 #pragma unroll
                 for (int b = 0; b < kHB; ++b) {
                     float h[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) h[i] = h_value(v[b][i], v[2 + b][i]);
+                    h_block(v[b], v[2 + b], h);
                     uint4 c8[2];
                     es[b] = mx8_quant32(h, c8);
                     if (lane == 0) bulk_wait_read();   // the previous store has read the block
@@ -695,8 +711,7 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
 #pragma unroll
                 for (int b = 0; b < kHB; ++b) {
                     float h[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) h[i] = h_value(v[b][i], v[2 + b][i]);
+                    h_block(v[b], v[2 + b], h);
                     es[b] = requant32(h, cds[b]);
                 }
                 if (lane == 0) bulk_wait_read();   // the previous store has read the block
@@ -726,8 +741,7 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
 #pragma unroll
                 for (int b = 0; b < kHB; ++b) {
                     float h[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) h[i] = h_value(v[b][i], v[2 + b][i]);
+                    h_block(v[b], v[2 + b], h);
                     const int64_t col = (int64_t)nt * (kN / 2) + (kN / 4) * hf + 32 * b;   // column of h
                     if constexpr (kA8) {
                         uint4 c8[2];

@@ -327,6 +327,8 @@ int moe_mxfp4_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64
  *     y    = bf16( hq . w2[e]^T )
  *   out[t] = bf16( sum_k topk_w[t, k] * y(t, k) )   (float32, slot order k = 0..K-1)
  *   An id outside [0, E) (e.g. -1) contributes nothing; a token with no valid id gets 0.
+ *   A NaN in h (a NaN g or u, silu(-inf), 0 * inf) is re-quantised as a positive NaN: its
+ *   block's scale byte is 255 and its code 7.
  *   Shared-expert mode: topk_ids == NULL and topk_w == NULL, E must be 1, K is ignored,
  *   out = y.
  *   x uint16 [T, H]; topk_ids int32 [T, K]; topk_w float32 [T, K];

@@ -95,6 +95,11 @@ R19 The warm-up-based activation global ([GS]'s "warmup-based gs"; the pages giv
     formula): the largest finite |x| over the calibration batches, divided by 6 * 448 (the
     largest NVFP4 magnitude) in one float32 division, clamped into R15's range. NaN and
     infinities are skipped (a non-finite input would leave no usable global).
+R20 A NaN in h (from a NaN g or u, from SiLU(-inf) = -inf / inf, or from 0 * inf) is the
+    positive quiet NaN 0x7FC0, so the re-quant codes it sign 0 (E2M1 code 7, E4M3 0x7F).
+    Float arithmetic gives a NaN it generates no defined sign, and the pages cover no
+    non-finite values; R7's "sign of the element" applies where the inputs define that
+    sign (the dequants).
 
 Parity status: every function below is pinned by the ``-m "not gpu"`` tests (tables from
 the OCP MX definitions and torch's float8 conversions, one-hot nibble/scale tests, the
@@ -507,11 +512,13 @@ def moe_l1_exact(xq_vals, w13_e, s13_e, I: int):
 
 
 def swiglu_bf16(g, u):
-    """h = bf16( silu(bf16(g)) * bf16(u) ) from exact g, u (R3); BF16 bits [n, I]."""
+    """h = bf16( silu(bf16(g)) * bf16(u) ) from exact g, u (R3); BF16 bits [n, I]. A NaN
+    h is the positive 0x7FC0 (R20)."""
     gb = bf16_bits_to_f64(bf16_bits_from_f64(g))
     ub = bf16_bits_to_f64(bf16_bits_from_f64(u))
-    with np.errstate(over="ignore"):
-        return bf16_bits_from_f64(_silu(gb) * ub)
+    with np.errstate(over="ignore", invalid="ignore"):
+        h = _silu(gb) * ub
+    return bf16_bits_from_f64(h, nan_sign=np.zeros(h.shape, dtype=bool))
 
 
 def moe_l2_bf16(hq, hs, w2_e, s2_e):

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 from gpu_util import assert_moe_close, bf16_host, dev, guarded_empty, native
-from moe_check import check_moe_run, tile_edge_tokens
+from moe_check import _ws_scales_stage_major, _ws_view, check_moe_run, tile_edge_tokens
 from workloads import make_config_inputs, make_moe_inputs
 
 pytestmark = pytest.mark.gpu
@@ -179,3 +179,37 @@ def test_prefill_config_sampled(mx):
     assert tokens.size >= 64
     print("prefill", check_moe_run(mx, d, tokens=tokens))
     np.testing.assert_array_equal(d.run(mx), got)
+
+
+@pytest.mark.parametrize("routed", [False, True])
+def test_nan_tokens_requantise_h_as_positive_nan(mx, routed):
+    """A token whose x holds a NaN (one of each sign) gets a NaN scale byte for that block,
+    so every g and u of its rows is NaN. Reading R20: its h re-quantises as the positive NaN
+    (scale 255, every code 7, so each byte 0x77), in full 32-row warps and in a ragged tile's
+    last warp alike, and its output row is NaN. Every other token is unaffected and within
+    the benchmark spec's bound."""
+    if routed:
+        inp = make_moe_inputs(T=200, H=256, I=256, E=3, K=2, seed=131, routing="uniform")
+        inp.topk_ids[:, 0] = 0                          # expert 0: 200 rows, a ragged second tile
+    else:
+        inp = make_moe_inputs(T=200, H=256, I=256, E=1, K=1, seed=132, routing=None)
+    bad = [5, 195]                                      # a full warp (rows 0-31) and a ragged one
+    inp.x[5, 10] = 0xFFC0                               # -NaN
+    inp.x[195, 40] = 0x7FC0                             # +NaN
+    d = Dev(mx, inp)
+    got = d.run(mx)
+    T, H, I, E, K = inp.T, inp.H, inp.I, inp.E, inp.K
+    L = mx.moe_mxfp4_workspace_layout(T, H, I, E, K, routed)
+    R = T * K if routed else T
+    hq = _ws_view(d.ws, L["hq"], R, I // 2)
+    hs = _ws_scales_stage_major(d.ws, L, L["hs"], R, I, True, E, T) if routed else _ws_view(d.ws, L["hs"], R, I // 32)
+    rows = _ws_view(d.ws, L["row_of"], T, K, "i32")[bad].ravel() if routed else np.array(bad)
+    assert (hq[rows] == 0x77).all() and (hs[rows] == 255).all()
+    # the oracle's h for those tokens is the same positive NaN block
+    g = np.full((1, I), np.nan)
+    ref_q, ref_s = oracle.act_quant_mxfp4(oracle.swiglu_bf16(g, g))
+    assert (ref_q == 0x77).all() and (ref_s == 255).all()
+    assert np.isnan((got[bad].astype(np.uint32) << 16).view(np.float32)).all()
+    good = np.setdiff1d(np.arange(T), bad)
+    assert_moe_close(got[good], _oracle(inp, tokens=good), f"tokens beside the NaN ones, routed={routed}")
+

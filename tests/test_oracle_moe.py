@@ -217,3 +217,26 @@ def test_weight_linearity_and_slot_pairing():
     ids = inp.topk_ids.copy()
     ids[:, 1] = -1
     np.testing.assert_array_equal(_run(inp, w=w), _run(inp, ids=ids))
+
+
+def test_nan_in_h_is_positive_and_requantises_to_code_7():
+    """Reading R20: every way the SwiGLU step makes a NaN -- a NaN g or u of either sign,
+    SiLU(-inf) = -inf / inf, 0 * inf, inf * 0 -- gives h = 0x7FC0 (sign clear), and the MX
+    re-quant of a block holding it is scale 255 with code 7 there. Finite and infinite h keep
+    their signs (R7 is untouched where the inputs define the sign)."""
+    from oracle import act_quant_mxfp4, swiglu_bf16
+    nan = np.float64("nan")
+    g = np.array([[nan, -nan, -np.inf, 0.0, np.inf, 1.0, np.inf, 2.0, -3.0]])
+    u = np.array([[1.0, 1.0, 1.0, np.inf, 0.0, -nan, -1.0, -3.0, 0.5]])
+    h = swiglu_bf16(g, u)
+    assert (h[0, :6] == 0x7FC0).all()
+    assert h[0, 6] == 0xFF80                               # silu(inf) * -1 = -inf
+    # silu(2) * -3 and silu(-3) * 0.5: finite, sign of the product, nearest-even BF16
+    for i, (gi, ui) in enumerate([(2.0, -3.0), (-3.0, 0.5)], start=7):
+        want = bf16_bits_from_f64(gi / (1.0 + math.exp(-gi)) * ui)
+        assert h[0, i] == want and (h[0, i] >> 15) == 1
+    block = np.concatenate([h[:, :1], np.full((1, 31), bf16_bits_from_f64(np.array(-1.5)), np.uint16)], axis=1)
+    q, s = act_quant_mxfp4(block)
+    assert s[0, 0] == 255
+    assert q[0, 0] & 0x0F == 0x7                           # element 0: the positive NaN
+    assert (q[0, 0] >> 4) == 0xF and (q[0, 1:] == 0xFF).all()   # the rest: sign | 7
