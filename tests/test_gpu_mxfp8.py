@@ -16,8 +16,8 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import assert_gemm_close, bf16_host, dev, guarded_empty, native
-from moe_check import check_moe_run, tile_edge_tokens
+from gpu_util import assert_gemm_close, assert_moe_close, bf16_host, dev, guarded_empty, native
+from moe_check import _ws_view, check_moe_run, tile_edge_tokens
 from workloads import f32_to_bf16_bits, make_config_inputs, make_moe_inputs
 
 pytestmark = pytest.mark.gpu
@@ -236,3 +236,29 @@ def test_mxfp8_graph_replay_bit_identical(mx):
     g.replay()
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bf16_host(d.out), eager)
+
+
+def test_mxfp8_nan_tokens_requantise_h_as_positive_nan(mx):
+    """Reading R20 in the MXFP8 re-quant: a token whose x holds a NaN (one of each sign) has
+    NaN g and u, and its h re-quantises as the positive NaN: scale 255, every E4M3 code 0x7F,
+    in a full 32-row warp and in a ragged tile's last warp. Its output row is NaN; every
+    other token is within the per-element bound."""
+    inp = make_moe_inputs(T=200, H=256, I=256, E=1, K=1, seed=133, routing=None)
+    bad = [5, 195]
+    inp.x[5, 10] = 0xFFC0
+    inp.x[195, 40] = 0x7FC0
+    d = Dev8(mx, inp)
+    got = d.run(mx)
+    T, H, I = inp.T, inp.H, inp.I
+    L = mx.moe_mxfp4w_mxfp8a_workspace_layout(T, H, I, 1, 1, False)
+    hq = _ws_view(d.ws, L["hq"], T, I)
+    hs = _ws_view(d.ws, L["hs"], T, I // 32)
+    assert (hq[bad] == 0x7F).all() and (hs[bad] == 255).all()
+    g = np.full((1, I), np.nan)
+    ref_q, ref_s = oracle.act_quant_mxfp8(oracle.swiglu_bf16(g, g))
+    assert (ref_q == 0x7F).all() and (ref_s == 255).all()
+    assert np.isnan((got[bad].astype(np.uint32) << 16).view(np.float32)).all()
+    good = np.setdiff1d(np.arange(T), bad)
+    ref = oracle.moe_mxfp8_forward(inp.x, None, None, inp.w13, inp.s13, inp.w2, inp.s2, inp.I, tokens=good)
+    assert_moe_close(got[good], ref, "MXFP8 tokens beside the NaN ones")
+
