@@ -644,10 +644,22 @@ __device__ __forceinline__ void gemm_run(const CUtensorMap& tmA, const CUtensorM
                     const int64_t col = (int64_t)nt * kN + (kN / 2) * hf + 32 * i;
                     if (col >= args.n_valid) break;
                     const float al[2] = {col_alpha(col), col_alpha(col + 16)};
+                    // the packed conversion writes a NaN as 0x7FFF; one test per piece finds it (a
+                    // BF16 magnitude above 0x7F80 carries into bit 15 when 0x7F is added), and
+                    // only such a piece is converted again with the NaN written as sign | 0x7FC0
                     uint32_t p[16];
+                    uint32_t nan_bits = 0;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        p[j] = pack_bf16x2(out_value(v[i][2 * j], al[j >> 3]), out_value(v[i][2 * j + 1], al[j >> 3]));
+                    for (int j = 0; j < 16; ++j) {
+                        p[j] = bf16x2_rn(out_value(v[i][2 * j], al[j >> 3]), out_value(v[i][2 * j + 1], al[j >> 3]));
+                        nan_bits |= ((p[j] & 0x7FFF7FFFu) + 0x007F007Fu) & 0x80008000u;
+                    }
+                    if (__builtin_expect(nan_bits != 0u, 0)) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            p[j] = pack_bf16x2(out_value(v[i][2 * j], al[j >> 3]),
+                                               out_value(v[i][2 * j + 1], al[j >> 3]));
+                    }
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {       // 16 columns (32 bytes) per row and store
                         if (col + 16 * c >= args.n_valid) break;

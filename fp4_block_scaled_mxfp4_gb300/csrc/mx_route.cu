@@ -3,7 +3,8 @@
 // pipeline plus routing, top-k and scatter).
 //
 // The routed (token, slot) pairs are grouped by expert in a stable order: expert, then
-// token, then slot. Three launches, no host synchronisation (graph-capturable):
+// token, then slot. Three launches (two when all pairs fit in one chunk, whose count and
+// scan then share one CTA), no host synchronisation (graph-capturable):
 //   1. route_count: per chunk of 2048 pairs, per-expert counts and each pair's rank among
 //      the earlier pairs of its expert inside the chunk (warp match + a per-warp scan);
 //   2. route_scan (one CTA): per-expert prefix over chunks, expert offsets, and the list of
@@ -38,6 +39,24 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
     pdl_launch_dependents();
 }
 
+// All pairs in one chunk (decode-sized batches): both routing steps in one CTA, one launch
+// fewer. The count's scratch is reused by the scan once the count is done.
+constexpr int kSmallRouteThreads = 1024;
+constexpr int kSmallRouteSmemInts = (1 + kCountWarps) * kMaxExperts > 3 * kMaxExperts + 2
+                                        ? (1 + kCountWarps) * kMaxExperts
+                                        : 3 * kMaxExperts + 2;
+__global__ void __launch_bounds__(kSmallRouteThreads) route_small_kernel(const int32_t* __restrict__ ids,
+                                                                         int64_t n_pairs, int E, RouteBufs rb,
+                                                                         uint32_t* clear_word) {
+    __shared__ int32_t s_buf[kSmallRouteSmemInts];
+    pdl_wait();
+    if (clear_word != nullptr && threadIdx.x == 0) *clear_word = 0u;
+    route_count_chunk(ids, n_pairs, E, 0, rb.chunk_counts, rb.local_rank, s_buf, s_buf + E, threadIdx.x);
+    __syncthreads();   // the chunk's counts (global) are read by other threads of the CTA below
+    route_scan(rb.chunk_counts, 1, E, rb, s_buf, s_buf + E, s_buf + 2 * E + 1, threadIdx.x, blockDim.x);
+    pdl_launch_dependents();
+}
+
 constexpr int kGatherThreads = 256;
 
 // One CTA per token (quant_gather_token).
@@ -58,6 +77,9 @@ cudaError_t launch_route(const int32_t* ids, int64_t T, int64_t K, int64_t E, co
                          cudaStream_t s, uint32_t* clear_word) {
     const int64_t n = T * K;
     if (n == 0) return cudaSuccess;
+    if (rb.nchunks == 1)
+        return launch_pdl(route_small_kernel, dim3(1), dim3(kSmallRouteThreads), 0, s, ids, n, (int)E, rb,
+                          clear_word);
     const cudaError_t err = launch_pdl(route_count_kernel, dim3((unsigned)rb.nchunks), dim3(kCountThreads), 0, s, ids,
                                        n, (int)E, rb.chunk_counts, rb.local_rank, clear_word);
     if (err != cudaSuccess) return err;
