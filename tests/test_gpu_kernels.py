@@ -294,7 +294,10 @@ def test_nvfp4_gemm_scale_words_one_hot(mx):
 
 # ----------------------------------------------------------------------------- routing
 
-@pytest.mark.parametrize("T,K,E", [(1, 1, 1), (100, 4, 5), (3000, 8, 48), (8192, 8, 48), (513, 6, 300)])
+# one chunk of at most 2048 pairs (routed in one CTA: 1, 400, exactly 2048 and 2046 pairs, the
+# last with the largest E) and several chunks
+@pytest.mark.parametrize("T,K,E", [(1, 1, 1), (100, 4, 5), (256, 8, 48), (341, 6, 1024), (3000, 8, 48),
+                                   (8192, 8, 48), (513, 6, 300)])
 def test_route_bit_exact(mx, T, K, E):
     import torch
     rng = np.random.default_rng(T + K + E)
