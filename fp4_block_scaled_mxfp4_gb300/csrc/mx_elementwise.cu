@@ -148,11 +148,9 @@ __device__ __forceinline__ void nvfp4_block_to_bf16(uint2 c, uint32_t sbyte, flo
     uint32_t t[4];
     const float m[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
     if (isfinite(sa) && isfinite(ga)) {
-        // finite factors: every product is finite or infinite, never NaN, so the packed
-        // conversion needs no NaN fix-up
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            t[k] = bf16x2_rn(__fmul_rn(__fmul_rn(m[2 * k], sa), ga), __fmul_rn(__fmul_rn(m[2 * k + 1], sa), ga));
+            t[k] = pack_bf16x2(__fmul_rn(__fmul_rn(m[2 * k], sa), ga), __fmul_rn(__fmul_rn(m[2 * k + 1], sa), ga));
     } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {

@@ -91,7 +91,8 @@ def test_nvfp4_dequant_full_size_sampled(mx):
     np.testing.assert_array_equal(got, oracle.nvfp4_dequant(w13[rows], n13[rows], g))
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 16), (130, 272), (300, 1040)])
+# units of 16 columns per row: 1, 17, 65, a power of two (32) and 3 over many block rows
+@pytest.mark.parametrize("rows,cols", [(1, 16), (130, 272), (300, 1040), (257, 512), (2049, 48)])
 def test_fp8_dequant_bit_exact(mx, rows, cols):
     import torch
     rng = np.random.default_rng(rows + cols)
